@@ -1,0 +1,346 @@
+#!/usr/bin/env python
+"""Throughput of the Qwen3-style speech decoder on GB300: decode tok/s and
+prefill tok/s, with the roofline fraction of the dominant kernel.
+
+One bench step is one utterance of the workload: a prefill over the
+audio-injected prompt, then the greedy step loop (all rows of the hot path).
+Inputs (token ids and encoder rows) are resident in HBM before the timed
+region; every step streams the full 3.4 GB of weights, far more than the
+129 MB L2, so no step is served from cache.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the
+decoder has no data-path exchange); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speech_decoder_gb300 import synth  # noqa: E402
+
+METRIC = "decode tok/s & prefill tok/s (Qwen3-1.7B shape, 1 GB300); % HBM/TC roofline"
+DEFAULT_WORKLOAD = "qwen3-1.7b-t152"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- environment
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        hbm = d.get("hbm_gbs") or d.get("hbm_GBps") or d.get("hbm")
+        bf16 = d.get("bf16_tflops_sustained") or d.get("bf16_tflops")
+        if hbm:
+            return float(hbm), float(bf16) if bf16 else 1714.0, "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(prefix="clocks_", suffix=".csv")
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for row in csv.reader(f):
+                if len(row) < 9:
+                    continue
+                try:
+                    sm.append(float(row[1]))
+                    mx.append(float(row[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, row[5:9]):
+                    if v.strip().lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("decode.cu", "decode.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "speech_decoder_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """Per-launch DRAM bytes of the dominant kernel from the committed ncu
+    summary, or None when the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "gemv_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_sha") != kernel_sha():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- workload
+def workload_inputs(wl, w):
+    items = []
+    for i, pr in enumerate(wl.prompts):
+        items.append(synth.prompt_inputs(wl.model, pr, seed=wl.seed, item=i))
+    return items
+
+
+def decode_bytes_per_step(spec, kv_len_mean: float) -> float:
+    """Algorithmic HBM bytes of one decode step of one sequence: every weight
+    once (bf16) plus the K and V rows read by attention (fp16)."""
+    H, F, d, nq, nkv, L = spec.hidden, spec.ffn, spec.head_dim, spec.n_heads, spec.n_kv_heads, spec.n_layers
+    per_layer = ((nq + 2 * nkv) * d * H + H * nq * d + 2 * F * H + H * F) * 2
+    return L * per_layer + spec.vocab * H * 2 + L * 2 * nkv * d * 2 * kv_len_mean
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = f"cuda:{local}"
+    torch.cuda.set_device(dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from speech_decoder_gb300.binding import Decoder
+
+    wl = synth.workload(args.workload)
+    spec = wl.model
+    if wl.batch != 1:
+        raise SystemExit(f"workload {wl.name}: batched bench path not built")
+    w = synth.model_weights(spec, seed=wl.seed)
+    item = workload_inputs(wl, w)[0]
+    pr = wl.prompts[0]
+    T = pr.T
+    max_new = wl.steps + 1                      # the prefill's token counts toward the budget
+    dec = Decoder(spec, w, max_ctx=T + max_new, max_new=max_new, eos_id=wl.eos_id, device=dev)
+    del w
+    stream = dec.stream
+    ids_dev = torch.from_numpy(item["ids"]).to(dev)
+    audio_dev = torch.from_numpy(item["audio"]).to(dev)
+
+    def utterance(ids, audio):
+        dec.prefill_ids(ids, audio, item["prefix_len"])
+        out, _ = dec.generate(max_new)
+        return out
+
+    for _ in range(args.warmup):
+        utterance(ids_dev, audio_dev)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = Clocks(local) if rank == 0 else None
+    n0 = dec.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    pre_ms, gen_ms, n_tok = 0.0, 0.0, 0
+    e0.record(stream)
+    for _ in range(args.steps):
+        out = utterance(ids_dev, audio_dev)
+        p, g = dec.timings()
+        pre_ms += p
+        gen_ms += g
+        n_tok += len(out) - 1
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    launches = dec.launch_count() - n0
+    clk = clocks.stop() if clocks else None
+    total_ms = e0.elapsed_time(e1)
+    vals = torch.tensor([total_ms, gen_ms, pre_ms], dtype=torch.float64, device=dev)
+    toks = torch.tensor([n_tok, args.steps * T], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(toks, op=torch.distributed.ReduceOp.SUM)
+    total_ms, gen_ms, pre_ms = vals.tolist()
+    n_tok_all, n_pre_all = toks.tolist()
+    decode_tok_s = n_tok_all / (gen_ms / 1e3)
+    prefill_tok_s = n_pre_all / (pre_ms / 1e3)
+
+    # dominant kernel: the RMSNorm + projection GEMV (q|k|v and gate|up), timed alone
+    hbm, bf16_peak, peak_kind = peaks()
+    dec.prefill_ids(ids_dev, audio_dev, item["prefix_len"])
+    kms, kbytes = dec.profile_kernel(0, 10)
+    achieved = kbytes / (kms / 1e3) / 1e9
+    roof = {"kernel": "k_gemv<bf16, IN_NORM, OUT_STORE> (q|k|v and gate|up)", "bound": "hbm",
+            "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+            "peak_source": peak_kind, "bytes_per_launch": int(kbytes), "avg_launch_us": round(kms * 1e3, 2),
+            "traffic": ncu_traffic()}
+    step_bytes = decode_bytes_per_step(spec, T + wl.steps / 2)
+    step_ms = gen_ms / max(1, n_tok) if world == 1 else gen_ms / max(1, n_tok_all / world)
+    step_roof = {"bytes_per_step": int(step_bytes), "achieved": round(step_bytes / (step_ms / 1e3) / 1e9, 1),
+                 "frac": round(step_bytes / (step_ms / 1e3) / 1e9 / hbm, 4)}
+
+    e2e = None
+    if not args.no_e2e:
+        ids_h = torch.from_numpy(item["ids"]).pin_memory()
+        audio_h = torch.from_numpy(item["audio"]).pin_memory()
+        utterance(ids_h, audio_h)
+        torch.cuda.synchronize()
+        t_pre, t_gen, n_e = 0.0, 0.0, 0
+        reps = max(1, args.steps)
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            dec.prefill_ids(ids_h, audio_h, item["prefix_len"])
+            t1 = time.perf_counter()
+            out, _ = dec.generate(max_new)
+            t2 = time.perf_counter()
+            t_pre += t1 - t0
+            t_gen += t2 - t1
+            n_e += len(out) - 1
+        e2e = {"value": round(n_e * world / t_gen, 1), "unit": "tok/s",
+               "prefill_tok_s": round(reps * T * world / t_pre, 1),
+               "h2d_bytes_per_step": int(ids_h.numel() * 4 + audio_h.numel() * 4),
+               "d2h_bytes_per_step": int(4 + 4 * max_new)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, sample_steps=3)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(decode_tok_s, 1), "unit": "tok/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded random-init weights N(0,0.02), encoder rows N(0,1))",
+            "config": {"workload": wl.name, "prompt_rows": T, "layout": [pr.prefix_len, pr.n_audio, pr.suffix_len],
+                       "decode_steps": wl.steps, "batch": wl.batch, "parallelism": f"replicas x{world}",
+                       "l2": "inputs larger than L2: every step streams 3.4 GB of weights"},
+            "prefill": {"value": round(prefill_tok_s, 1), "unit": "tok/s", "ms": round(pre_ms / args.steps, 3)},
+            "decode_ms_per_token": round(gen_ms / max(1, n_tok), 4),
+            "roofline": roof, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clk, "gpu_launches": int(launches),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# ---------------------------------------------------------------- oracle timings
+def cpu_baseline(wl, sample_steps=3, rows=8):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload:
+    a prefill of the first `rows` prompt rows, then `sample_steps` greedy
+    steps of the full model.  Decode tok/s = steps / their time."""
+    import oracle as O
+    spec = wl.model
+    w = synth.model_weights(spec, seed=wl.seed)
+    item = synth.prompt_inputs(spec, wl.prompts[0], seed=wl.seed, item=0)
+    emb = O.assemble_prompt(w["embed"], item["ids"], item["audio"], item["prefix_len"])[:rows]
+    orc = O.Oracle(spec, w, rows + sample_steps + 1)
+    t0 = time.perf_counter()
+    logits = orc.prefill(emb)
+    t1 = time.perf_counter()
+    tok = O.argmax_lowest(logits)
+    for _ in range(sample_steps):
+        tok = O.argmax_lowest(orc.step(tok))
+    t2 = time.perf_counter()
+    return {"value": round(sample_steps / (t2 - t1), 4), "unit": "tok/s", "cores": os.cpu_count(),
+            "kind": "oracle", "prefill_tok_s": round(rows / (t1 - t0), 3),
+            "sample": f"{wl.name}: prefill of the first {rows} prompt rows, then {sample_steps} greedy steps of "
+                      f"all {spec.n_layers} layers (numpy fp64, BLAS on all host cores)"}
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return
+    import oracle as O
+    wl = synth.workload(args.workload)
+    spec = wl.model
+    w = synth.model_weights(spec, seed=wl.seed)
+    item = synth.prompt_inputs(spec, wl.prompts[0], seed=wl.seed, item=0)
+    rows = 8
+    emb = O.assemble_prompt(w["embed"], item["ids"], item["audio"], item["prefix_len"])[:rows]
+    orc = O.Oracle(spec, w, rows + args.warmup + args.steps + 1)
+    tok = O.argmax_lowest(orc.prefill(emb))
+    for _ in range(args.warmup):
+        tok = O.argmax_lowest(orc.step(tok))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        tok = O.argmax_lowest(orc.step(tok))
+    dt = time.perf_counter() - t0
+    v = args.steps / dt
+    sample = (f"{wl.name}: each step is one greedy decode step of all {spec.n_layers} layers after an untimed "
+              f"{rows}-row prefill (numpy fp64 oracle, BLAS on all host cores)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "tok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "prompt_rows": wl.prompts[0].T, "decode_steps": wl.steps},
+        "cpu_baseline": {"value": round(v, 4), "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(v, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)

@@ -1,0 +1,947 @@
+// C ABI and runtime of the decoder: workspace layout, weight packing, the
+// prefill sequence, the captured step graph, and the device-side greedy loop.
+//
+// Sources: qwen3_asr/decoder.cpp (transcribe-cpp-sys 0.2.0) build_prefill_graph,
+// build_step_graph, build_*_batched; qwen3_asr/model.cpp run / run_batch
+// (input-length gate, KV sizing, greedy loop, truncation, EOS strip).
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "dec.h"
+#include "decode.cuh"
+#include "gemm_tc.cuh"
+#include "prefill.cuh"
+
+using namespace dec;
+
+namespace {
+
+struct DevLayer {
+    void *wqkv = nullptr, *wo = nullptr, *wgu = nullptr, *wd = nullptr;
+    float *attn_norm = nullptr, *ffn_norm = nullptr, *qn = nullptr, *kn = nullptr;
+    void *K = nullptr, *V = nullptr;
+};
+
+struct Bump {
+    char *base;
+    size_t off = 0;
+    template <typename T> T *take(size_t count) {
+        off = (off + 255) & ~size_t(255);
+        T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+        off += count * sizeof(T);
+        return p;
+    }
+};
+
+constexpr int kGenChunk = 16;     // steps per captured generate graph
+constexpr int kMaxSplits = 32;    // split-KV partitions per (sequence, kv head)
+
+}  // namespace
+
+struct dec_handle {
+    dec_hparams hp{};
+    cudaStream_t stream = nullptr;
+    int num_sms = 0;
+    bool w_bf16 = true, kv_f16 = true, use_tc = true;
+    size_t slots = 0;
+    // weights
+    void *embed = nullptr;
+    float *final_norm = nullptr;
+    std::vector<DevLayer> L;
+    float2 *rope = nullptr;
+    // prefill activations
+    float *x = nullptr, *qkv = nullptr, *gu = nullptr;
+    void *xn = nullptr, *q16 = nullptr, *attn_o = nullptr, *hbuf = nullptr;
+    int32_t *row_pos = nullptr, *row_slot = nullptr, *last_row = nullptr, *ids_dev = nullptr;
+    // decode activations and scratch
+    float *xd = nullptr, *qkvd = nullptr, *od = nullptr, *gud = nullptr, *logits = nullptr;
+    float *attn_part = nullptr;
+    unsigned *attn_counter = nullptr;
+    float *am_val = nullptr;
+    int *am_idx = nullptr;
+    unsigned *am_counter = nullptr;
+    int lm_grid = 0;
+    int32_t *out_ids = nullptr;
+    SeqState *st = nullptr;
+    // dumps
+    float *dump_inj = nullptr, *dump_b0 = nullptr, *dump_blast = nullptr, *dump_final = nullptr;
+    bool dumps = false;
+    int dump_T = 0, dump_B = 0;
+    bool dump_b0_valid = false;
+    // host state
+    SeqState hst{};
+    int n_seq = 0;
+    bool prefilled = false;
+    int logits_rows = 0;
+    std::vector<int32_t> h_row_pos, h_row_slot, h_last_row;
+    // graphs
+    cudaGraphExec_t step_exec = nullptr;
+    int step_B = -1;
+    size_t step_nodes = 0;
+    cudaGraphExec_t gen_exec = nullptr;
+    int gen_B = -1;
+    size_t gen_nodes = 0;
+    int64_t launches = 0;
+    int64_t enq = 0;                // kernels enqueued by the current enqueue pass
+    std::string err;
+    cudaEvent_t ev[4] = {};
+    float prefill_ms = 0.f, gen_ms = 0.f;
+};
+
+// ------------------------------------------------------------------ helpers
+static dec_status fail(dec_handle *h, dec_status s, const std::string &msg) {
+    if (h) h->err = msg;
+    return s;
+}
+
+#define CK(call)                                                                                \
+    do {                                                                                        \
+        cudaError_t e_ = (call);                                                                \
+        if (e_ != cudaSuccess)                                                                  \
+            return fail(h, DEC_ERR_CUDA, std::string(#call " failed: ") + cudaGetErrorString(e_)); \
+    } while (0)
+
+static size_t wsize(const dec_hparams &hp) { return hp.weight_dtype == DEC_BF16 ? 2 : 4; }
+static size_t kvsize(const dec_hparams &hp) { return hp.kv_dtype == DEC_F16 ? 2 : 4; }
+static int qkv_rows(const dec_hparams &hp) { return (hp.n_heads + 2 * hp.n_kv_heads) * hp.head_dim; }
+
+static std::string validate(const dec_hparams *hp) {
+    if (!hp) return "hparams is NULL";
+    const dec_hparams &p = *hp;
+    if (p.n_layers < 1) return "n_layers must be >= 1";
+    if (p.hidden < 256 || p.hidden % 256) return "hidden must be a positive multiple of 256";
+    if (p.head_dim != 64 && p.head_dim != 128) return "head_dim must be 64 or 128";
+    if (p.n_kv_heads < 1 || p.n_heads < 1 || p.n_heads % p.n_kv_heads) return "n_heads must be a multiple of n_kv_heads";
+    if (p.n_heads / p.n_kv_heads > 8) return "at most 8 query heads per KV head";
+    if ((p.n_heads * p.head_dim) % 256) return "n_heads*head_dim must be a multiple of 256";
+    if (p.ffn < 128 || p.ffn % 128) return "ffn must be a positive multiple of 128";
+    if (p.vocab < 1) return "vocab must be >= 1";
+    if ((size_t)kGroupB * std::max({p.hidden, p.ffn, p.n_heads * p.head_dim}) * 4 > (size_t)kGemvMaxSmem)
+        return "hidden, ffn and n_heads*head_dim must be <= 12800";
+    if (!(p.rms_eps >= 0.f) || !(p.rope_theta > 0.f)) return "rms_eps must be >= 0 and rope_theta > 0";
+    if (p.max_batch < 1 || p.max_batch > kMaxBatch) return "max_batch must be in [1, 64]";
+    if (p.max_new < 1) return "max_new must be >= 1";
+    if (p.max_ctx < 2 || p.max_ctx <= p.max_new) return "max_ctx must exceed max_new";
+    if (p.max_tokens < 1) return "max_tokens must be >= 1";
+    if (p.eos_id < -1 || p.eos_id >= p.vocab) return "eos_id must be -1 or a vocabulary id";
+    const bool ok = (p.weight_dtype == DEC_BF16 && p.kv_dtype == DEC_F16) ||
+                    (p.weight_dtype == DEC_F32 && p.kv_dtype == DEC_F32);
+    if (!ok) return "supported formats: bf16 weights with f16 KV, or f32 weights with f32 KV";
+    return "";
+}
+
+static int splits_for(const dec_handle *h, int B) {
+    const int want = (2 * h->num_sms + B * h->hp.n_kv_heads - 1) / (B * h->hp.n_kv_heads);
+    return std::max(1, std::min(kMaxSplits, want));
+}
+
+// Assign every device buffer from the bump allocator (base == nullptr: size only).
+static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms) {
+    Bump b{base};
+    const size_t ws = wsize(hp), kvs = kvsize(hp), as = ws;   // activations use the weight format
+    const size_t H = hp.hidden, d = hp.head_dim, nq = hp.n_heads, nkv = hp.n_kv_heads, F = hp.ffn;
+    const size_t V = hp.vocab, Tm = hp.max_tokens, Bm = hp.max_batch;
+    const size_t slots = (size_t)hp.max_batch * hp.max_ctx;
+    h->slots = slots;
+    h->embed = b.take<char>(V * H * ws);
+    h->final_norm = b.take<float>(H);
+    h->L.assign(hp.n_layers, DevLayer{});
+    for (auto &l : h->L) {
+        l.wqkv = b.take<char>((size_t)qkv_rows(hp) * H * ws);
+        l.wo = b.take<char>(H * nq * d * ws);
+        l.wgu = b.take<char>(2 * F * H * ws);
+        l.wd = b.take<char>(H * F * ws);
+        l.attn_norm = b.take<float>(H);
+        l.ffn_norm = b.take<float>(H);
+        l.qn = b.take<float>(d);
+        l.kn = b.take<float>(d);
+        l.K = b.take<char>(nkv * slots * d * kvs);
+        l.V = b.take<char>(nkv * slots * d * kvs);
+    }
+    h->rope = b.take<float2>((size_t)hp.max_ctx * (d / 2));
+    h->x = b.take<float>(Tm * H);
+    h->xn = b.take<char>(Tm * std::max(H, F) * as);
+    h->qkv = b.take<float>(Tm * qkv_rows(hp));
+    h->q16 = b.take<char>(Tm * nq * d * kvs);
+    h->attn_o = b.take<char>(Tm * nq * d * as);
+    h->gu = b.take<float>(Tm * 2 * F);
+    h->hbuf = b.take<char>(Tm * F * as);
+    h->row_pos = b.take<int32_t>(Tm);
+    h->row_slot = b.take<int32_t>(Tm);
+    h->last_row = b.take<int32_t>(Bm);
+    h->ids_dev = b.take<int32_t>(Tm);
+    h->xd = b.take<float>(Bm * H);
+    h->qkvd = b.take<float>(Bm * qkv_rows(hp));
+    h->od = b.take<float>(Bm * nq * d);
+    h->gud = b.take<float>(Bm * 2 * F);
+    h->logits = b.take<float>(Bm * V);
+    h->attn_part = b.take<float>(Bm * nkv * kMaxSplits * (nq / nkv) * (d + 2));
+    h->attn_counter = b.take<unsigned>(Bm * nkv);
+    h->lm_grid = gemv_grid((int)V, num_sms);
+    h->am_val = b.take<float>(Bm * h->lm_grid);
+    h->am_idx = b.take<int>(Bm * h->lm_grid);
+    h->am_counter = b.take<unsigned>(64);
+    h->out_ids = b.take<int32_t>(Bm * hp.max_new);
+    h->st = b.take<SeqState>(1);
+    h->dump_inj = b.take<float>(Tm * H);
+    h->dump_b0 = b.take<float>(Tm * H);
+    h->dump_blast = b.take<float>(Bm * H);
+    h->dump_final = b.take<float>(Bm * H);
+    return b.off + 256;
+}
+
+// ------------------------------------------------------------------ enqueue passes
+static void gemm(dec_handle *h, const void *A, const void *W, float *C, int ldc, int M, int N, int K, int epi) {
+    if (h->use_tc && h->w_bf16 && gemm_tc_supported(M, N, K))
+        launch_gemm_tc(A, W, C, ldc, M, N, K, epi, h->stream);
+    else
+        launch_gemm_simt(A, h->w_bf16, W, h->w_bf16, C, ldc, M, N, K, epi, h->stream);
+    h->enq++;
+}
+
+// One decoder block for the step rows in xd (one row per sequence).
+static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
+    const dec_hparams &hp = h->hp;
+    const DevLayer &L = h->L[l];
+    const int H = hp.hidden, F = hp.ffn, nqd = hp.n_heads * hp.head_dim;
+    cudaStream_t s = h->stream;
+
+    GemvArgs g{};
+    g.st = h->st;
+    g.B = B;
+    g.eps = hp.rms_eps;
+    g.W = L.wqkv;
+    g.N = qkv_rows(hp);
+    g.K = H;
+    g.in = h->xd;
+    g.norm_w = L.attn_norm;
+    g.embed = h->embed;
+    g.x_resid = h->xd;
+    g.out = h->qkvd;
+    const bool emb = from_embed && l == 0;
+    launch_gemv(emb ? IN_EMBED_NORM : IN_NORM, OUT_STORE, h->w_bf16, g, gemv_grid(g.N, h->num_sms), s);
+
+    AttnDecArgs a{};
+    a.qkv = h->qkvd;
+    a.qn_w = L.qn;
+    a.kn_w = L.kn;
+    a.eps = hp.rms_eps;
+    a.rope = h->rope;
+    a.Kc = L.K;
+    a.Vc = L.V;
+    a.slots = (int)h->slots;
+    a.o = h->od;
+    a.part = h->attn_part;
+    a.counter = h->attn_counter;
+    a.st = h->st;
+    a.nq = hp.n_heads;
+    a.nkv = hp.n_kv_heads;
+    a.d = hp.head_dim;
+    a.B = B;
+    a.append = 1;
+    launch_attn_decode(h->kv_f16, a, splits_for(h, B), s);
+
+    GemvArgs o{};
+    o.st = h->st;
+    o.B = B;
+    o.eps = hp.rms_eps;
+    o.W = L.wo;
+    o.N = H;
+    o.K = nqd;
+    o.in = h->od;
+    o.out = h->xd;
+    launch_gemv(IN_PLAIN, OUT_RESID, h->w_bf16, o, gemv_grid(H, h->num_sms), s);
+
+    GemvArgs f1 = g;
+    f1.W = L.wgu;
+    f1.N = 2 * F;
+    f1.norm_w = L.ffn_norm;
+    f1.out = h->gud;
+    launch_gemv(IN_NORM, OUT_STORE, h->w_bf16, f1, gemv_grid(2 * F, h->num_sms), s);
+
+    GemvArgs f2{};
+    f2.st = h->st;
+    f2.B = B;
+    f2.W = L.wd;
+    f2.N = H;
+    f2.K = F;
+    f2.in = h->gud;
+    f2.ffn = F;
+    f2.out = h->xd;
+    launch_gemv(IN_SWIGLU, OUT_RESID, h->w_bf16, f2, gemv_grid(H, h->num_sms), s);
+    h->enq += 5;
+}
+
+static void enqueue_head(dec_handle *h, int B) {
+    GemvArgs g{};
+    g.st = h->st;
+    g.B = B;
+    g.eps = h->hp.rms_eps;
+    g.W = h->embed;
+    g.N = h->hp.vocab;
+    g.K = h->hp.hidden;
+    g.in = h->xd;
+    g.norm_w = h->final_norm;
+    g.out = h->logits;
+    g.part_val = h->am_val;
+    g.part_idx = h->am_idx;
+    g.counter = h->am_counter;
+    g.out_ids = h->out_ids;
+    g.out_ids_cap = h->hp.max_new;
+    launch_gemv(IN_NORM, OUT_ARGMAX, h->w_bf16, g, h->lm_grid, h->stream);
+    h->enq++;
+}
+
+static void enqueue_step(dec_handle *h, int B) {
+    for (int l = 0; l < h->hp.n_layers; ++l) enqueue_decode_layer(h, l, B, true);
+    enqueue_head(h, B);
+}
+
+static dec_status capture(dec_handle *h, int steps, int B, cudaGraphExec_t *exec, size_t *nodes) {
+    if (*exec) {
+        cudaGraphExecDestroy(*exec);
+        *exec = nullptr;
+    }
+    cudaGraph_t graph = nullptr;
+    CK(cudaStreamBeginCapture(h->stream, cudaStreamCaptureModeThreadLocal));
+    for (int i = 0; i < steps; ++i) enqueue_step(h, B);
+    CK(cudaStreamEndCapture(h->stream, &graph));
+    size_t n = 0;
+    CK(cudaGraphGetNodes(graph, nullptr, &n));
+    cudaError_t e = cudaGraphInstantiate(exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return fail(h, DEC_ERR_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(e));
+    *nodes = n;
+    return DEC_OK;
+}
+
+static dec_status sync_state(dec_handle *h) {
+    CK(cudaMemcpyAsync(&h->hst, h->st, sizeof(SeqState), cudaMemcpyDeviceToHost, h->stream));
+    CK(cudaStreamSynchronize(h->stream));
+    if (h->hst.error) return fail(h, DEC_ERR_DEVICE, "device reported error " + std::to_string(h->hst.error));
+    return DEC_OK;
+}
+
+// ------------------------------------------------------------------ prefill
+// Rows are already in h->x (sum T_b rows); cu has B + 1 offsets.
+static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t *first_tokens) {
+    const dec_hparams &hp = h->hp;
+    const int total = cu[B];
+    const int H = hp.hidden, F = hp.ffn, nqd = hp.n_heads * hp.head_dim;
+    cudaStream_t s = h->stream;
+    h->enq = 0;
+
+    h->h_row_pos.resize(total);
+    h->h_row_slot.resize(total);
+    h->h_last_row.resize(B);
+    SeqState &st = h->hst;
+    std::memset(&st, 0, sizeof(st));
+    int off = 0;
+    for (int b = 0; b < B; ++b) {
+        const int T = cu[b + 1] - cu[b];
+        const int cap = T + hp.max_new;
+        for (int t = 0; t < T; ++t) {
+            h->h_row_pos[cu[b] + t] = t;
+            h->h_row_slot[cu[b] + t] = off + t;
+        }
+        h->h_last_row[b] = cu[b + 1] - 1;
+        st.n_past[b] = T - 1;            // the head pass processes the last row
+        st.kv_off[b] = off;
+        st.kv_cap[b] = cap;
+        st.active[b] = 1;
+        off += cap;
+    }
+    st.max_new = hp.max_new;
+    st.eos_id = hp.eos_id;
+    st.n_seq = B;
+    CK(cudaMemcpyAsync(h->row_pos, h->h_row_pos.data(), total * 4, cudaMemcpyHostToDevice, s));
+    CK(cudaMemcpyAsync(h->row_slot, h->h_row_slot.data(), total * 4, cudaMemcpyHostToDevice, s));
+    CK(cudaMemcpyAsync(h->last_row, h->h_last_row.data(), B * 4, cudaMemcpyHostToDevice, s));
+    CK(cudaMemcpyAsync(h->st, &st, sizeof(SeqState), cudaMemcpyHostToDevice, s));
+
+    if (h->dumps) {
+        CK(cudaMemcpyAsync(h->dump_inj, h->x, (size_t)total * H * 4, cudaMemcpyDeviceToDevice, s));
+        h->dump_T = total;
+        h->dump_B = B;
+        h->dump_b0_valid = false;
+    }
+    for (int l = 0; l < hp.n_layers; ++l) {
+        const DevLayer &L = h->L[l];
+        launch_rmsnorm_rows(h->x, L.attn_norm, hp.rms_eps, h->xn, h->w_bf16, total, H, s);
+        gemm(h, h->xn, L.wqkv, h->qkv, qkv_rows(hp), total, qkv_rows(hp), H, EPI_STORE_F32);
+        RopeKvArgs r{};
+        r.qkv = h->qkv;
+        r.qn_w = L.qn;
+        r.kn_w = L.kn;
+        r.eps = hp.rms_eps;
+        r.rope = h->rope;
+        r.row_pos = h->row_pos;
+        r.row_slot = h->row_slot;
+        r.q_out = h->q16;
+        r.Kc = L.K;
+        r.Vc = L.V;
+        r.slots = (int)h->slots;
+        r.T = total;
+        r.nq = hp.n_heads;
+        r.nkv = hp.n_kv_heads;
+        r.d = hp.head_dim;
+        launch_qk_rope_kv(h->kv_f16, r, s);
+        h->enq += 2;
+        if (l + 1 < hp.n_layers) {
+            AttnPrefillArgs a{};
+            a.q = h->q16;
+            a.Kc = L.K;
+            a.Vc = L.V;
+            a.row_pos = h->row_pos;
+            a.row_slot = h->row_slot;
+            a.o = h->attn_o;
+            a.slots = (int)h->slots;
+            a.T = total;
+            a.nq = hp.n_heads;
+            a.nkv = hp.n_kv_heads;
+            a.d = hp.head_dim;
+            launch_attn_prefill_simt(h->kv_f16, h->w_bf16, a, s);
+            gemm(h, h->attn_o, L.wo, h->x, H, total, H, nqd, EPI_RESID_F32);
+            launch_rmsnorm_rows(h->x, L.ffn_norm, hp.rms_eps, h->xn, h->w_bf16, total, H, s);
+            gemm(h, h->xn, L.wgu, h->gu, 2 * F, total, 2 * F, H, EPI_STORE_F32);
+            launch_swiglu(h->gu, h->hbuf, h->w_bf16, total, F, s);
+            gemm(h, h->hbuf, L.wd, h->x, H, total, H, F, EPI_RESID_F32);
+            h->enq += 3;
+            if (h->dumps && l == 0) {
+                CK(cudaMemcpyAsync(h->dump_b0, h->x, (size_t)total * H * 4, cudaMemcpyDeviceToDevice, s));
+                h->dump_b0_valid = true;
+            }
+        } else {
+            // slice_last: the last block's query side, FFN and head run on the
+            // last row of each sequence only (decoder.cpp, build_prefill_graph)
+            launch_gather_rows(h->x, h->last_row, h->xd, B, H, s);
+            h->enq++;
+            enqueue_decode_layer(h, l, B, false);
+        }
+    }
+    if (h->dumps) {
+        CK(cudaMemcpyAsync(h->dump_blast, h->xd, (size_t)B * H * 4, cudaMemcpyDeviceToDevice, s));
+        launch_rmsnorm_rows(h->xd, h->final_norm, hp.rms_eps, h->dump_final, false, B, H, s);
+    }
+    enqueue_head(h, B);
+    CK(cudaGetLastError());
+    h->launches += h->enq;
+    dec_status rc = sync_state(h);
+    if (rc != DEC_OK) return rc;
+    h->n_seq = B;
+    h->prefilled = true;
+    h->logits_rows = B;
+    for (int b = 0; b < B; ++b) first_tokens[b] = h->hst.cur_tok[b];
+    return DEC_OK;
+}
+
+static dec_status check_lengths(dec_handle *h, const int32_t *cu, int B) {
+    const dec_hparams &hp = h->hp;
+    if (B < 1 || B > hp.max_batch) return fail(h, DEC_ERR_INVALID_ARG, "batch size out of range");
+    if (cu[0] != 0) return fail(h, DEC_ERR_INVALID_ARG, "cu_seqlens[0] must be 0");
+    for (int b = 0; b < B; ++b) {
+        const int T = cu[b + 1] - cu[b];
+        if (T < 1) return fail(h, DEC_ERR_INVALID_ARG, "every sequence needs at least one row");
+        if (T + hp.max_new > hp.max_ctx)
+            return fail(h, DEC_ERR_INPUT_TOO_LONG,
+                        "prompt of " + std::to_string(T) + " rows + generation budget " +
+                            std::to_string(hp.max_new) + " exceeds the context of " + std::to_string(hp.max_ctx));
+    }
+    if (cu[B] > hp.max_tokens)
+        return fail(h, DEC_ERR_INPUT_TOO_LONG, "prompt rows exceed max_tokens");
+    return DEC_OK;
+}
+
+static dec_status timed_prefill(dec_handle *h, const int32_t *cu, int B, int32_t *first) {
+    cudaEventRecord(h->ev[0], h->stream);
+    dec_status rc = prefill_rows(h, cu, B, first);
+    cudaEventRecord(h->ev[1], h->stream);
+    cudaEventSynchronize(h->ev[1]);
+    cudaEventElapsedTime(&h->prefill_ms, h->ev[0], h->ev[1]);
+    return rc;
+}
+
+// ------------------------------------------------------------------ generate
+static dec_status run_step_graph(dec_handle *h, int B) {
+    if (h->step_B != B) {
+        h->enq = 0;
+        dec_status rc = capture(h, 1, B, &h->step_exec, &h->step_nodes);
+        if (rc != DEC_OK) return rc;
+        h->step_B = B;
+    }
+    CK(cudaGraphLaunch(h->step_exec, h->stream));
+    h->launches += (int64_t)h->step_nodes;
+    return DEC_OK;
+}
+
+static dec_status generate_core(dec_handle *h, int max_new) {
+    const int B = h->n_seq;
+    SeqState &st = h->hst;
+    st.max_new = max_new;
+    for (int b = 0; b < B; ++b) {
+        if (!st.active[b]) continue;
+        st.done[b] = (st.cur_tok[b] == st.eos_id) || st.gen[b] >= max_new || st.n_past[b] + 1 > st.kv_cap[b];
+    }
+    CK(cudaMemcpyAsync(h->st, &st, sizeof(SeqState), cudaMemcpyHostToDevice, h->stream));
+    if (h->gen_B != B) {
+        h->enq = 0;
+        dec_status rc = capture(h, kGenChunk, B, &h->gen_exec, &h->gen_nodes);
+        if (rc != DEC_OK) return rc;
+        h->gen_B = B;
+    }
+    CK(cudaEventRecord(h->ev[2], h->stream));
+    for (;;) {
+        bool live = false;
+        for (int b = 0; b < B; ++b) live |= st.active[b] && !st.done[b];
+        if (!live) break;
+        CK(cudaGraphLaunch(h->gen_exec, h->stream));
+        h->launches += (int64_t)h->gen_nodes;
+        dec_status rc = sync_state(h);
+        if (rc != DEC_OK) return rc;
+    }
+    CK(cudaEventRecord(h->ev[3], h->stream));
+    CK(cudaEventSynchronize(h->ev[3]));
+    cudaEventElapsedTime(&h->gen_ms, h->ev[2], h->ev[3]);
+    h->logits_rows = B;
+    return DEC_OK;
+}
+
+// ================================================================== C ABI
+extern "C" {
+
+const char *dec_status_string(dec_status s) {
+    switch (s) {
+    case DEC_OK: return "DEC_OK";
+    case DEC_ERR_INVALID_ARG: return "DEC_ERR_INVALID_ARG";
+    case DEC_ERR_OOM: return "DEC_ERR_OOM";
+    case DEC_ERR_INPUT_TOO_LONG: return "DEC_ERR_INPUT_TOO_LONG";
+    case DEC_ERR_OUTPUT_TRUNCATED: return "DEC_ERR_OUTPUT_TRUNCATED";
+    case DEC_ERR_CUDA: return "DEC_ERR_CUDA";
+    case DEC_ERR_STATE: return "DEC_ERR_STATE";
+    case DEC_ERR_DEVICE: return "DEC_ERR_DEVICE";
+    }
+    return "unknown";
+}
+
+const char *dec_last_error(const dec_handle *h) { return h ? h->err.c_str() : "null handle"; }
+
+dec_status dec_workspace_size(const dec_hparams *hp, size_t *bytes) {
+    if (!bytes) return DEC_ERR_INVALID_ARG;
+    if (!validate(hp).empty()) return DEC_ERR_INVALID_ARG;
+    dec_handle tmp;
+    int dev = 0, sms = 152;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaGetLastError();
+    *bytes = plan(&tmp, *hp, nullptr, sms);
+    return DEC_OK;
+}
+
+static void to_f32_host(const void *src, bool bf16, size_t n, float *dst) {
+    if (!bf16) {
+        std::memcpy(dst, src, n * 4);
+        return;
+    }
+    const uint16_t *s = static_cast<const uint16_t *>(src);
+    for (size_t i = 0; i < n; ++i) {
+        const uint32_t u = (uint32_t)s[i] << 16;
+        std::memcpy(dst + i, &u, 4);
+    }
+}
+
+dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspace, size_t ws_bytes,
+                      void *stream, dec_handle **out) {
+    if (!out) return DEC_ERR_INVALID_ARG;
+    *out = nullptr;
+    const std::string why = validate(hp);
+    if (!why.empty()) return DEC_ERR_INVALID_ARG;
+    if (!w || !w->embed || !w->final_norm || !w->layers || !workspace) return DEC_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256) return DEC_ERR_INVALID_ARG;
+    for (int l = 0; l < hp->n_layers; ++l) {
+        const dec_layer_weights &L = w->layers[l];
+        if (!L.attn_norm || !L.q || !L.k || !L.v || !L.o || !L.q_norm || !L.k_norm || !L.ffn_norm || !L.gate ||
+            !L.up || !L.down)
+            return DEC_ERR_INVALID_ARG;
+    }
+    dec_handle *h = new dec_handle();
+    h->hp = *hp;
+    h->stream = static_cast<cudaStream_t>(stream);
+    h->w_bf16 = hp->weight_dtype == DEC_BF16;
+    h->kv_f16 = hp->kv_dtype == DEC_F16;
+    const char *g = std::getenv("SPEECH_DECODER_GEMM");
+    h->use_tc = !(g && std::strcmp(g, "simt") == 0);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        delete h;
+        return DEC_ERR_CUDA;
+    }
+    const size_t need = plan(h, *hp, nullptr, h->num_sms);
+    if (ws_bytes < need) {
+        delete h;
+        return DEC_ERR_OOM;
+    }
+    plan(h, *hp, static_cast<char *>(workspace), h->num_sms);
+    for (auto &e : h->ev) cudaEventCreate(&e);
+
+    auto fail_create = [&](dec_status s) {
+        dec_destroy(h);
+        return s;
+    };
+#define CKC(call)                                   \
+    do {                                            \
+        if ((call) != cudaSuccess) return fail_create(DEC_ERR_CUDA); \
+    } while (0)
+
+    init_gemv_kernels();
+    init_gemm_tc();
+    cudaStream_t s = h->stream;
+    const size_t ws = wsize(*hp), H = hp->hidden, F = hp->ffn, d = hp->head_dim;
+    const size_t nq = hp->n_heads, nkv = hp->n_kv_heads;
+    CKC(cudaMemcpyAsync(h->embed, w->embed, (size_t)hp->vocab * H * ws, cudaMemcpyHostToDevice, s));
+    std::vector<float> nbuf(std::max(H, d));
+    std::vector<char> gu_host(2 * F * H * ws);
+    auto put_norm = [&](float *dst, const void *src, size_t n) -> cudaError_t {
+        to_f32_host(src, h->w_bf16, n, nbuf.data());
+        cudaError_t e = cudaMemcpyAsync(dst, nbuf.data(), n * 4, cudaMemcpyHostToDevice, s);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+        return e;
+    };
+    CKC(put_norm(h->final_norm, w->final_norm, H));
+    for (int l = 0; l < hp->n_layers; ++l) {
+        const dec_layer_weights &W = w->layers[l];
+        DevLayer &D = h->L[l];
+        char *q = static_cast<char *>(D.wqkv);
+        CKC(cudaMemcpyAsync(q, W.q, nq * d * H * ws, cudaMemcpyHostToDevice, s));
+        CKC(cudaMemcpyAsync(q + nq * d * H * ws, W.k, nkv * d * H * ws, cudaMemcpyHostToDevice, s));
+        CKC(cudaMemcpyAsync(q + (nq + nkv) * d * H * ws, W.v, nkv * d * H * ws, cudaMemcpyHostToDevice, s));
+        CKC(cudaMemcpyAsync(D.wo, W.o, H * nq * d * ws, cudaMemcpyHostToDevice, s));
+        CKC(cudaMemcpyAsync(D.wd, W.down, H * F * ws, cudaMemcpyHostToDevice, s));
+        // gate|up packed per 128 features: [gate rows of the block | up rows of the block]
+        const size_t blk = 128 * H * ws;
+        CKC(cudaStreamSynchronize(s));
+        for (size_t j = 0; j < F / 128; ++j) {
+            std::memcpy(gu_host.data() + (2 * j) * blk, static_cast<const char *>(W.gate) + j * blk, blk);
+            std::memcpy(gu_host.data() + (2 * j + 1) * blk, static_cast<const char *>(W.up) + j * blk, blk);
+        }
+        CKC(cudaMemcpyAsync(D.wgu, gu_host.data(), 2 * F * H * ws, cudaMemcpyHostToDevice, s));
+        CKC(cudaStreamSynchronize(s));
+        CKC(put_norm(D.attn_norm, W.attn_norm, H));
+        CKC(put_norm(D.ffn_norm, W.ffn_norm, H));
+        CKC(put_norm(D.qn, W.q_norm, d));
+        CKC(put_norm(D.kn, W.k_norm, d));
+    }
+    // RoPE table: angle p * theta^(-2i/d) in double, stored as float (cos, sin)
+    {
+        const size_t P = hp->max_ctx, half = d / 2;
+        std::vector<float2> tab(P * half);
+        for (size_t i = 0; i < half; ++i) {
+            const double inv = std::pow((double)hp->rope_theta, -2.0 * (double)i / (double)d);
+            for (size_t p = 0; p < P; ++p) {
+                const double a = (double)p * inv;
+                tab[p * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+            }
+        }
+        CKC(cudaMemcpyAsync(h->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice, s));
+        CKC(cudaStreamSynchronize(s));
+    }
+    CKC(cudaMemsetAsync(h->attn_counter, 0, (size_t)hp->max_batch * nkv * sizeof(unsigned), s));
+    CKC(cudaMemsetAsync(h->am_counter, 0, 64 * sizeof(unsigned), s));
+    std::memset(&h->hst, 0, sizeof(SeqState));
+    h->hst.eos_id = hp->eos_id;
+    CKC(cudaMemcpyAsync(h->st, &h->hst, sizeof(SeqState), cudaMemcpyHostToDevice, s));
+    CKC(cudaStreamSynchronize(s));
+#undef CKC
+    *out = h;
+    return DEC_OK;
+}
+
+void dec_destroy(dec_handle *h) {
+    if (!h) return;
+    if (h->step_exec) cudaGraphExecDestroy(h->step_exec);
+    if (h->gen_exec) cudaGraphExecDestroy(h->gen_exec);
+    for (auto &e : h->ev)
+        if (e) cudaEventDestroy(e);
+    delete h;
+}
+
+dec_status dec_reset(dec_handle *h) {
+    if (!h) return DEC_ERR_INVALID_ARG;
+    h->prefilled = false;
+    h->n_seq = 0;
+    h->logits_rows = 0;
+    std::memset(&h->hst, 0, sizeof(SeqState));
+    h->hst.eos_id = h->hp.eos_id;
+    CK(cudaMemcpyAsync(h->st, &h->hst, sizeof(SeqState), cudaMemcpyHostToDevice, h->stream));
+    CK(cudaStreamSynchronize(h->stream));
+    h->err.clear();
+    return DEC_OK;
+}
+
+static dec_status copy_in(dec_handle *h, void *dst, const void *src, size_t bytes, int on_device) {
+    CK(cudaMemcpyAsync(dst, src, bytes, on_device ? cudaMemcpyDeviceToDevice : cudaMemcpyHostToDevice,
+                       h->stream));
+    return DEC_OK;
+}
+
+dec_status dec_prefill(dec_handle *h, const float *embeds, int32_t T, int32_t on_device, int32_t *first_token) {
+    if (!h || !embeds || !first_token || T < 1) return fail(h, DEC_ERR_INVALID_ARG, "bad prefill arguments");
+    const int32_t cu[2] = {0, T};
+    dec_status rc = check_lengths(h, cu, 1);
+    if (rc != DEC_OK) return rc;
+    rc = copy_in(h, h->x, embeds, (size_t)T * h->hp.hidden * 4, on_device);
+    if (rc != DEC_OK) return rc;
+    return timed_prefill(h, cu, 1, first_token);
+}
+
+dec_status dec_prefill_ids(dec_handle *h, const int32_t *ids, int32_t n_ids, const float *audio, int32_t n_audio,
+                           int32_t prefix_len, int32_t on_device, int32_t *first_token) {
+    if (!h || !first_token || n_ids < 0 || n_audio < 0 || prefix_len < 0 || prefix_len > n_ids ||
+        (n_ids > 0 && !ids) || (n_audio > 0 && !audio) || n_ids + n_audio < 1)
+        return fail(h, DEC_ERR_INVALID_ARG, "bad prefill_ids arguments");
+    const int T = n_ids + n_audio;
+    const int32_t cu[2] = {0, T};
+    dec_status rc = check_lengths(h, cu, 1);
+    if (rc != DEC_OK) return rc;
+    if (n_ids > 0) {
+        std::vector<int32_t> hid(n_ids);
+        if (on_device) CK(cudaMemcpy(hid.data(), ids, n_ids * 4, cudaMemcpyDeviceToHost));
+        else std::memcpy(hid.data(), ids, n_ids * 4);
+        for (int i = 0; i < n_ids; ++i)
+            if (hid[i] < 0 || hid[i] >= h->hp.vocab) return fail(h, DEC_ERR_INVALID_ARG, "token id out of range");
+        CK(cudaMemcpyAsync(h->ids_dev, hid.data(), n_ids * 4, cudaMemcpyHostToDevice, h->stream));
+        CK(cudaStreamSynchronize(h->stream));
+    }
+    const size_t H = h->hp.hidden;
+    float *span = h->x + (size_t)prefix_len * H;
+    if (n_audio > 0) {
+        rc = copy_in(h, span, audio, (size_t)n_audio * H * 4, on_device);
+        if (rc != DEC_OK) return rc;
+    }
+    launch_assemble(h->embed, h->w_bf16, h->ids_dev, span, h->x, T, n_audio, prefix_len, (int)H, h->stream);
+    h->launches++;
+    return timed_prefill(h, cu, 1, first_token);
+}
+
+dec_status dec_prefill_batch(dec_handle *h, const float *embeds, const int32_t *cu_seqlens, int32_t B,
+                             int32_t on_device, int32_t *first_tokens) {
+    if (!h || !embeds || !cu_seqlens || !first_tokens) return fail(h, DEC_ERR_INVALID_ARG, "null argument");
+    dec_status rc = check_lengths(h, cu_seqlens, B);
+    if (rc != DEC_OK) return rc;
+    rc = copy_in(h, h->x, embeds, (size_t)cu_seqlens[B] * h->hp.hidden * 4, on_device);
+    if (rc != DEC_OK) return rc;
+    return timed_prefill(h, cu_seqlens, B, first_tokens);
+}
+
+static dec_status step_rows(dec_handle *h, const int32_t *tokens, const uint8_t *active, int32_t *next) {
+    SeqState &st = h->hst;
+    const int B = h->n_seq;
+    for (int b = 0; b < B; ++b) {
+        const bool on = active ? active[b] != 0 : true;
+        if (on && (tokens[b] < 0 || tokens[b] >= h->hp.vocab))
+            return fail(h, DEC_ERR_INVALID_ARG, "token id out of range");
+        if (on && st.n_past[b] + 1 > st.kv_cap[b])
+            return fail(h, DEC_ERR_INPUT_TOO_LONG, "KV range of the sequence is full");
+    }
+    for (int b = 0; b < B; ++b) {
+        const bool on = active ? active[b] != 0 : true;
+        st.active[b] = on;
+        st.done[b] = 0;
+        if (on) st.cur_tok[b] = tokens[b];
+    }
+    st.max_new = 0x7fffffff;
+    CK(cudaMemcpyAsync(h->st, &st, sizeof(SeqState), cudaMemcpyHostToDevice, h->stream));
+    dec_status rc = run_step_graph(h, B);
+    if (rc != DEC_OK) return rc;
+    rc = sync_state(h);
+    if (rc != DEC_OK) return rc;
+    for (int b = 0; b < B; ++b) next[b] = st.active[b] ? st.cur_tok[b] : -1;
+    for (int b = 0; b < B; ++b) st.active[b] = 1;
+    h->logits_rows = B;
+    return DEC_OK;
+}
+
+dec_status dec_step(dec_handle *h, int32_t token, int32_t *next_token) {
+    if (!h || !next_token) return fail(h, DEC_ERR_INVALID_ARG, "null argument");
+    if (!h->prefilled) return fail(h, DEC_ERR_STATE, "dec_step before dec_prefill");
+    if (h->n_seq != 1) return fail(h, DEC_ERR_STATE, "dec_step needs a single-sequence prefill");
+    return step_rows(h, &token, nullptr, next_token);
+}
+
+dec_status dec_step_batch(dec_handle *h, const int32_t *tokens, const uint8_t *active, int32_t *next_tokens) {
+    if (!h || !tokens || !next_tokens) return fail(h, DEC_ERR_INVALID_ARG, "null argument");
+    if (!h->prefilled) return fail(h, DEC_ERR_STATE, "dec_step_batch before a prefill");
+    return step_rows(h, tokens, active, next_tokens);
+}
+
+static void finish_ids(dec_handle *h, int b, int max_new, int32_t *out, int32_t *n_out, int32_t *trunc,
+                       const std::vector<int32_t> &all) {
+    int n = std::min(h->hst.gen[b], max_new);
+    const int32_t *src = all.data() + (size_t)b * h->hp.max_new;
+    std::copy(src, src + n, out);
+    const bool eos = n > 0 && src[n - 1] == h->hp.eos_id;
+    if (eos) --n;
+    *n_out = n;
+    *trunc = eos ? 0 : 1;
+}
+
+dec_status dec_generate(dec_handle *h, int32_t max_new, int32_t *out_ids, int32_t *n_out) {
+    if (!h || !out_ids || !n_out) return fail(h, DEC_ERR_INVALID_ARG, "null argument");
+    if (!h->prefilled || h->n_seq != 1) return fail(h, DEC_ERR_STATE, "dec_generate needs a single-sequence prefill");
+    if (max_new < 1 || max_new > h->hp.max_new) return fail(h, DEC_ERR_INVALID_ARG, "max_new out of range");
+    dec_status rc = generate_core(h, max_new);
+    if (rc != DEC_OK) return rc;
+    std::vector<int32_t> all((size_t)h->hp.max_new * h->n_seq);
+    CK(cudaMemcpy(all.data(), h->out_ids, all.size() * 4, cudaMemcpyDeviceToHost));
+    int32_t trunc = 0;
+    finish_ids(h, 0, max_new, out_ids, n_out, &trunc, all);
+    return trunc ? fail(h, DEC_ERR_OUTPUT_TRUNCATED, "generation budget or context reached before EOS") : DEC_OK;
+}
+
+dec_status dec_generate_batch(dec_handle *h, int32_t max_new, int32_t *out_ids, int32_t *n_out, int32_t *truncated) {
+    if (!h || !out_ids || !n_out || !truncated) return fail(h, DEC_ERR_INVALID_ARG, "null argument");
+    if (!h->prefilled) return fail(h, DEC_ERR_STATE, "dec_generate_batch before a prefill");
+    if (max_new < 1 || max_new > h->hp.max_new) return fail(h, DEC_ERR_INVALID_ARG, "max_new out of range");
+    dec_status rc = generate_core(h, max_new);
+    if (rc != DEC_OK) return rc;
+    std::vector<int32_t> all((size_t)h->hp.max_new * h->n_seq);
+    CK(cudaMemcpy(all.data(), h->out_ids, all.size() * 4, cudaMemcpyDeviceToHost));
+    for (int b = 0; b < h->n_seq; ++b)
+        finish_ids(h, b, max_new, out_ids + (size_t)b * max_new, n_out + b, truncated + b, all);
+    return DEC_OK;
+}
+
+dec_status dec_debug_logits(dec_handle *h, float *out, int32_t rows) {
+    if (!h || !out || rows < 1) return fail(h, DEC_ERR_INVALID_ARG, "bad arguments");
+    if (rows > h->logits_rows) return fail(h, DEC_ERR_STATE, "fewer logits rows available");
+    CK(cudaMemcpyAsync(out, h->logits, (size_t)rows * h->hp.vocab * 4, cudaMemcpyDeviceToHost, h->stream));
+    CK(cudaStreamSynchronize(h->stream));
+    return DEC_OK;
+}
+
+dec_status dec_set_dumps(dec_handle *h, int32_t enable) {
+    if (!h) return DEC_ERR_INVALID_ARG;
+    h->dumps = enable != 0;
+    return DEC_OK;
+}
+
+dec_status dec_debug_dump(dec_handle *h, const char *name, float *out, size_t n_floats) {
+    if (!h || !name || !out) return fail(h, DEC_ERR_INVALID_ARG, "null argument");
+    const size_t H = h->hp.hidden;
+    const float *src = nullptr;
+    size_t n = 0;
+    if (!std::strcmp(name, "dec.audio_injected")) { src = h->dump_inj; n = (size_t)h->dump_T * H; }
+    else if (!std::strcmp(name, "dec.block.0.out") && h->dump_b0_valid) { src = h->dump_b0; n = (size_t)h->dump_T * H; }
+    else if (!std::strcmp(name, "dec.block.last.out")) { src = h->dump_blast; n = (size_t)h->dump_B * H; }
+    else if (!std::strcmp(name, "dec.out_before_head")) { src = h->dump_final; n = (size_t)h->dump_B * H; }
+    if (!src || n == 0) return fail(h, DEC_ERR_STATE, std::string("no capture named ") + name);
+    if (n != n_floats) return fail(h, DEC_ERR_INVALID_ARG, "size mismatch for " + std::string(name));
+    CK(cudaMemcpyAsync(out, src, n * 4, cudaMemcpyDeviceToHost, h->stream));
+    CK(cudaStreamSynchronize(h->stream));
+    return DEC_OK;
+}
+
+dec_status dec_launch_count(const dec_handle *h, int64_t *count) {
+    if (!h || !count) return DEC_ERR_INVALID_ARG;
+    *count = h->launches;
+    return DEC_OK;
+}
+
+dec_status dec_profile_kernel(dec_handle *h, int32_t op, int32_t iters, float *avg_ms, double *bytes_per_launch) {
+    if (!h || !avg_ms || !bytes_per_launch || iters < 1 || op < 0 || op > 2)
+        return fail(h, DEC_ERR_INVALID_ARG, "bad profile arguments");
+    if (!h->prefilled) return fail(h, DEC_ERR_STATE, "profile needs a prefill first");
+    dec_status rc = sync_state(h);
+    if (rc != DEC_OK) return rc;
+    const SeqState saved = h->hst;
+    const dec_hparams &hp = h->hp;
+    const int B = h->n_seq, H = hp.hidden, F = hp.ffn, d = hp.head_dim, nkv = hp.n_kv_heads;
+    const double ws = (double)wsize(hp), kvs = (double)kvsize(hp);
+    cudaStream_t s = h->stream;
+    int64_t launches = 0;
+    double bytes = 0.0;
+    CK(cudaEventRecord(h->ev[2], s));
+    for (int it = 0; it < iters; ++it) {
+        if (op == 1) {
+            // keep every row live so each launch does the full work
+            CK(cudaMemcpyAsync(h->st, &saved, sizeof(SeqState), cudaMemcpyHostToDevice, s));
+            enqueue_head(h, B);
+            ++launches;
+            bytes += (double)hp.vocab * H * ws + (double)B * (H + hp.vocab) * 4.0;
+            continue;
+        }
+        for (int l = 0; l < hp.n_layers; ++l) {
+            const DevLayer &L = h->L[l];
+            if (op == 0) {
+                GemvArgs g{};
+                g.st = h->st;
+                g.B = B;
+                g.eps = hp.rms_eps;
+                g.K = H;
+                g.in = h->xd;
+                g.W = L.wqkv;
+                g.N = qkv_rows(hp);
+                g.norm_w = L.attn_norm;
+                g.out = h->qkvd;
+                launch_gemv(IN_NORM, OUT_STORE, h->w_bf16, g, gemv_grid(g.N, h->num_sms), s);
+                bytes += (double)g.N * H * ws + (double)B * (H + g.N) * 4.0;
+                g.W = L.wgu;
+                g.N = 2 * F;
+                g.norm_w = L.ffn_norm;
+                g.out = h->gud;
+                launch_gemv(IN_NORM, OUT_STORE, h->w_bf16, g, gemv_grid(g.N, h->num_sms), s);
+                bytes += (double)g.N * H * ws + (double)B * (H + g.N) * 4.0;
+                launches += 2;
+            } else {
+                AttnDecArgs a{};
+                a.qkv = h->qkvd;
+                a.qn_w = L.qn;
+                a.kn_w = L.kn;
+                a.eps = hp.rms_eps;
+                a.rope = h->rope;
+                a.Kc = L.K;
+                a.Vc = L.V;
+                a.slots = (int)h->slots;
+                a.o = h->od;
+                a.part = h->attn_part;
+                a.counter = h->attn_counter;
+                a.st = h->st;
+                a.nq = hp.n_heads;
+                a.nkv = nkv;
+                a.d = d;
+                a.B = B;
+                a.append = 0;
+                launch_attn_decode(h->kv_f16, a, splits_for(h, B), s);
+                for (int b = 0; b < B; ++b)
+                    bytes += 2.0 * nkv * (double)(saved.n_past[b] + 1) * d * kvs;
+                bytes += (double)B * (qkv_rows(hp) + hp.n_heads * d) * 4.0;
+                ++launches;
+            }
+        }
+    }
+    CK(cudaEventRecord(h->ev[3], s));
+    CK(cudaEventSynchronize(h->ev[3]));
+    CK(cudaGetLastError());
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, h->ev[2], h->ev[3]);
+    h->launches += launches;
+    h->hst = saved;
+    CK(cudaMemcpyAsync(h->st, &h->hst, sizeof(SeqState), cudaMemcpyHostToDevice, s));
+    CK(cudaStreamSynchronize(s));
+    *avg_ms = ms / (float)launches;
+    *bytes_per_launch = bytes / (double)launches;
+    return DEC_OK;
+}
+
+dec_status dec_last_timings(const dec_handle *h, float *prefill_ms, float *generate_ms) {
+    if (!h) return DEC_ERR_INVALID_ARG;
+    if (prefill_ms) *prefill_ms = h->prefill_ms;
+    if (generate_ms) *generate_ms = h->gen_ms;
+    return DEC_OK;
+}
+
+}  // extern "C"

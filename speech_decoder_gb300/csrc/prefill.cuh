@@ -1,0 +1,49 @@
+// Prefill-path kernel interfaces (all prompt rows of one or more sequences).
+#pragma once
+#include "common.cuh"
+
+namespace dec {
+
+enum GemmEpi { EPI_STORE_F32 = 0, EPI_RESID_F32 = 1 };
+
+// rows of x (float32 [T, H]) -> RMSNorm(x) * w in bf16 (act_bf16) or float32
+void launch_rmsnorm_rows(const float *x, const float *w, float eps, void *out, bool act_bf16, int T,
+                         int H, cudaStream_t s);
+
+// C[M, N] (float32, row stride ldc) = or += A[M, K] . W[N, K]^T on CUDA cores
+void launch_gemm_simt(const void *A, bool a_bf16, const void *W, bool w_bf16, float *C, int ldc,
+                      int M, int N, int K, int epi, cudaStream_t s);
+
+// h[t, f] = silu(gate) * up from the packed gate|up rows (blocks of 128 + 128)
+void launch_swiglu(const float *gu, void *h, bool act_bf16, int T, int F, cudaStream_t s);
+
+struct RopeKvArgs {
+    const float *qkv;          // [T, (nq + 2 nkv) d]
+    const float *qn_w, *kn_w;
+    float eps;
+    const float2 *rope;        // [max_pos, d/2]
+    const int32_t *row_pos;    // [T] position of each row in its sequence
+    const int32_t *row_slot;   // [T] KV slot of each row in the pool
+    void *q_out;               // [T, nq, d] (f16 or f32, same type as the cache)
+    void *Kc, *Vc;             // this layer's pool [nkv][slots][d]
+    int slots, T, nq, nkv, d;
+};
+void launch_qk_rope_kv(bool kv_f16, const RopeKvArgs &a, cudaStream_t s);
+
+struct AttnPrefillArgs {
+    const void *q;             // [T, nq, d] roped queries (cache type)
+    const void *Kc, *Vc;       // pool [nkv][slots][d]
+    const int32_t *row_pos, *row_slot;
+    void *o;                   // [T, nq d] (bf16 or f32)
+    int slots, T, nq, nkv, d;
+};
+void launch_attn_prefill_simt(bool kv_f16, bool out_bf16, const AttnPrefillArgs &a, cudaStream_t s);
+
+// out[b] = x[idx[b]] for b < B (float32 rows of width H)
+void launch_gather_rows(const float *x, const int32_t *idx, float *out, int B, int H, cudaStream_t s);
+
+// x[t] = audio[t - prefix] inside the audio span, else embed[ids[..]] (prompt assembly)
+void launch_assemble(const void *embed, bool w_bf16, const int32_t *ids, const float *audio,
+                     float *x, int T, int n_audio, int prefix_len, int H, cudaStream_t s);
+
+}  // namespace dec
