@@ -100,7 +100,9 @@ dec_status dec_workspace_size(const dec_hparams *hp, size_t *bytes);
  * one [(n_heads+2*n_kv_heads)*d, H] matrix and gate|up packed into one
  * [2F, H] matrix in blocks of 128 rows (gate rows of the block, then the up
  * rows of the same features; model.cpp, load: pack_gate_up).  `stream` is a
- * cudaStream_t (NULL = legacy default stream).  Blocks until the upload is
+ * cudaStream_t; it must not be the legacy default stream, because the step
+ * loop is captured into CUDA graphs.  NULL makes the handle create (and
+ * later destroy) its own non-blocking stream.  Blocks until the upload is
  * done.  On success *out owns host-side objects only; free with dec_destroy. */
 dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspace,
                       size_t ws_bytes, void *stream, dec_handle **out);

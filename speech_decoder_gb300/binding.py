@@ -135,7 +135,9 @@ class Decoder:
         self.device = torch.device(device)
         size = workspace_size(self.hp)
         self.workspace = torch.empty(size, dtype=torch.uint8, device=self.device)
-        self.stream = torch.cuda.current_stream(self.device)
+        # a dedicated stream: the library captures CUDA graphs on it, which the
+        # legacy default stream does not allow
+        self.stream = torch.cuda.Stream(device=self.device)
         bf16 = spec.weight_dtype == "bf16"
         keep = []
 
@@ -174,6 +176,9 @@ class Decoder:
         t = self.torch
         if isinstance(a, t.Tensor):
             assert a.dtype == t.float32 and a.is_contiguous()
+            if a.is_cuda:
+                # order the library's stream after the work that produced `a`
+                self.stream.wait_stream(t.cuda.current_stream(a.device))
             return a.data_ptr(), int(a.is_cuda), a
         arr = _host_f32(a)
         return arr.ctypes.data, 0, arr
@@ -186,15 +191,23 @@ class Decoder:
         return tok.value
 
     def prefill_ids(self, ids, audio, prefix_len: int) -> int:
-        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        """ids and audio both on the device (torch CUDA tensors) or both on the
+        host (numpy arrays or torch CPU tensors, pinned or not)."""
+        t = self.torch
         p, dev, keep = self._rows(audio)
         if dev:
-            ids_t = self.torch.from_numpy(ids).to(self.device)
-            ip = ids_t.data_ptr()
+            ids_t = ids if isinstance(ids, t.Tensor) else t.from_numpy(np.ascontiguousarray(ids, np.int32))
+            ids_t = ids_t.to(device=self.device, dtype=t.int32).contiguous()
+            self.stream.wait_stream(t.cuda.current_stream(self.device))
+            ip, n_ids = ids_t.data_ptr(), ids_t.numel()
+        elif isinstance(ids, t.Tensor):
+            ids_t = ids.to(t.int32).contiguous()
+            ip, n_ids = ids_t.data_ptr(), ids_t.numel()
         else:
-            ip = ids.ctypes.data
+            ids_t = np.ascontiguousarray(ids, dtype=np.int32)
+            ip, n_ids = ids_t.ctypes.data, ids_t.size
         tok = c_int32()
-        self._check(self.lib.dec_prefill_ids(self.h, ip, len(ids), p, int(audio.shape[0]), prefix_len, dev,
+        self._check(self.lib.dec_prefill_ids(self.h, ip, n_ids, p, int(audio.shape[0]), prefix_len, dev,
                                              byref(tok)))
         return tok.value
 

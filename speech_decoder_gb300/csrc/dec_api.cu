@@ -91,6 +91,7 @@ struct dec_handle {
     std::string err;
     cudaEvent_t ev[4] = {};
     float prefill_ms = 0.f, gen_ms = 0.f;
+    bool own_stream = false;
 };
 
 // ------------------------------------------------------------------ helpers
@@ -570,6 +571,14 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
     dec_handle *h = new dec_handle();
     h->hp = *hp;
     h->stream = static_cast<cudaStream_t>(stream);
+    if (!h->stream) {
+        // the step loop is captured into CUDA graphs, which the legacy default stream cannot do
+        if (cudaStreamCreateWithFlags(&h->stream, cudaStreamNonBlocking) != cudaSuccess) {
+            delete h;
+            return DEC_ERR_CUDA;
+        }
+        h->own_stream = true;
+    }
     h->w_bf16 = hp->weight_dtype == DEC_BF16;
     h->kv_f16 = hp->kv_dtype == DEC_F16;
     const char *g = std::getenv("SPEECH_DECODER_GEMM");
@@ -666,6 +675,7 @@ void dec_destroy(dec_handle *h) {
     if (h->gen_exec) cudaGraphExecDestroy(h->gen_exec);
     for (auto &e : h->ev)
         if (e) cudaEventDestroy(e);
+    if (h->own_stream) cudaStreamDestroy(h->stream);
     delete h;
 }
 

@@ -191,9 +191,13 @@ def test_generate_batch_per_item_eos(small):
     spec, w = small
     prompts = [synth.Prompt(2, 12, 1), synth.Prompt(3, 30, 2), synth.Prompt(0, 5, 0)]
     embs = [prompt_rows(spec, w, p, seed=13, item=i)[0] for i, p in enumerate(prompts)]
-    # EOS = the oracle's 4th token of item 0, so item 0 stops early
+    # EOS = the first token of item 0's oracle run that did not occur before it,
+    # so item 0 stops early after k ids
     probe, _, _ = O.greedy(O.Oracle(spec, w, 64), embs[0], 12)
-    eos = probe[3]
+    ks = [i for i in range(1, len(probe)) if probe[i] not in probe[:i]]
+    assert ks, "item 0 repeats one token; pick another seed"
+    k = ks[0]
+    eos = probe[k]
     refs = [O.greedy(O.Oracle(spec, w, e.shape[0] + 12), e, 12, eos_id=eos) for e in embs]
     dec = make(spec, w, max_ctx=128, max_batch=3, max_tokens=128, max_new=12, eos_id=eos)
     dec.prefill_batch(embs)
@@ -202,7 +206,7 @@ def test_generate_batch_per_item_eos(small):
         ids, trunc = out[b]
         rids, rtrunc, _ = refs[b]
         assert ids == rids and trunc == rtrunc, (b, ids, rids)
-    assert not out[0][1] and len(out[0][0]) == 3
+    assert not out[0][1] and len(out[0][0]) == k
 
 
 # ------------------------------------------------------------------ errors
