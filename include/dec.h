@@ -207,6 +207,32 @@ dec_status dec_last_timings(const dec_handle *h, float *prefill_ms, float *gener
 dec_status dec_profile_kernel(dec_handle *h, int32_t op, int32_t iters, float *avg_ms,
                               double *bytes_per_launch);
 
+/* ---------------------------------------------------------------------
+ * Standalone kernel: the split-KV grouped-query attention of the step
+ * (decoder.cpp, build_step_graph: attention of one new row per sequence
+ * over its cached keys), for queries that are already Q-normed and rotated.
+ * All data pointers are device memory; work is queued on `stream` and the
+ * call returns without synchronising.
+ *   q       float32 [B, n_heads, head_dim]
+ *   K, V    pool [n_kv_heads, slots, head_dim] of kv_dtype (DEC_F16/DEC_F32)
+ *   kv_off  int32 [B]: first pool slot of sequence b
+ *   kv_len  int32 [B]: keys kv_off[b] .. kv_off[b]+kv_len[b]-1 are visible;
+ *           rows with kv_len <= 0 or outside the pool are skipped and their
+ *           output left unchanged
+ *   out     float32 [B, n_heads, head_dim] = softmax(q k^T / sqrt(d)) v with
+ *           query head h reading KV head h / (n_heads / n_kv_heads)
+ *   scratch device memory of at least dec_attn_decode_scratch_size() bytes
+ *           (per-split partials and arrival counters; zeroed by the call)
+ * Shapes: head_dim 64 or 128, n_heads a multiple of n_kv_heads, at most 8
+ * query heads per KV head.  Calls sharing one scratch buffer must not
+ * overlap on the GPU. */
+dec_status dec_attn_decode_scratch_size(int32_t B, int32_t n_heads, int32_t n_kv_heads,
+                                        int32_t head_dim, size_t *bytes);
+dec_status dec_attn_decode(const float *q, const void *K, const void *V, int32_t kv_dtype,
+                           int32_t slots, const int32_t *kv_off, const int32_t *kv_len, int32_t B,
+                           int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, float *out,
+                           void *scratch, size_t scratch_bytes, void *stream);
+
 /* Message of the last error on this handle ("" if none). */
 const char *dec_last_error(const dec_handle *h);
 

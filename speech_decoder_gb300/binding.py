@@ -25,7 +25,8 @@ EXPORTS = [
     "dec_workspace_size", "dec_create", "dec_destroy", "dec_reset", "dec_prefill", "dec_prefill_ids",
     "dec_prefill_batch", "dec_step", "dec_step_batch", "dec_generate", "dec_generate_batch",
     "dec_debug_logits", "dec_set_dumps", "dec_debug_dump", "dec_launch_count", "dec_last_timings",
-    "dec_last_error", "dec_status_string", "dec_profile_kernel",
+    "dec_last_error", "dec_status_string", "dec_profile_kernel", "dec_attn_decode_scratch_size",
+    "dec_attn_decode",
 ]
 
 
@@ -86,6 +87,9 @@ def load_library():
         "dec_launch_count": ([H, POINTER(c_int64)], c_int32),
         "dec_last_timings": ([H, POINTER(c_float), POINTER(c_float)], c_int32),
         "dec_profile_kernel": ([H, c_int32, c_int32, POINTER(c_float), POINTER(ctypes.c_double)], c_int32),
+        "dec_attn_decode_scratch_size": ([c_int32, c_int32, c_int32, c_int32, POINTER(c_size_t)], c_int32),
+        "dec_attn_decode": ([c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_int32, c_int32,
+                             c_int32, c_int32, c_void_p, c_void_p, c_size_t, c_void_p], c_int32),
         "dec_last_error": ([H], c_char_p),
         "dec_status_string": ([c_int32], c_char_p),
     }

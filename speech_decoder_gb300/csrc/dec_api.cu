@@ -39,7 +39,6 @@ struct Bump {
 };
 
 constexpr int kGenChunk = 16;     // steps per captured generate graph
-constexpr int kMaxSplits = 32;    // split-KV partitions per (sequence, kv head)
 
 }  // namespace
 
@@ -136,10 +135,7 @@ static std::string validate(const dec_hparams *hp) {
     return "";
 }
 
-static int splits_for(const dec_handle *h, int B) {
-    const int want = (2 * h->num_sms + B * h->hp.n_kv_heads - 1) / (B * h->hp.n_kv_heads);
-    return std::max(1, std::min(kMaxSplits, want));
-}
+static int splits_for(const dec_handle *h, int B) { return attn_decode_splits(B, h->hp.n_kv_heads, h->num_sms); }
 
 // Assign every device buffer from the bump allocator (base == nullptr: size only).
 static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms) {
@@ -181,7 +177,7 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     h->od = b.take<float>(Bm * nq * d);
     h->gud = b.take<float>(Bm * 2 * F);
     h->logits = b.take<float>(Bm * V);
-    h->attn_part = b.take<float>(Bm * nkv * kMaxSplits * (nq / nkv) * (d + 2));
+    h->attn_part = b.take<float>(Bm * nkv * kAttnMaxSplits * (nq / nkv) * (d + 2));
     h->attn_counter = b.take<unsigned>(Bm * nkv);
     h->lm_grid = gemv_grid((int)V, num_sms);
     h->am_val = b.take<float>(Bm * h->lm_grid);
@@ -945,6 +941,38 @@ dec_status dec_profile_kernel(dec_handle *h, int32_t op, int32_t iters, float *a
     *avg_ms = ms / (float)launches;
     *bytes_per_launch = bytes / (double)launches;
     return DEC_OK;
+}
+
+static int current_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return sms;
+}
+
+dec_status dec_attn_decode_scratch_size(int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                        size_t *bytes) {
+    if (!bytes || !attn_op_shape_ok(B, n_heads, n_kv_heads, head_dim, 1, 1)) return DEC_ERR_INVALID_ARG;
+    const int sms = current_sms();
+    if (sms <= 0) return DEC_ERR_CUDA;
+    *bytes = attn_op_scratch_bytes(B, n_heads, n_kv_heads, head_dim, sms);
+    return DEC_OK;
+}
+
+dec_status dec_attn_decode(const float *q, const void *K, const void *V, int32_t kv_dtype, int32_t slots,
+                           const int32_t *kv_off, const int32_t *kv_len, int32_t B, int32_t n_heads,
+                           int32_t n_kv_heads, int32_t head_dim, float *out, void *scratch, size_t scratch_bytes,
+                           void *stream) {
+    if (!q || !K || !V || !kv_off || !kv_len || !out || !scratch ||
+        !attn_op_shape_ok(B, n_heads, n_kv_heads, head_dim, slots, kv_dtype == DEC_F16 || kv_dtype == DEC_F32))
+        return DEC_ERR_INVALID_ARG;
+    const int sms = current_sms();
+    if (sms <= 0) return DEC_ERR_CUDA;
+    if (scratch_bytes < attn_op_scratch_bytes(B, n_heads, n_kv_heads, head_dim, sms)) return DEC_ERR_OOM;
+    cudaError_t e = attn_op_launch(q, K, V, kv_dtype == DEC_F16, slots, kv_off, kv_len, B, n_heads, n_kv_heads,
+                                   head_dim, out, scratch, sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
 }
 
 dec_status dec_last_timings(const dec_handle *h, float *prefill_ms, float *generate_ms) {

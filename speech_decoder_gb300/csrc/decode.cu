@@ -261,7 +261,7 @@ __device__ __forceinline__ void load_kv(const TKV *p, float (&f)[PL]) {
 
 constexpr int kMaxRep = 8;
 
-template <typename TKV, int D>
+template <typename TKV, int D, bool STEP>
 __global__ void __launch_bounds__(128) k_attn_decode(AttnDecArgs a, float scale) {
     constexpr int PL = D / 32;
     __shared__ float qs[kMaxRep][D];
@@ -270,29 +270,40 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecArgs a, float scale)
     __shared__ unsigned ticket;
 
     const int g = blockIdx.x, s = blockIdx.y, S = gridDim.y, b = blockIdx.z;
-    if (!row_live(a.st, b)) return;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n_rep = a.nq / a.nkv;
-    const int pos = a.st->n_past[b], len = pos + 1, off = a.st->kv_off[b];
+    int pos, len, off;
+    if (STEP) {
+        if (!row_live(a.st, b)) return;
+        pos = a.st->n_past[b];
+        len = pos + 1;
+        off = a.st->kv_off[b];
+    } else {
+        len = a.kv_len[b];
+        off = a.kv_off[b];
+        if (len <= 0 || off < 0 || (long long)off + len > (long long)a.slots) return;   // row skipped
+        pos = len - 1;
+    }
     const size_t ldq = (size_t)(a.nq + 2 * a.nkv) * D;
-    const float *row = a.qkv + (size_t)b * ldq;
-    const float2 *rope_row = a.rope + (size_t)pos * (D / 2);
+    const float *row = STEP ? a.qkv + (size_t)b * ldq : nullptr;
+    const float2 *rope_row = STEP ? a.rope + (size_t)pos * (D / 2) : nullptr;
     TKV *Kc = reinterpret_cast<TKV *>(a.Kc);
     TKV *Vc = reinterpret_cast<TKV *>(a.Vc);
 
     for (int r = warp; r < n_rep; r += 4) {
         float v[PL];
-        const float *src = row + (size_t)(g * n_rep + r) * D + lane * PL;
+        const float *src = STEP ? row + (size_t)(g * n_rep + r) * D + lane * PL
+                                : a.q_plain + ((size_t)b * a.nq + g * n_rep + r) * D + lane * PL;
 #pragma unroll
         for (int e = 0; e < PL; ++e) v[e] = src[e];
-        norm_rope_lane<PL>(v, a.qn_w, a.eps, D, rope_row, lane);
+        if (STEP) norm_rope_lane<PL>(v, a.qn_w, a.eps, D, rope_row, lane);
 #pragma unroll
         for (int e = 0; e < PL; ++e) qs[r][lane * PL + e] = v[e];
     }
 
     const int chunk = (len + S - 1) / S;
     const int j0 = min(len, s * chunk), j1 = min(len, j0 + chunk);
-    if (a.append && j0 <= pos && pos < j1) {
+    if (STEP && a.append && j0 <= pos && pos < j1) {
         const size_t slot = ((size_t)g * a.slots + off + pos) * D + lane * PL;
         if (warp == 0) {
             float v[PL];
@@ -395,16 +406,73 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecArgs a, float scale)
     if (tid == 0) a.counter[b * nkv + g] = 0u;
 }
 
-void launch_attn_decode(bool kv_f16, const AttnDecArgs &a, int splits, cudaStream_t s) {
+template <bool STEP>
+static void attn_launch(bool kv_f16, const AttnDecArgs &a, int splits, cudaStream_t s) {
     dim3 grid(a.nkv, splits, a.B);
     const float scale = (float)(1.0 / sqrt((double)a.d));
     if (kv_f16) {
-        if (a.d == 128) k_attn_decode<__half, 128><<<grid, 128, 0, s>>>(a, scale);
-        else k_attn_decode<__half, 64><<<grid, 128, 0, s>>>(a, scale);
+        if (a.d == 128) k_attn_decode<__half, 128, STEP><<<grid, 128, 0, s>>>(a, scale);
+        else k_attn_decode<__half, 64, STEP><<<grid, 128, 0, s>>>(a, scale);
     } else {
-        if (a.d == 128) k_attn_decode<float, 128><<<grid, 128, 0, s>>>(a, scale);
-        else k_attn_decode<float, 64><<<grid, 128, 0, s>>>(a, scale);
+        if (a.d == 128) k_attn_decode<float, 128, STEP><<<grid, 128, 0, s>>>(a, scale);
+        else k_attn_decode<float, 64, STEP><<<grid, 128, 0, s>>>(a, scale);
     }
+}
+
+void launch_attn_decode(bool kv_f16, const AttnDecArgs &a, int splits, cudaStream_t s) {
+    attn_launch<true>(kv_f16, a, splits, s);
+}
+
+void launch_attn_decode_plain(bool kv_f16, const AttnDecArgs &a, int splits, cudaStream_t s) {
+    attn_launch<false>(kv_f16, a, splits, s);
+}
+
+int attn_decode_splits(int B, int nkv, int num_sms) {
+    const int want = (2 * num_sms + B * nkv - 1) / (B * nkv);
+    return want < 1 ? 1 : (want > kAttnMaxSplits ? kAttnMaxSplits : want);
+}
+
+size_t attn_decode_part_floats(int B, int nq, int nkv, int d, int splits) {
+    return (size_t)B * nkv * splits * (nq / nkv) * (d + 2);
+}
+
+static size_t align256(size_t n) { return (n + 255) & ~size_t(255); }
+
+size_t attn_op_scratch_bytes(int B, int nq, int nkv, int d, int num_sms) {
+    const int S = attn_decode_splits(B, nkv, num_sms);
+    return align256(attn_decode_part_floats(B, nq, nkv, d, S) * sizeof(float)) +
+           align256((size_t)B * nkv * sizeof(unsigned));
+}
+
+bool attn_op_shape_ok(int B, int nq, int nkv, int d, int slots, int kv_ok) {
+    return B >= 1 && B <= 1 << 16 && nkv >= 1 && nq >= nkv && nq % nkv == 0 && nq / nkv <= kMaxRep &&
+           (d == 64 || d == 128) && slots >= 1 && kv_ok;
+}
+
+cudaError_t attn_op_launch(const float *q, const void *K, const void *V, bool kv_f16, int slots,
+                           const int32_t *kv_off, const int32_t *kv_len, int B, int nq, int nkv, int d, float *out,
+                           void *scratch, int num_sms, cudaStream_t s) {
+    const int S = attn_decode_splits(B, nkv, num_sms);
+    const size_t part_bytes = align256(attn_decode_part_floats(B, nq, nkv, d, S) * sizeof(float));
+    unsigned *counter = reinterpret_cast<unsigned *>(static_cast<char *>(scratch) + part_bytes);
+    cudaError_t e = cudaMemsetAsync(counter, 0, (size_t)B * nkv * sizeof(unsigned), s);
+    if (e != cudaSuccess) return e;
+    AttnDecArgs a{};
+    a.Kc = const_cast<void *>(K);
+    a.Vc = const_cast<void *>(V);
+    a.slots = slots;
+    a.o = out;
+    a.part = static_cast<float *>(scratch);
+    a.counter = counter;
+    a.nq = nq;
+    a.nkv = nkv;
+    a.d = d;
+    a.B = B;
+    a.q_plain = q;
+    a.kv_off = kv_off;
+    a.kv_len = kv_len;
+    launch_attn_decode_plain(kv_f16, a, S, s);
+    return cudaGetLastError();
 }
 
 }  // namespace dec

@@ -41,15 +41,35 @@ struct AttnDecArgs {
     int nq, nkv, d;
     int B;                  // sequences (grid z)
     int append;             // 1: write the row's K/V at slot n_past first
+    // plain mode (no state, no norm/RoPE/append): q already normed and roped
+    const float *q_plain;   // [B, nq, d]
+    const int32_t *kv_off;  // [B] first slot of each sequence
+    const int32_t *kv_len;  // [B] visible keys (rows with len <= 0 or out of range are skipped)
 };
 
 void launch_gemv(int in_mode, int out_mode, bool w_bf16, const GemvArgs &a, int grid_x,
                  cudaStream_t s);
 void launch_attn_decode(bool kv_f16, const AttnDecArgs &a, int splits, cudaStream_t s);
+// plain-mode launch over caller buffers; a.part/a.counter are the scratch
+void launch_attn_decode_plain(bool kv_f16, const AttnDecArgs &a, int splits, cudaStream_t s);
+// split-KV partitions for B sequences and the scratch bytes they need
+int attn_decode_splits(int B, int nkv, int num_sms);
+size_t attn_decode_part_floats(int B, int nq, int nkv, int d, int splits);
+
+// Standalone plain-mode attention over caller buffers (shared by the C entry
+// points): checks shapes, zeroes the counters in `scratch` and launches.
+// scratch = [partials (256-aligned)][B * nkv counters].
+size_t attn_op_scratch_bytes(int B, int nq, int nkv, int d, int num_sms);
+bool attn_op_shape_ok(int B, int nq, int nkv, int d, int slots, int kv_dtype_f16_or_f32);
+cudaError_t attn_op_launch(const float *q, const void *K, const void *V, bool kv_f16, int slots,
+                           const int32_t *kv_off, const int32_t *kv_len, int B, int nq, int nkv, int d,
+                           float *out, void *scratch, int num_sms, cudaStream_t s);
 int gemv_grid(int N, int num_sms);
 void init_gemv_kernels();
 
 // activation rows x K floats of one GEMV CTA must fit: kGroupB * K * 4 <= kGemvMaxSmem
 constexpr int kGemvMaxSmem = 200 * 1024;
+// split-KV partitions per (sequence, kv head)
+constexpr int kAttnMaxSplits = 32;
 
 }  // namespace dec
