@@ -233,6 +233,29 @@ dec_status dec_attn_decode(const float *q, const void *K, const void *V, int32_t
                            int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, float *out,
                            void *scratch, size_t scratch_bytes, void *stream);
 
+/* dec_attn_decode without the scratch argument, for callers that cannot
+ * allocate device memory: code running inside a host engine or plugin
+ * interface whose device memory belongs to someone else and offers no
+ * allocator, or a latency-bound loop that must not call cudaMalloc (which can
+ * synchronise the device).  The pages have no counterpart: their decoder
+ * always owns a ggml scheduler that allocates its own buffers.
+ *
+ * Arguments and results are those of dec_attn_decode.  The partials and the
+ * arrival counters live in one file-scope device array of 4 MiB, reserved on
+ * every GPU that loads the library and held until the process exits; a shape
+ * whose scratch (dec_attn_decode_scratch_size) exceeds 4 MiB returns
+ * DEC_ERR_OOM without launching.  The call allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine); it zeroes the counters with
+ * cudaMemsetAsync on `stream`.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture.  Every call shares the one
+ * array, so calls that overlap on the GPU (other streams, other threads) race
+ * and corrupt each other's results: serialise them. */
+dec_status dec_attn_decode_noalloc(const float *q, const void *K, const void *V, int32_t kv_dtype,
+                                   int32_t slots, const int32_t *kv_off, const int32_t *kv_len,
+                                   int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
+                                   float *out, void *stream);
+
 /* Message of the last error on this handle ("" if none). */
 const char *dec_last_error(const dec_handle *h);
 
