@@ -91,6 +91,7 @@ struct dec_handle {
     cudaEvent_t ev[4] = {};
     float prefill_ms = 0.f, gen_ms = 0.f;
     bool own_stream = false;
+    int gemv_ctas = 1;              // GEMV CTAs per SM
 };
 
 // ------------------------------------------------------------------ helpers
@@ -121,8 +122,15 @@ static std::string validate(const dec_hparams *hp) {
     if ((p.n_heads * p.head_dim) % 256) return "n_heads*head_dim must be a multiple of 256";
     if (p.ffn < 128 || p.ffn % 128) return "ffn must be a positive multiple of 128";
     if (p.vocab < 1) return "vocab must be >= 1";
-    if ((size_t)kGroupB * std::max({p.hidden, p.ffn, p.n_heads * p.head_dim}) * 4 > (size_t)kGemvMaxSmem)
-        return "hidden, ffn and n_heads*head_dim must be <= 12800";
+    {
+        // every projection of the step must fit the GEMV's shared-memory plan
+        const int H = p.hidden, F = p.ffn, nqd = p.n_heads * p.head_dim;
+        const int qkv = (p.n_heads + 2 * p.n_kv_heads) * p.head_dim;
+        const int shapes[5][2] = {{qkv, H}, {H, nqd}, {2 * F, H}, {H, F}, {p.vocab, H}};
+        for (auto &nk : shapes)
+            if (!gemv_plan(nk[1], p.weight_dtype == DEC_BF16, std::min(p.max_batch, kGroupB), nk[0], 152).ok)
+                return "projection too large for the decode GEMV (hidden, ffn, n_heads*head_dim <= 6144)";
+    }
     if (!(p.rms_eps >= 0.f) || !(p.rope_theta > 0.f)) return "rms_eps must be >= 0 and rope_theta > 0";
     if (p.max_batch < 1 || p.max_batch > kMaxBatch) return "max_batch must be in [1, 64]";
     if (p.max_new < 1) return "max_new must be >= 1";
@@ -137,9 +145,15 @@ static std::string validate(const dec_hparams *hp) {
 
 static int splits_for(const dec_handle *h, int B) { return attn_decode_splits(B, h->hp.n_kv_heads, h->num_sms); }
 
+static int gemv_ctas_per_sm() {
+    const char *c = std::getenv("SPEECH_DECODER_GEMV_CTAS_PER_SM");
+    return c ? std::max(1, std::min(4, std::atoi(c))) : 1;
+}
+
 // Assign every device buffer from the bump allocator (base == nullptr: size only).
 static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms) {
     Bump b{base};
+    h->gemv_ctas = gemv_ctas_per_sm();
     const size_t ws = wsize(hp), kvs = kvsize(hp), as = ws;   // activations use the weight format
     const size_t H = hp.hidden, d = hp.head_dim, nq = hp.n_heads, nkv = hp.n_kv_heads, F = hp.ffn;
     const size_t V = hp.vocab, Tm = hp.max_tokens, Bm = hp.max_batch;
@@ -179,7 +193,7 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     h->logits = b.take<float>(Bm * V);
     h->attn_part = b.take<float>(Bm * nkv * kAttnMaxSplits * (nq / nkv) * (d + 2));
     h->attn_counter = b.take<unsigned>(Bm * nkv);
-    h->lm_grid = gemv_grid((int)V, num_sms);
+    h->lm_grid = gemv_grid((int)V, num_sms, h->gemv_ctas);
     h->am_val = b.take<float>(Bm * h->lm_grid);
     h->am_idx = b.take<int>(Bm * h->lm_grid);
     h->am_counter = b.take<unsigned>(64);
@@ -221,7 +235,7 @@ static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
     g.x_resid = h->xd;
     g.out = h->qkvd;
     const bool emb = from_embed && l == 0;
-    launch_gemv(emb ? IN_EMBED_NORM : IN_NORM, OUT_STORE, h->w_bf16, g, gemv_grid(g.N, h->num_sms), s);
+    launch_gemv(emb ? IN_EMBED_NORM : IN_NORM, OUT_STORE, h->w_bf16, g, gemv_grid(g.N, h->num_sms, h->gemv_ctas), s);
 
     AttnDecArgs a{};
     a.qkv = h->qkvd;
@@ -252,14 +266,14 @@ static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
     o.K = nqd;
     o.in = h->od;
     o.out = h->xd;
-    launch_gemv(IN_PLAIN, OUT_RESID, h->w_bf16, o, gemv_grid(H, h->num_sms), s);
+    launch_gemv(IN_PLAIN, OUT_RESID, h->w_bf16, o, gemv_grid(H, h->num_sms, h->gemv_ctas), s);
 
     GemvArgs f1 = g;
     f1.W = L.wgu;
     f1.N = 2 * F;
     f1.norm_w = L.ffn_norm;
     f1.out = h->gud;
-    launch_gemv(IN_NORM, OUT_STORE, h->w_bf16, f1, gemv_grid(2 * F, h->num_sms), s);
+    launch_gemv(IN_NORM, OUT_STORE, h->w_bf16, f1, gemv_grid(2 * F, h->num_sms, h->gemv_ctas), s);
 
     GemvArgs f2{};
     f2.st = h->st;
@@ -270,7 +284,7 @@ static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
     f2.in = h->gud;
     f2.ffn = F;
     f2.out = h->xd;
-    launch_gemv(IN_SWIGLU, OUT_RESID, h->w_bf16, f2, gemv_grid(H, h->num_sms), s);
+    launch_gemv(IN_SWIGLU, OUT_RESID, h->w_bf16, f2, gemv_grid(H, h->num_sms, h->gemv_ctas), s);
     h->enq += 5;
 }
 
@@ -579,6 +593,7 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
     h->kv_f16 = hp->kv_dtype == DEC_F16;
     const char *g = std::getenv("SPEECH_DECODER_GEMM");
     h->use_tc = !(g && std::strcmp(g, "simt") == 0);
+
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -602,6 +617,9 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
         if ((call) != cudaSuccess) return fail_create(DEC_ERR_CUDA); \
     } while (0)
 
+    if (const char *v = std::getenv("SPEECH_DECODER_GEMV"))
+        gemv_set_impl(!std::strcmp(v, "ldg") ? 1 : !std::strcmp(v, "cpasync") ? 2 : 3);
+    if (const char *v = std::getenv("SPEECH_DECODER_GEMV_SLOTS")) gemv_set_ring(std::atoi(v));
     init_gemv_kernels();
     init_gemm_tc();
     cudaStream_t s = h->stream;
@@ -864,6 +882,12 @@ dec_status dec_profile_kernel(dec_handle *h, int32_t op, int32_t iters, float *a
     dec_status rc = sync_state(h);
     if (rc != DEC_OK) return rc;
     const SeqState saved = h->hst;
+    SeqState live = saved;                      // profile every row, whatever the loop state
+    for (int b = 0; b < h->n_seq; ++b) {
+        live.active[b] = 1;
+        live.done[b] = 0;
+    }
+    CK(cudaMemcpyAsync(h->st, &live, sizeof(SeqState), cudaMemcpyHostToDevice, h->stream));
     const dec_hparams &hp = h->hp;
     const int B = h->n_seq, H = hp.hidden, F = hp.ffn, d = hp.head_dim, nkv = hp.n_kv_heads;
     const double ws = (double)wsize(hp), kvs = (double)kvsize(hp);
@@ -874,7 +898,7 @@ dec_status dec_profile_kernel(dec_handle *h, int32_t op, int32_t iters, float *a
     for (int it = 0; it < iters; ++it) {
         if (op == 1) {
             // keep every row live so each launch does the full work
-            CK(cudaMemcpyAsync(h->st, &saved, sizeof(SeqState), cudaMemcpyHostToDevice, s));
+            CK(cudaMemcpyAsync(h->st, &live, sizeof(SeqState), cudaMemcpyHostToDevice, s));
             enqueue_head(h, B);
             ++launches;
             bytes += (double)hp.vocab * H * ws + (double)B * (H + hp.vocab) * 4.0;
@@ -893,13 +917,13 @@ dec_status dec_profile_kernel(dec_handle *h, int32_t op, int32_t iters, float *a
                 g.N = qkv_rows(hp);
                 g.norm_w = L.attn_norm;
                 g.out = h->qkvd;
-                launch_gemv(IN_NORM, OUT_STORE, h->w_bf16, g, gemv_grid(g.N, h->num_sms), s);
+                launch_gemv(IN_NORM, OUT_STORE, h->w_bf16, g, gemv_grid(g.N, h->num_sms, h->gemv_ctas), s);
                 bytes += (double)g.N * H * ws + (double)B * (H + g.N) * 4.0;
                 g.W = L.wgu;
                 g.N = 2 * F;
                 g.norm_w = L.ffn_norm;
                 g.out = h->gud;
-                launch_gemv(IN_NORM, OUT_STORE, h->w_bf16, g, gemv_grid(g.N, h->num_sms), s);
+                launch_gemv(IN_NORM, OUT_STORE, h->w_bf16, g, gemv_grid(g.N, h->num_sms, h->gemv_ctas), s);
                 bytes += (double)g.N * H * ws + (double)B * (H + g.N) * 4.0;
                 launches += 2;
             } else {

@@ -25,7 +25,21 @@ struct GemvArgs {
     unsigned *counter;
     int32_t *out_ids;       // [B, out_ids_cap]
     int out_ids_cap;
+    // filled in by launch_gemv: shared-memory slots per warp, units per CTA
+    int n_ring;
+    int max_units;
 };
+
+struct GemvPlan {
+    int n_ring, max_units;
+    size_t smem;
+    bool ok;
+};
+GemvPlan gemv_plan(int K, bool w_bf16, int nb, int N, int grid_x);
+// tuning knobs (process-wide): pipeline implementation and bulk ring sizes
+void gemv_set_impl(int impl);
+int gemv_impl();
+void gemv_set_ring(int slots);
 
 struct AttnDecArgs {
     const float *qkv;       // [B, (nq + 2 nkv) d] raw projections of the step's row
@@ -64,12 +78,14 @@ bool attn_op_shape_ok(int B, int nq, int nkv, int d, int slots, int kv_dtype_f16
 cudaError_t attn_op_launch(const float *q, const void *K, const void *V, bool kv_f16, int slots,
                            const int32_t *kv_off, const int32_t *kv_len, int B, int nq, int nkv, int d,
                            float *out, void *scratch, int num_sms, cudaStream_t s);
-int gemv_grid(int N, int num_sms);
+int gemv_grid(int N, int num_sms, int ctas_per_sm);
 void init_gemv_kernels();
 
 // activation rows x K floats of one GEMV CTA must fit: kGroupB * K * 4 <= kGemvMaxSmem
 constexpr int kGemvMaxSmem = 200 * 1024;
 // split-KV partitions per (sequence, kv head)
 constexpr int kAttnMaxSplits = 32;
+// keys per split at least (short sequences run few splits)
+constexpr int kAttnMinChunk = 32;
 
 }  // namespace dec
