@@ -39,6 +39,8 @@ struct Bump {
 };
 
 constexpr int kGenChunk = 16;     // steps per captured generate graph
+constexpr size_t kTcScratchFloats = size_t(12) << 20;   // 48 MB of split-K partial tiles
+constexpr int kTcCounters = 4096;
 
 }  // namespace
 
@@ -92,6 +94,8 @@ struct dec_handle {
     float prefill_ms = 0.f, gen_ms = 0.f;
     bool own_stream = false;
     int gemv_ctas = 1;              // GEMV CTAs per SM
+    float *tc_scratch = nullptr;    // split-K partial tiles of the tensor-core GEMM
+    unsigned *tc_counters = nullptr;
 };
 
 // ------------------------------------------------------------------ helpers
@@ -199,6 +203,8 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     h->am_counter = b.take<unsigned>(64);
     h->out_ids = b.take<int32_t>(Bm * hp.max_new);
     h->st = b.take<SeqState>(1);
+    h->tc_scratch = b.take<float>(kTcScratchFloats);
+    h->tc_counters = b.take<unsigned>(kTcCounters);
     h->dump_inj = b.take<float>(Tm * H);
     h->dump_b0 = b.take<float>(Tm * H);
     h->dump_blast = b.take<float>(Bm * H);
@@ -207,12 +213,30 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
 }
 
 // ------------------------------------------------------------------ enqueue passes
+static int *dev_error(dec_handle *h) { return &h->st->error; }
+
+// Prompt-row projection C[M, N] (=|+=) A[M, K] W[N, K]^T: tcgen05 for bf16
+// weights, CUDA cores for the fp32 debug build.
 static void gemm(dec_handle *h, const void *A, const void *W, float *C, int ldc, int M, int N, int K, int epi) {
-    if (h->use_tc && h->w_bf16 && gemm_tc_supported(M, N, K))
-        launch_gemm_tc(A, W, C, ldc, M, N, K, epi, h->stream);
+    if (h->use_tc && h->w_bf16 && gemm_tc_plan(M, N, K, 1, h->num_sms, kTcScratchFloats).ok)
+        launch_gemm_tc(A, M, W, N, K, 1, epi, C, ldc, nullptr, 0, h->tc_scratch, kTcScratchFloats, h->tc_counters,
+                       dev_error(h), h->num_sms, h->stream);   // a launch error surfaces at the end of the pass
     else
         launch_gemm_simt(A, h->w_bf16, W, h->w_bf16, C, ldc, M, N, K, epi, h->stream);
     h->enq++;
+}
+
+// Gate|up projection and SwiGLU into h->hbuf.
+static void gemm_swiglu(dec_handle *h, const void *A, const void *Wgu, int M, int F, int K) {
+    if (h->use_tc && h->w_bf16 && gemm_tc_plan(M, 2 * F, K, 2, h->num_sms, kTcScratchFloats).ok) {
+        launch_gemm_tc(A, M, Wgu, 2 * F, K, 2, EPI_SWIGLU_BF16, nullptr, 0, h->hbuf, F, h->tc_scratch,
+                       kTcScratchFloats, h->tc_counters, dev_error(h), h->num_sms, h->stream);
+        h->enq++;
+    } else {
+        launch_gemm_simt(A, h->w_bf16, Wgu, h->w_bf16, h->gu, 2 * F, M, 2 * F, K, EPI_STORE_F32, h->stream);
+        launch_swiglu(h->gu, h->hbuf, h->w_bf16, M, F, h->stream);
+        h->enq += 2;
+    }
 }
 
 // One decoder block for the step rows in xd (one row per sequence).
@@ -419,10 +443,9 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
             launch_attn_prefill_simt(h->kv_f16, h->w_bf16, a, s);
             gemm(h, h->attn_o, L.wo, h->x, H, total, H, nqd, EPI_RESID_F32);
             launch_rmsnorm_rows(h->x, L.ffn_norm, hp.rms_eps, h->xn, h->w_bf16, total, H, s);
-            gemm(h, h->xn, L.wgu, h->gu, 2 * F, total, 2 * F, H, EPI_STORE_F32);
-            launch_swiglu(h->gu, h->hbuf, h->w_bf16, total, F, s);
+            gemm_swiglu(h, h->xn, L.wgu, total, F, H);
             gemm(h, h->hbuf, L.wd, h->x, H, total, H, F, EPI_RESID_F32);
-            h->enq += 3;
+            h->enq += 2;
             if (h->dumps && l == 0) {
                 CK(cudaMemcpyAsync(h->dump_b0, h->x, (size_t)total * H * 4, cudaMemcpyDeviceToDevice, s));
                 h->dump_b0_valid = true;
@@ -674,6 +697,7 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
     }
     CKC(cudaMemsetAsync(h->attn_counter, 0, (size_t)hp->max_batch * nkv * sizeof(unsigned), s));
     CKC(cudaMemsetAsync(h->am_counter, 0, 64 * sizeof(unsigned), s));
+    CKC(cudaMemsetAsync(h->tc_counters, 0, kTcCounters * sizeof(unsigned), s));
     std::memset(&h->hst, 0, sizeof(SeqState));
     h->hst.eos_id = hp->eos_id;
     CKC(cudaMemcpyAsync(h->st, &h->hst, sizeof(SeqState), cudaMemcpyHostToDevice, s));
@@ -997,6 +1021,32 @@ dec_status dec_attn_decode(const float *q, const void *K, const void *V, int32_t
     cudaError_t e = attn_op_launch(q, K, V, kv_dtype == DEC_F16, slots, kv_off, kv_len, B, n_heads, n_kv_heads,
                                    head_dim, out, scratch, sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
+}
+
+dec_status dec_debug_gemm(const void *X, int32_t T, const void *W, int32_t n_feat, int32_t K, int32_t epi, float *C,
+                          int32_t ldc, void *Hout, int32_t ldh, int32_t use_tc, int32_t splits, void *scratch,
+                          size_t scratch_bytes, void *stream) {
+    const size_t counter_bytes = 16 * 1024;
+    if (!X || !W || T < 1 || n_feat < 1 || K < 1 || epi < 0 || epi > 2 || !scratch ||
+        scratch_bytes < (size_t(16) << 20) || (epi == 2 ? !Hout : !C))
+        return DEC_ERR_INVALID_ARG;
+    const int sms = current_sms();
+    if (sms <= 0) return DEC_ERR_CUDA;
+    init_gemm_tc();
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t floats = (scratch_bytes - counter_bytes) / 4;
+    unsigned *counters = reinterpret_cast<unsigned *>(static_cast<char *>(scratch) + scratch_bytes - counter_bytes);
+    if (use_tc) {
+        const int groups = epi == 2 ? 2 : 1;
+        if (!gemm_tc_plan(T, n_feat, K, groups, sms, floats, splits).ok) return DEC_ERR_INVALID_ARG;
+        cudaError_t e = launch_gemm_tc(X, T, W, n_feat, K, groups, epi, C, ldc, Hout, ldh, static_cast<float *>(scratch),
+                                       floats, counters, nullptr, sms, s, splits);
+        if (e != cudaSuccess) cudaGetLastError();
+        return e == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
+    }
+    if (epi == 2) return DEC_ERR_INVALID_ARG;
+    launch_gemm_simt(X, true, W, true, C, ldc, T, n_feat, K, epi, s);
+    return cudaGetLastError() == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
 }
 
 dec_status dec_last_timings(const dec_handle *h, float *prefill_ms, float *generate_ms) {

@@ -1,7 +1,359 @@
+// Tensor-core GEMM of the prefill projections on sm_103a: tcgen05.mma with
+// TMEM accumulators, operands staged by TMA (cp.async.bulk.tensor, 128-byte
+// swizzle), one elected thread issuing the MMAs.
+//
+// Swapped operands: the weight rows are the MMA's M side (128 features per
+// tile) and the prompt rows are its N side (up to 256 tokens per tile), so a
+// short prompt (T = 152) fills one N tile with no padding waste.  The
+// accumulator tile sits in TMEM with TMEM lane = feature and column = token;
+// the epilogue warps read it back with tcgen05.ld and write C[token][feature]
+// (consecutive lanes -> consecutive features -> coalesced rows).
+//
+// Epilogues: store fp32 (q|k|v), add into the fp32 residual (o and down
+// projections), or SwiGLU: a gate|up weight block of 256 rows feeds two MMAs
+// into two TMEM column ranges, and the epilogue writes silu(gate) * up in bf16
+// (model.cpp, load: pack_gate_up; decoder.cpp header: SwiGLU on packed
+// gate_up).
+//
+// When a GEMM has fewer output tiles than SMs (short prompts), K is split
+// across CTAs; each split writes its partial tile to scratch and the last CTA
+// of the tile (arrival counter) sums the splits in split order, so results do
+// not depend on which CTA finishes last.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "gemm_tc.cuh"
+#include "ptx.cuh"
 
 namespace dec {
-bool gemm_tc_supported(int, int, int) { return false; }
-void launch_gemm_tc(const void *, const void *, float *, int, int, int, int, int, cudaStream_t) {}
-void init_gemm_tc() {}
+
+constexpr int kBK = 64;                 // K elements per stage: one 128-byte swizzle row of bf16
+constexpr int kTcThreads = 192;         // warp 0 TMA, warp 1 MMA + TMEM allocation, warps 2-5 epilogue
+constexpr uint32_t kTcPolls = 1u << 24; // bounded mbarrier waits
+
+struct TcArgs {
+    int n_feat, T, K;
+    int groups;                  // 1, or 2 for gate|up blocks
+    int BN, n_stages, k_tiles, splits, kt_per_split;
+    int epi;
+    float *C;
+    int ldc;
+    __nv_bfloat16 *Hout;
+    int ldh;
+    float *part;
+    unsigned *counter;
+    int *err;
+    uint32_t idesc, tmem_cols;
+};
+
+// ------------------------------------------------------------------ PTX helpers
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);     // start address
+    d |= (uint64_t)1 << 16;                        // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;              // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;                        // descriptor version for sm_100 family
+    d |= (uint64_t)2 << 61;                        // 128-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            ptx::smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(ptx::smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, int accum) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     ptx::smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_report(int *err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+// ------------------------------------------------------------------ epilogue
+// One output element: feature f of this tile (TMEM lane), token t.
+__device__ __forceinline__ void epi_store(const TcArgs &a, int f, int t, float v, float up) {
+    if (t >= a.T) return;
+    if (a.epi == EPI_SWIGLU_BF16) {
+        a.Hout[(size_t)t * a.ldh + f] = __float2bfloat16_rn(v / (1.f + expf(-v)) * up);
+    } else if (f < a.n_feat) {
+        float *c = a.C + (size_t)t * a.ldc + f;
+        if (a.epi == EPI_STORE_F32) *c = v;
+        else *c += v;
+    }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem =
+        reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int S = a.n_stages;
+    const uint32_t a_bytes = (uint32_t)a.groups * 16384u, b_bytes = (uint32_t)a.BN * 128u;
+    const uint32_t stage_bytes = a_bytes + b_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * stage_bytes);
+    uint64_t *empty = full + S;
+    uint64_t *done = empty + S;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
+    __shared__ int abort_s;
+    __shared__ unsigned ticket_s;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * 128 * a.groups;              // first weight row of the tile
+    const int n0 = blockIdx.y * a.BN;                        // first token of the tile
+    const int kt0 = blockIdx.z * a.kt_per_split;
+    const int nk = min(a.k_tiles, kt0 + a.kt_per_split) - kt0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        ptx::mbar_init(done, 1);
+        abort_s = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         ptx::smem_u32(tmem_slot)),
+                     "r"(a.tmem_cols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    int issued = 0;    // producer: stages issued (for the drain on abort)
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------------- TMA producer
+        for (int i = 0; i < nk; ++i) {
+            const int s = i % S;
+            if (i >= S && !ptx::mbar_wait_bounded(&empty[s], ((i / S) - 1) & 1, kTcPolls)) {
+                tc_report(a.err, 4);
+                abort_s = 1;
+                break;
+            }
+            if (*(volatile int *)&abort_s) break;
+            ptx::mbar_expect_tx(&full[s], stage_bytes);
+            unsigned char *st = smem + (size_t)s * stage_bytes;
+            tma_load_2d(st, &tmA, (kt0 + i) * kBK, m0, &full[s]);
+            tma_load_2d(st + a_bytes, &tmB, (kt0 + i) * kBK, n0, &full[s]);
+            issued = i + 1;
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------------------------------------------- MMA issuer
+        for (int i = 0; i < nk; ++i) {
+            const int s = i % S;
+            if (!ptx::mbar_wait_bounded(&full[s], (i / S) & 1, kTcPolls)) {
+                tc_report(a.err, 5);
+                abort_s = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t abase = ptx::smem_u32(smem + (size_t)s * stage_bytes), bbase = abase + a_bytes;
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+                const uint64_t bdesc = sw128_desc(bbase + kk * 32);
+                for (int g = 0; g < a.groups; ++g)
+                    mma_bf16(tmem + (uint32_t)(g * a.BN), sw128_desc(abase + g * 16384 + kk * 32), bdesc, a.idesc,
+                             (i | kk) != 0);
+            }
+            mma_commit(&empty[s]);                     // stage free once these MMAs have read it
+        }
+        mma_commit(done);                               // accumulator final
+    } else if (warp >= 2) {
+        // ---------------------------------------------------------- epilogue
+        const bool ok = ptx::mbar_wait_bounded(done, 0, kTcPolls);
+        if (!ok) tc_report(a.err, 6);
+        tc_fence_after();
+        const int q = warp & 3;                         // TMEM lane quarter this warp may access
+        const int r = 32 * q + lane;                    // feature row within the 128-row MMA tile
+        const int f = (a.epi == EPI_SWIGLU_BF16 ? blockIdx.x * 128 : m0) + r;
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+        const int ncols = a.groups * a.BN;
+        if (a.splits == 1) {
+            for (int c = 0; c < a.BN; c += 16) {
+                float v[16], u[16];
+                tmem_ld16(tq + c, v);
+                if (a.groups == 2) tmem_ld16(tq + a.BN + c, u);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) epi_store(a, f, n0 + c + j, v[j], a.groups == 2 ? u[j] : 0.f);
+            }
+        } else {
+            // split-K: park the partial tile, the last split of the tile finishes it
+            const int tile = blockIdx.y * gridDim.x + blockIdx.x;
+            float *mine = a.part + ((size_t)tile * a.splits + blockIdx.z) * ncols * 128;
+            for (int c = 0; c < ncols; c += 16) {
+                float v[16];
+                tmem_ld16(tq + c, v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) mine[(size_t)(c + j) * 128 + r] = v[j];
+            }
+            __threadfence();
+            ptx::named_bar_sync(1, 128);
+            if (threadIdx.x == 64) ticket_s = atomicAdd(&a.counter[tile], 1u);
+            ptx::named_bar_sync(1, 128);
+            if (ticket_s == (unsigned)a.splits - 1) {
+                __threadfence();
+                const float *all = a.part + (size_t)tile * a.splits * ncols * 128;
+                for (int c = 0; c < a.BN; ++c) {
+                    float v = 0.f, u = 0.f;
+                    for (int s = 0; s < a.splits; ++s) {
+                        v += __ldcg(all + ((size_t)s * ncols + c) * 128 + r);
+                        if (a.groups == 2) u += __ldcg(all + ((size_t)s * ncols + a.BN + c) * 128 + r);
+                    }
+                    epi_store(a, f, n0 + c, v, u);
+                }
+                if (threadIdx.x == 64) a.counter[tile] = 0u;
+            }
+        }
+    }
+    // the producer drains what it issued if the MMA side gave up
+    if (warp == 0 && lane == 0 && abort_s) {
+        for (int i = 0; i < issued; ++i) ptx::mbar_wait_bounded(&full[i % S], (i / S) & 1, kTcPolls);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
+}
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static bool g_tc_ready = false;
+static int g_max_dyn_smem = 0;
+
+void init_gemm_tc() {
+    if (g_tc_ready) return;
+    cudaDriverEntryPointQueryResult q;
+    void *fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess && fn) {
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        // the opt-in limit covers static and dynamic shared memory together
+        int dev = 0, optin = 0;
+        cudaFuncAttributes fa{};
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
+            cudaFuncGetAttributes(&fa, k_gemm_tc) == cudaSuccess) {
+            g_max_dyn_smem = optin - (int)fa.sharedSizeBytes;
+            if (cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, g_max_dyn_smem) ==
+                cudaSuccess)
+                g_tc_ready = true;
+        }
+    }
+    cudaGetLastError();
+}
+
+bool gemm_tc_ready() { return g_tc_ready; }
+
+static bool make_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t K, uint32_t box_rows) {
+    const cuuint64_t dims[2] = {K, rows};
+    const cuuint64_t strides[1] = {K * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
+    const cuuint32_t es[2] = {1, 1};
+    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+TcPlan gemm_tc_plan(int T, int n_feat, int K, int groups, int num_sms, size_t scratch_floats, int force_splits) {
+    TcPlan p{};
+    p.ok = g_tc_ready && T >= 1 && K % kBK == 0 && n_feat % (128 * groups) == 0;
+    if (!p.ok) return p;
+    const int BN = T <= 256 ? ((T + 15) / 16) * 16 : 256;
+    p.BN = BN;
+    const size_t stage = (size_t)groups * 16384 + (size_t)BN * 128;
+    const size_t budget = (size_t)g_max_dyn_smem - 1024 - 256;     // alignment pad + barriers
+    p.n_stages = (int)std::min<size_t>(8, budget / stage);
+    if (p.n_stages < 2) {
+        p.ok = false;
+        return p;
+    }
+    p.mt = n_feat / (128 * groups);
+    p.nt = (T + BN - 1) / BN;
+    p.k_tiles = K / kBK;
+    const int tiles = p.mt * p.nt;
+    int splits = 1;
+    if (tiles < num_sms) splits = std::max(1, std::min(p.k_tiles / 2, (num_sms + tiles - 1) / tiles));
+    if (force_splits > 0) splits = std::min(force_splits, p.k_tiles);
+    // the scratch for partial tiles bounds the split count
+    while (splits > 1 && (size_t)tiles * splits * groups * BN * 128 > scratch_floats) --splits;
+    p.kt_per_split = (p.k_tiles + splits - 1) / splits;
+    p.splits = (p.k_tiles + p.kt_per_split - 1) / p.kt_per_split;
+    int cols = 32;
+    while (cols < groups * BN) cols *= 2;
+    p.tmem_cols = cols;
+    p.smem = (size_t)p.n_stages * stage + 1024 + 256;
+    return p;
+}
+
+cudaError_t launch_gemm_tc(const void *X, int T, const void *W, int n_feat, int K, int groups, int epi, float *C,
+                           int ldc, void *Hout, int ldh, float *scratch, size_t scratch_floats, unsigned *counters,
+                           int *err, int num_sms, cudaStream_t s, int force_splits) {
+    const TcPlan p = gemm_tc_plan(T, n_feat, K, groups, num_sms, scratch_floats, force_splits);
+    if (!p.ok) return cudaErrorInvalidValue;
+    CUtensorMap mA, mB;
+    if (!make_map(&mA, W, (uint64_t)n_feat, (uint64_t)K, 128u * groups) ||
+        !make_map(&mB, X, (uint64_t)T, (uint64_t)K, (uint32_t)p.BN))
+        return cudaErrorInvalidValue;
+    TcArgs a{};
+    a.n_feat = groups == 2 ? n_feat / 2 : n_feat;
+    a.T = T;
+    a.K = K;
+    a.groups = groups;
+    a.BN = p.BN;
+    a.n_stages = p.n_stages;
+    a.k_tiles = p.k_tiles;
+    a.splits = p.splits;
+    a.kt_per_split = p.kt_per_split;
+    a.epi = epi;
+    a.C = C;
+    a.ldc = ldc;
+    a.Hout = static_cast<__nv_bfloat16 *>(Hout);
+    a.ldh = ldh;
+    a.part = scratch;
+    a.counter = counters;
+    a.err = err;
+    // instruction descriptor: f32 accumulate, bf16 A and B, both K-major, N = BN, M = 128
+    a.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(p.BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    a.tmem_cols = (uint32_t)p.tmem_cols;
+    dim3 grid(p.mt, p.nt, p.splits);
+    k_gemm_tc<<<grid, kTcThreads, p.smem, s>>>(mA, mB, a);
+    return cudaPeekAtLastError();
+}
+
 }  // namespace dec

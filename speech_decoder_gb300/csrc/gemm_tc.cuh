@@ -1,13 +1,32 @@
 // Tensor-core (tcgen05 / TMEM / TMA) bf16 GEMM for the prefill projections.
 #pragma once
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace dec {
 
-// C[M, N] (float32, row stride ldc) = or += A[M, K] . W[N, K]^T, A and W bf16.
-bool gemm_tc_supported(int M, int N, int K);
-void launch_gemm_tc(const void *A, const void *W, float *C, int ldc, int M, int N, int K, int epi,
-                    cudaStream_t s);
+// Epilogues of the prefill projections (shared with the CUDA-core GEMM).
+enum GemmEpi { EPI_STORE_F32 = 0, EPI_RESID_F32 = 1, EPI_SWIGLU_BF16 = 2 };
+
+struct TcPlan {
+    bool ok;
+    int BN, n_stages, mt, nt, k_tiles, splits, kt_per_split, tmem_cols;
+    size_t smem;
+};
+
+// Y = X W^T for X [T, K] (bf16 rows of the prompt) and W [n_feat, K] (bf16
+// weights).  epi: EPI_STORE_F32 writes C[t][f]; EPI_RESID_F32 adds into C;
+// EPI_SWIGLU_BF16 (groups = 2, W packed in blocks of 128 gate rows + 128 up
+// rows) writes Hout[t][f] = silu(gate) * up for f < n_feat / 2.
+// scratch/counters hold split-K partial tiles (counters zero between calls);
+// err receives a device error code if a bounded wait expires.
+TcPlan gemm_tc_plan(int T, int n_feat, int K, int groups, int num_sms, size_t scratch_floats,
+                    int force_splits = 0);
+cudaError_t launch_gemm_tc(const void *X, int T, const void *W, int n_feat, int K, int groups, int epi, float *C,
+                           int ldc, void *Hout, int ldh, float *scratch, size_t scratch_floats, unsigned *counters,
+                           int *err, int num_sms, cudaStream_t s, int force_splits = 0);
 void init_gemm_tc();
+bool gemm_tc_ready();
 
 }  // namespace dec

@@ -1,10 +1,8 @@
 // Prefill-path kernel interfaces (all prompt rows of one or more sequences).
 #pragma once
-#include "common.cuh"
+#include "gemm_tc.cuh"
 
 namespace dec {
-
-enum GemmEpi { EPI_STORE_F32 = 0, EPI_RESID_F32 = 1 };
 
 // rows of x (float32 [T, H]) -> RMSNorm(x) * w in bf16 (act_bf16) or float32
 void launch_rmsnorm_rows(const float *x, const float *w, float eps, void *out, bool act_bf16, int T,

@@ -86,3 +86,80 @@ def test_attn_decode_op_skips_invalid_rows(lib):
     assert np.all(got[0] == 7.0) and np.all(got[2] == 7.0)          # len 0 and out-of-pool rows untouched
     ref = oracle_attn(q[1:2], K, V, lens[1:2], offs[1:2])
     assert rel_err(got[1].reshape(1, -1), ref.reshape(1, -1)) <= 1e-4
+
+
+# ------------------------------------------------------------------ prefill GEMM (tcgen05 / CUDA cores)
+def _bf16(a):
+    from speech_decoder_gb300 import synth
+    a = np.ascontiguousarray(a, np.float32).copy()
+    synth.round_bf16(a)
+    return a
+
+
+def run_gemm(lib, X, W, epi, use_tc, splits=0, C0=None):
+    import torch
+    from speech_decoder_gb300 import synth
+    dev = "cuda:0"
+    T, K = X.shape
+    N = W.shape[0]
+    xt = torch.from_numpy(synth.bf16_bits(X).view(np.int16)).to(dev)
+    wt = torch.from_numpy(synth.bf16_bits(W).view(np.int16)).to(dev)
+    scratch = torch.zeros(64 << 20, dtype=torch.uint8, device=dev)
+    if epi == 2:
+        out = torch.zeros((T, N // 2), dtype=torch.int16, device=dev)
+        st = lib.dec_debug_gemm(xt.data_ptr(), T, wt.data_ptr(), N, K, 2, None, 0, out.data_ptr(), N // 2, 1,
+                                splits, scratch.data_ptr(), scratch.numel(), torch.cuda.current_stream().cuda_stream)
+        assert st == 0, st
+        torch.cuda.synchronize()
+        bits = out.cpu().numpy().view(np.uint16).astype(np.uint32) << 16
+        return bits.view(np.float32)
+    C = torch.from_numpy(np.zeros((T, N), np.float32) if C0 is None else C0.copy()).to(dev)
+    st = lib.dec_debug_gemm(xt.data_ptr(), T, wt.data_ptr(), N, K, epi, C.data_ptr(), N, None, 0, use_tc, splits,
+                            scratch.data_ptr(), scratch.numel(), torch.cuda.current_stream().cuda_stream)
+    assert st == 0, st
+    torch.cuda.synchronize()
+    return C.cpu().numpy()
+
+
+GEMMS = [  # T, N, K, splits (0 = automatic)
+    (16, 512, 256, 0), (152, 4096, 2048, 0), (152, 2048, 6144, 0), (1, 256, 512, 0), (700, 1024, 512, 0),
+    (8015, 256, 256, 0), (37, 384, 1408, 3), (152, 128, 64, 1), (300, 768, 192, 2),
+]
+
+
+@pytest.mark.parametrize("shape", GEMMS, ids=[f"T{s[0]}N{s[1]}K{s[2]}s{s[3]}" for s in GEMMS])
+def test_gemm_tc_matches_oracle_linear(lib, shape):
+    T, N, K, splits = shape
+    rng = np.random.default_rng(T * 7 + N)
+    X = _bf16(rng.standard_normal((T, K)))
+    W = _bf16(rng.standard_normal((N, K)) * 0.02)
+    ref = O.linear(X, W)
+    got = run_gemm(lib, X, W, 0, 1, splits)
+    assert rel_err(got, ref) <= 1e-5
+    C0 = rng.standard_normal((T, N)).astype(np.float32)
+    got = run_gemm(lib, X, W, 1, 1, splits, C0=C0)                      # residual add
+    assert rel_err(got, C0 + ref) <= 1e-5
+
+
+@pytest.mark.parametrize("shape", [(152, 1536, 512, 0), (16, 512, 256, 2), (500, 768, 256, 0)],
+                         ids=["T152F768", "T16F256s2", "T500F384"])
+def test_gemm_tc_swiglu_matches_oracle(lib, shape):
+    T, N2, K, splits = shape
+    F = N2 // 2
+    rng = np.random.default_rng(N2 + T)
+    X = _bf16(rng.standard_normal((T, K)))
+    Wg = _bf16(rng.standard_normal((F, K)) * 0.05)
+    Wu = _bf16(rng.standard_normal((F, K)) * 0.05)
+    # pack as the library does: blocks of 128 gate rows then the same 128 features' up rows
+    packed = np.concatenate([np.concatenate([Wg[j:j + 128], Wu[j:j + 128]]) for j in range(0, F, 128)])
+    got = run_gemm(lib, X, packed, 2, 1, splits)
+    ref = O.silu(O.linear(X, Wg)) * O.linear(X, Wu)
+    # output is rounded to bf16: relative error up to 2^-8 of each value
+    assert np.all(np.abs(got - ref) <= 2 ** -8 * np.abs(ref) + 1e-6)
+
+
+def test_gemm_simt_matches_oracle_linear(lib):
+    rng = np.random.default_rng(5)
+    X = _bf16(rng.standard_normal((45, 512)))
+    W = _bf16(rng.standard_normal((384, 512)) * 0.02)
+    assert rel_err(run_gemm(lib, X, W, 0, 0), O.linear(X, W)) <= 1e-5
