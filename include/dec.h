@@ -262,8 +262,8 @@ dec_status dec_attn_decode_noalloc(const float *q, const void *K, const void *V,
  * W bf16 [n_feat, K], C float32 [T, ldc], Hout bf16 [T, ldh]; all device
  * memory.  use_tc = 1 runs the tcgen05 GEMM, 0 the CUDA-core GEMM (epi 0/1
  * only).  splits > 0 forces the tcgen05 split-K count.  scratch: device
- * memory for split-K partials and counters, scratch_bytes >= 16 MB; its last
- * 16 KB must be zero on entry and is left zero.  Queued on `stream`. */
+ * memory for split-K partial tiles, scratch_bytes >= 16 MB.  Queued on
+ * `stream`. */
 dec_status dec_debug_gemm(const void *X, int32_t T, const void *W, int32_t n_feat, int32_t K,
                           int32_t epi, float *C, int32_t ldc, void *Hout, int32_t ldh, int32_t use_tc,
                           int32_t splits, void *scratch, size_t scratch_bytes, void *stream);

@@ -40,7 +40,6 @@ struct Bump {
 
 constexpr int kGenChunk = 16;     // steps per captured generate graph
 constexpr size_t kTcScratchFloats = size_t(12) << 20;   // 48 MB of split-K partial tiles
-constexpr int kTcCounters = 4096;
 
 }  // namespace
 
@@ -95,7 +94,6 @@ struct dec_handle {
     bool own_stream = false;
     int gemv_ctas = 1;              // GEMV CTAs per SM
     float *tc_scratch = nullptr;    // split-K partial tiles of the tensor-core GEMM
-    unsigned *tc_counters = nullptr;
 };
 
 // ------------------------------------------------------------------ helpers
@@ -151,7 +149,7 @@ static int splits_for(const dec_handle *h, int B) { return attn_decode_splits(B,
 
 static int gemv_ctas_per_sm() {
     const char *c = std::getenv("SPEECH_DECODER_GEMV_CTAS_PER_SM");
-    return c ? std::max(1, std::min(4, std::atoi(c))) : 1;
+    return c ? std::max(1, std::min(4, std::atoi(c))) : 2;
 }
 
 // Assign every device buffer from the bump allocator (base == nullptr: size only).
@@ -204,7 +202,6 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     h->out_ids = b.take<int32_t>(Bm * hp.max_new);
     h->st = b.take<SeqState>(1);
     h->tc_scratch = b.take<float>(kTcScratchFloats);
-    h->tc_counters = b.take<unsigned>(kTcCounters);
     h->dump_inj = b.take<float>(Tm * H);
     h->dump_b0 = b.take<float>(Tm * H);
     h->dump_blast = b.take<float>(Bm * H);
@@ -219,8 +216,8 @@ static int *dev_error(dec_handle *h) { return &h->st->error; }
 // weights, CUDA cores for the fp32 debug build.
 static void gemm(dec_handle *h, const void *A, const void *W, float *C, int ldc, int M, int N, int K, int epi) {
     if (h->use_tc && h->w_bf16 && gemm_tc_plan(M, N, K, 1, h->num_sms, kTcScratchFloats).ok)
-        launch_gemm_tc(A, M, W, N, K, 1, epi, C, ldc, nullptr, 0, h->tc_scratch, kTcScratchFloats, h->tc_counters,
-                       dev_error(h), h->num_sms, h->stream);   // a launch error surfaces at the end of the pass
+        launch_gemm_tc(A, M, W, N, K, 1, epi, C, ldc, nullptr, 0, h->tc_scratch, kTcScratchFloats, dev_error(h),
+                       h->num_sms, h->stream);   // a launch error surfaces at the end of the pass
     else
         launch_gemm_simt(A, h->w_bf16, W, h->w_bf16, C, ldc, M, N, K, epi, h->stream);
     h->enq++;
@@ -230,7 +227,7 @@ static void gemm(dec_handle *h, const void *A, const void *W, float *C, int ldc,
 static void gemm_swiglu(dec_handle *h, const void *A, const void *Wgu, int M, int F, int K) {
     if (h->use_tc && h->w_bf16 && gemm_tc_plan(M, 2 * F, K, 2, h->num_sms, kTcScratchFloats).ok) {
         launch_gemm_tc(A, M, Wgu, 2 * F, K, 2, EPI_SWIGLU_BF16, nullptr, 0, h->hbuf, F, h->tc_scratch,
-                       kTcScratchFloats, h->tc_counters, dev_error(h), h->num_sms, h->stream);
+                       kTcScratchFloats, dev_error(h), h->num_sms, h->stream);
         h->enq++;
     } else {
         launch_gemm_simt(A, h->w_bf16, Wgu, h->w_bf16, h->gu, 2 * F, M, 2 * F, K, EPI_STORE_F32, h->stream);
@@ -697,7 +694,6 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
     }
     CKC(cudaMemsetAsync(h->attn_counter, 0, (size_t)hp->max_batch * nkv * sizeof(unsigned), s));
     CKC(cudaMemsetAsync(h->am_counter, 0, 64 * sizeof(unsigned), s));
-    CKC(cudaMemsetAsync(h->tc_counters, 0, kTcCounters * sizeof(unsigned), s));
     std::memset(&h->hst, 0, sizeof(SeqState));
     h->hst.eos_id = hp->eos_id;
     CKC(cudaMemcpyAsync(h->st, &h->hst, sizeof(SeqState), cudaMemcpyHostToDevice, s));
@@ -1026,7 +1022,6 @@ dec_status dec_attn_decode(const float *q, const void *K, const void *V, int32_t
 dec_status dec_debug_gemm(const void *X, int32_t T, const void *W, int32_t n_feat, int32_t K, int32_t epi, float *C,
                           int32_t ldc, void *Hout, int32_t ldh, int32_t use_tc, int32_t splits, void *scratch,
                           size_t scratch_bytes, void *stream) {
-    const size_t counter_bytes = 16 * 1024;
     if (!X || !W || T < 1 || n_feat < 1 || K < 1 || epi < 0 || epi > 2 || !scratch ||
         scratch_bytes < (size_t(16) << 20) || (epi == 2 ? !Hout : !C))
         return DEC_ERR_INVALID_ARG;
@@ -1034,13 +1029,12 @@ dec_status dec_debug_gemm(const void *X, int32_t T, const void *W, int32_t n_fea
     if (sms <= 0) return DEC_ERR_CUDA;
     init_gemm_tc();
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const size_t floats = (scratch_bytes - counter_bytes) / 4;
-    unsigned *counters = reinterpret_cast<unsigned *>(static_cast<char *>(scratch) + scratch_bytes - counter_bytes);
+    const size_t floats = scratch_bytes / 4;
     if (use_tc) {
         const int groups = epi == 2 ? 2 : 1;
         if (!gemm_tc_plan(T, n_feat, K, groups, sms, floats, splits).ok) return DEC_ERR_INVALID_ARG;
         cudaError_t e = launch_gemm_tc(X, T, W, n_feat, K, groups, epi, C, ldc, Hout, ldh, static_cast<float *>(scratch),
-                                       floats, counters, nullptr, sms, s, splits);
+                                       floats, nullptr, sms, s, splits);
         if (e != cudaSuccess) cudaGetLastError();
         return e == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
     }

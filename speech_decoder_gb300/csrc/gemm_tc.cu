@@ -16,9 +16,9 @@
 // gate_up).
 //
 // When a GEMM has fewer output tiles than SMs (short prompts), K is split
-// across CTAs; each split writes its partial tile to scratch and the last CTA
-// of the tile (arrival counter) sums the splits in split order, so results do
-// not depend on which CTA finishes last.
+// across CTAs; each split writes its partial tile to scratch and a second,
+// fully parallel kernel sums the splits in split order (deterministic) and
+// applies the epilogue.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -41,7 +41,6 @@ struct TcArgs {
     __nv_bfloat16 *Hout;
     int ldh;
     float *part;
-    unsigned *counter;
     int *err;
     uint32_t idesc, tmem_cols;
 };
@@ -125,7 +124,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t *done = empty + S;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
     __shared__ int abort_s;
-    __shared__ unsigned ticket_s;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * 128 * a.groups;              // first weight row of the tile
@@ -211,7 +209,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int j = 0; j < 16; ++j) epi_store(a, f, n0 + c + j, v[j], a.groups == 2 ? u[j] : 0.f);
             }
         } else {
-            // split-K: park the partial tile, the last split of the tile finishes it
+            // split-K: park the partial tile; k_splitk_reduce sums the splits
             const int tile = blockIdx.y * gridDim.x + blockIdx.x;
             float *mine = a.part + ((size_t)tile * a.splits + blockIdx.z) * ncols * 128;
             for (int c = 0; c < ncols; c += 16) {
@@ -219,23 +217,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tmem_ld16(tq + c, v);
 #pragma unroll
                 for (int j = 0; j < 16; ++j) mine[(size_t)(c + j) * 128 + r] = v[j];
-            }
-            __threadfence();
-            ptx::named_bar_sync(1, 128);
-            if (threadIdx.x == 64) ticket_s = atomicAdd(&a.counter[tile], 1u);
-            ptx::named_bar_sync(1, 128);
-            if (ticket_s == (unsigned)a.splits - 1) {
-                __threadfence();
-                const float *all = a.part + (size_t)tile * a.splits * ncols * 128;
-                for (int c = 0; c < a.BN; ++c) {
-                    float v = 0.f, u = 0.f;
-                    for (int s = 0; s < a.splits; ++s) {
-                        v += __ldcg(all + ((size_t)s * ncols + c) * 128 + r);
-                        if (a.groups == 2) u += __ldcg(all + ((size_t)s * ncols + a.BN + c) * 128 + r);
-                    }
-                    epi_store(a, f, n0 + c, v, u);
-                }
-                if (threadIdx.x == 64) a.counter[tile] = 0u;
             }
         }
     }
@@ -248,6 +229,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     if (warp == 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
+}
+
+// Sum the split-K partial tiles in split order and apply the epilogue.  One
+// thread per (tile, token column, 4 consecutive features): reads are
+// 512-byte coalesced per column and every load of a thread is independent.
+__global__ void __launch_bounds__(256) k_splitk_reduce(TcArgs a, int mt) {
+    const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const int per_tile = a.BN * 32;
+    const int tile = (int)(idx / per_tile), rem = (int)(idx % per_tile);
+    const int c = rem >> 5, r = (rem & 31) * 4;
+    const int tx = tile % mt, ty = tile / mt;
+    const int t = ty * a.BN + c;
+    if (ty >= (a.T + a.BN - 1) / a.BN || t >= a.T) return;
+    const int ncols = a.groups * a.BN;
+    const float *base = a.part + (size_t)tile * a.splits * ncols * 128;
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+    for (int s = 0; s < a.splits; ++s) {
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(base + ((size_t)s * ncols + c) * 128 + r));
+        g.x += v.x; g.y += v.y; g.z += v.z; g.w += v.w;
+        if (a.groups == 2) {
+            const float4 w = __ldcg(reinterpret_cast<const float4 *>(base + ((size_t)s * ncols + a.BN + c) * 128 + r));
+            u.x += w.x; u.y += w.y; u.z += w.z; u.w += w.w;
+        }
+    }
+    const int f = (a.epi == EPI_SWIGLU_BF16 ? tx * 128 : tx * 128 * a.groups) + r;
+    epi_store(a, f, t, g.x, u.x);
+    epi_store(a, f + 1, t, g.y, u.y);
+    epi_store(a, f + 2, t, g.z, u.z);
+    epi_store(a, f + 3, t, g.w, u.w);
 }
 
 // ------------------------------------------------------------------ host side
@@ -322,8 +332,8 @@ TcPlan gemm_tc_plan(int T, int n_feat, int K, int groups, int num_sms, size_t sc
 }
 
 cudaError_t launch_gemm_tc(const void *X, int T, const void *W, int n_feat, int K, int groups, int epi, float *C,
-                           int ldc, void *Hout, int ldh, float *scratch, size_t scratch_floats, unsigned *counters,
-                           int *err, int num_sms, cudaStream_t s, int force_splits) {
+                           int ldc, void *Hout, int ldh, float *scratch, size_t scratch_floats, int *err, int num_sms,
+                           cudaStream_t s, int force_splits) {
     const TcPlan p = gemm_tc_plan(T, n_feat, K, groups, num_sms, scratch_floats, force_splits);
     if (!p.ok) return cudaErrorInvalidValue;
     CUtensorMap mA, mB;
@@ -346,13 +356,16 @@ cudaError_t launch_gemm_tc(const void *X, int T, const void *W, int n_feat, int 
     a.Hout = static_cast<__nv_bfloat16 *>(Hout);
     a.ldh = ldh;
     a.part = scratch;
-    a.counter = counters;
     a.err = err;
     // instruction descriptor: f32 accumulate, bf16 A and B, both K-major, N = BN, M = 128
     a.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(p.BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
     a.tmem_cols = (uint32_t)p.tmem_cols;
     dim3 grid(p.mt, p.nt, p.splits);
     k_gemm_tc<<<grid, kTcThreads, p.smem, s>>>(mA, mB, a);
+    if (p.splits > 1) {
+        const long long threads = (long long)p.mt * p.nt * p.BN * 32;
+        k_splitk_reduce<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(a, p.mt);
+    }
     return cudaPeekAtLastError();
 }
 

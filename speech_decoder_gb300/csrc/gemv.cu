@@ -46,10 +46,13 @@ __device__ __forceinline__ int xs_off(int k, int CPR) {
 }
 
 // Build the activation rows of this CTA's sequences in shared memory.  All
-// threads of the block take part.  Returns whether any row is live.
+// threads of the block take part.  Global loads are issued kPro at a time
+// before any of them is used.  Returns whether any row is live.
+constexpr int kPro = 8;
+
 template <typename TW, int IN>
 __device__ bool gemv_prologue(const GemvArgs &a, float *xs, int b0, int nb, int CPR, int *live_s, float *sred) {
-    const int K = a.K, tid = threadIdx.x;
+    const int K = a.K, tid = threadIdx.x, nt = blockDim.x;
     int any = 0;
     for (int bi = 0; bi < kGroupB; ++bi) {
         const int b = b0 + bi;
@@ -58,38 +61,63 @@ __device__ bool gemv_prologue(const GemvArgs &a, float *xs, int b0, int nb, int 
         if (tid == 0) live_s[bi] = live;
         if (!live) continue;                                    // uniform in the block
         float *xr = xs + (size_t)bi * K;
-        if (IN == IN_PLAIN) {
-            for (int k = tid; k < K; k += blockDim.x) xr[xs_off<TW>(k, CPR)] = a.in[(size_t)b * K + k];
-        } else if (IN == IN_SWIGLU) {
+        if (IN == IN_SWIGLU) {
             // packed gate|up: block j of 256 outputs = 128 gate rows, then the 128 up rows
             const float *gu = a.in + (size_t)b * 2 * a.ffn;
-            for (int f = tid; f < K; f += blockDim.x) {
-                const int blk = f >> 7, j = f & 127;
-                const float g = gu[blk * 256 + j], u = gu[blk * 256 + 128 + j];
-                xr[xs_off<TW>(f, CPR)] = g / (1.f + expf(-g)) * u;
-            }
-        } else {
-            float ss = 0.f;
-            if (IN == IN_EMBED_NORM) {
-                const TW *er = reinterpret_cast<const TW *>(a.embed) + (size_t)a.st->cur_tok[b] * K;
-                for (int k = tid; k < K; k += blockDim.x) {
-                    const float v = to_f32(er[k]);
-                    xr[xs_off<TW>(k, CPR)] = v;
-                    ss += v * v;
-                    if (blockIdx.x == 0) a.x_resid[(size_t)b * K + k] = v;
+            for (int f0 = tid; f0 < K; f0 += kPro * nt) {
+                float g[kPro], u[kPro];
+#pragma unroll
+                for (int i = 0; i < kPro; ++i) {
+                    const int f = f0 + i * nt, blk = f >> 7, j = f & 127;
+                    g[i] = f < K ? gu[blk * 256 + j] : 0.f;
+                    u[i] = f < K ? gu[blk * 256 + 128 + j] : 0.f;
                 }
-            } else {
-                for (int k = tid; k < K; k += blockDim.x) {
-                    const float v = a.in[(size_t)b * K + k];
-                    xr[xs_off<TW>(k, CPR)] = v;
-                    ss += v * v;
+#pragma unroll
+                for (int i = 0; i < kPro; ++i) {
+                    const int f = f0 + i * nt;
+                    if (f < K) xr[xs_off<TW>(f, CPR)] = g[i] / (1.f + expf(-g[i])) * u[i];
                 }
             }
-            ss = block_sum(ss, sred);
-            const float r = rsqrtf(ss / (float)K + a.eps);
-            for (int k = tid; k < K; k += blockDim.x) {
-                const int o = xs_off<TW>(k, CPR);
-                xr[o] = xr[o] * r * a.norm_w[k];
+            continue;
+        }
+        const float *src = IN == IN_EMBED_NORM ? nullptr : a.in + (size_t)b * K;
+        const TW *er = IN == IN_EMBED_NORM ? reinterpret_cast<const TW *>(a.embed) + (size_t)a.st->cur_tok[b] * K
+                                           : nullptr;
+        float ss = 0.f;
+        for (int k0 = tid; k0 < K; k0 += kPro * nt) {
+            float v[kPro];
+#pragma unroll
+            for (int i = 0; i < kPro; ++i) {
+                const int k = k0 + i * nt;
+                v[i] = k < K ? (IN == IN_EMBED_NORM ? to_f32(er[k]) : src[k]) : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < kPro; ++i) {
+                const int k = k0 + i * nt;
+                if (k < K) {
+                    xr[xs_off<TW>(k, CPR)] = v[i];
+                    ss += v[i] * v[i];
+                    if (IN == IN_EMBED_NORM && blockIdx.x == 0) a.x_resid[(size_t)b * K + k] = v[i];
+                }
+            }
+        }
+        if (IN == IN_PLAIN) continue;
+        ss = block_sum(ss, sred);
+        const float r = rsqrtf(ss / (float)K + a.eps);
+        for (int k0 = tid; k0 < K; k0 += kPro * nt) {
+            float w[kPro];
+#pragma unroll
+            for (int i = 0; i < kPro; ++i) {
+                const int k = k0 + i * nt;
+                w[i] = k < K ? a.norm_w[k] : 0.f;
+            }
+#pragma unroll
+            for (int i = 0; i < kPro; ++i) {
+                const int k = k0 + i * nt;
+                if (k < K) {
+                    const int o = xs_off<TW>(k, CPR);
+                    xr[o] = xr[o] * r * w[i];
+                }
             }
         }
     }
@@ -442,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_ldg(GemvArgs a) {
 }
 
 // ------------------------------------------------------------------ host side
-static int g_impl = 3;      // 1: registers, 2: ring fed by cp.async, 3: ring fed by 1-D TMA
+static int g_impl = 1;      // 1: registers, 2: ring fed by cp.async, 3: ring fed by 1-D TMA
 static int g_ring_slots = 3;
 void gemv_set_impl(int impl) {
     if (impl >= 1 && impl <= 3) g_impl = impl;

@@ -194,17 +194,48 @@ __global__ void __launch_bounds__(256) k_attn_prefill_simt(AttnPrefillArgs a, fl
     const TKV *Kc = reinterpret_cast<const TKV *>(a.Kc) + ((size_t)g * a.slots + slot0) * D + lane * PL;
     const TKV *Vc = reinterpret_cast<const TKV *>(a.Vc) + ((size_t)g * a.slots + slot0) * D + lane * PL;
     float m = -INFINITY, l = 0.f, acc[PL] = {};
-    for (int j = 0; j <= pos; ++j) {
-        float d = 0.f;
+    constexpr int KB = 8;                 // keys per batch: all loads issued before use
+    for (int jb = 0; jb <= pos; jb += KB) {
+        float kf[KB][PL], vf[KB][PL], sc[KB];
 #pragma unroll
-        for (int e = 0; e < PL; ++e) d = fmaf(qf[e], to_f32(Kc[(size_t)j * D + e]), d);
-        const float sc = warp_sum(d) * scale;
-        const float mn = fmaxf(m, sc);
-        const float corr = expf(m - mn), p = expf(sc - mn);
-        l = l * corr + p;
+        for (int k = 0; k < KB; ++k) {
+            const int j = jb + k;
 #pragma unroll
-        for (int e = 0; e < PL; ++e) acc[e] = fmaf(p, to_f32(Vc[(size_t)j * D + e]), acc[e] * corr);
-        m = mn;
+            for (int e = 0; e < PL; ++e) {
+                kf[k][e] = j <= pos ? to_f32(Kc[(size_t)j * D + e]) : 0.f;
+                vf[k][e] = j <= pos ? to_f32(Vc[(size_t)j * D + e]) : 0.f;
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < KB; ++k) {
+            float d = 0.f;
+#pragma unroll
+            for (int e = 0; e < PL; ++e) d = fmaf(qf[e], kf[k][e], d);
+            sc[k] = d;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int k = 0; k < KB; ++k) sc[k] += __shfl_xor_sync(0xffffffffu, sc[k], o);
+        float mb = m;
+#pragma unroll
+        for (int k = 0; k < KB; ++k) {
+            sc[k] = jb + k <= pos ? sc[k] * scale : -INFINITY;
+            mb = fmaxf(mb, sc[k]);
+        }
+        const float corr = expf(m - mb);
+        float ls = 0.f;
+#pragma unroll
+        for (int e = 0; e < PL; ++e) acc[e] *= corr;
+#pragma unroll
+        for (int k = 0; k < KB; ++k) {
+            const float p = expf(sc[k] - mb);
+            ls += p;
+#pragma unroll
+            for (int e = 0; e < PL; ++e) acc[e] = fmaf(p, vf[k][e], acc[e]);
+        }
+        l = l * corr + ls;
+        m = mb;
     }
     TO *o = reinterpret_cast<TO *>(a.o) + (size_t)t * a.nq * D + (size_t)h * D + lane * PL;
     const float inv = 1.f / l;
