@@ -119,7 +119,7 @@ class Clocks:
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
-    for f in ("decode.cu", "decode.cuh", "common.cuh"):
+    for f in ("gemv.cu", "decode.cuh", "common.cuh"):
         with open(os.path.join(ROOT, "speech_decoder_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -146,12 +146,12 @@ def workload_inputs(wl, w):
     return items
 
 
-def decode_bytes_per_step(spec, kv_len_mean: float) -> float:
-    """Algorithmic HBM bytes of one decode step of one sequence: every weight
-    once (bf16) plus the K and V rows read by attention (fp16)."""
+def decode_bytes_per_step(spec, kv_len_mean: float, batch: int = 1) -> float:
+    """Algorithmic HBM bytes of one decode step: every weight once (bf16)
+    plus the K and V rows each sequence's attention reads (fp16)."""
     H, F, d, nq, nkv, L = spec.hidden, spec.ffn, spec.head_dim, spec.n_heads, spec.n_kv_heads, spec.n_layers
     per_layer = ((nq + 2 * nkv) * d * H + H * nq * d + 2 * F * H + H * F) * 2
-    return L * per_layer + spec.vocab * H * 2 + L * 2 * nkv * d * 2 * kv_len_mean
+    return L * per_layer + spec.vocab * H * 2 + batch * L * 2 * nkv * d * 2 * kv_len_mean
 
 
 # ---------------------------------------------------------------- our arm
@@ -171,26 +171,39 @@ def run_ours(args):
 
     wl = synth.workload(args.workload)
     spec = wl.model
-    if wl.batch != 1:
-        raise SystemExit(f"workload {wl.name}: batched bench path not built")
     w = synth.model_weights(spec, seed=wl.seed)
-    item = workload_inputs(wl, w)[0]
-    pr = wl.prompts[0]
-    T = pr.T
+    items = workload_inputs(wl, w)
+    B = wl.batch
+    Ts = [p.T for p in wl.prompts]
+    T_all = sum(Ts)
     max_new = wl.steps + 1                      # the prefill's token counts toward the budget
-    dec = Decoder(spec, w, max_ctx=T + max_new, max_new=max_new, eos_id=wl.eos_id, device=dev)
+    dec = Decoder(spec, w, max_ctx=max(Ts) + max_new, max_batch=B, max_tokens=T_all, max_new=max_new,
+                  eos_id=wl.eos_id, device=dev)
     del w
     stream = dec.stream
-    ids_dev = torch.from_numpy(item["ids"]).to(dev)
-    audio_dev = torch.from_numpy(item["audio"]).to(dev)
+    ids_np = np.concatenate([it["ids"] for it in items]).astype(np.int32)
+    audio_np = np.concatenate([it["audio"] for it in items]).astype(np.float32)
+    cu_ids = np.zeros(B + 1, np.int32)
+    cu_ids[1:] = np.cumsum([len(it["ids"]) for it in items])
+    cu_au = np.zeros(B + 1, np.int32)
+    cu_au[1:] = np.cumsum([it["audio"].shape[0] for it in items])
+    pre_lens = np.array([it["prefix_len"] for it in items], np.int32)
+    ids_dev = torch.from_numpy(ids_np).to(dev)
+    audio_dev = torch.from_numpy(audio_np).to(dev)
+    torch.cuda.synchronize()
 
-    def utterance(ids, audio):
-        dec.prefill_ids(ids, audio, item["prefix_len"])
-        out, _ = dec.generate(max_new)
-        return out
+    def utterance(ids, audio, on_device):
+        """One pass of the hot path: prefill every item, then the greedy loop."""
+        if B == 1:
+            dec.prefill_ids(ids, audio, int(pre_lens[0]))
+            out, _ = dec.generate(max_new)
+            return len(out) - 1
+        dec.prefill_ids_batch_ptr(ids.data_ptr(), cu_ids, audio.data_ptr(), cu_au, pre_lens, int(on_device))
+        res = dec.generate_batch(max_new, B)
+        return sum(len(r[0]) - 1 for r in res)
 
     for _ in range(args.warmup):
-        utterance(ids_dev, audio_dev)
+        utterance(ids_dev, audio_dev, True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -200,11 +213,11 @@ def run_ours(args):
     pre_ms, gen_ms, n_tok = 0.0, 0.0, 0
     e0.record(stream)
     for _ in range(args.steps):
-        out = utterance(ids_dev, audio_dev)
+        n = utterance(ids_dev, audio_dev, True)
         p, g = dec.timings()
         pre_ms += p
         gen_ms += g
-        n_tok += len(out) - 1
+        n_tok += n
     e1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -213,7 +226,7 @@ def run_ours(args):
     clk = clocks.stop() if clocks else None
     total_ms = e0.elapsed_time(e1)
     vals = torch.tensor([total_ms, gen_ms, pre_ms], dtype=torch.float64, device=dev)
-    toks = torch.tensor([n_tok, args.steps * T], dtype=torch.float64, device=dev)
+    toks = torch.tensor([n_tok, args.steps * T_all], dtype=torch.float64, device=dev)
     if world > 1:
         torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
         torch.distributed.all_reduce(toks, op=torch.distributed.ReduceOp.SUM)
@@ -222,41 +235,55 @@ def run_ours(args):
     decode_tok_s = n_tok_all / (gen_ms / 1e3)
     prefill_tok_s = n_pre_all / (pre_ms / 1e3)
 
-    # dominant kernel: the RMSNorm + projection GEMV (q|k|v and gate|up), timed alone
+    # dominant kernel: the projection kernel of the decode step, timed alone
     hbm, bf16_peak, peak_kind = peaks()
-    dec.prefill_ids(ids_dev, audio_dev, item["prefix_len"])
+    utterance(ids_dev, audio_dev, True)
+    if B == 1:
+        dec.prefill_ids(ids_dev, audio_dev, int(pre_lens[0]))
+        kname = "k_gemv_ldg<bf16, IN_NORM, OUT_STORE> (q|k|v and gate|up GEMV, one launch per layer)"
+    else:
+        dec.prefill_ids_batch_ptr(ids_dev.data_ptr(), cu_ids, audio_dev.data_ptr(), cu_au, pre_lens, 1)
+        kname = "k_gemm_tc + k_splitk_reduce (q|k|v and gate|up projections of %d rows, per projection)" % B
     kms, kbytes = dec.profile_kernel(0, 10)
     achieved = kbytes / (kms / 1e3) / 1e9
-    roof = {"kernel": "k_gemv<bf16, IN_NORM, OUT_STORE> (q|k|v and gate|up)", "bound": "hbm",
+    roof = {"kernel": kname, "bound": "hbm",
             "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
             "peak_source": peak_kind, "bytes_per_launch": int(kbytes), "avg_launch_us": round(kms * 1e3, 2),
-            "traffic": ncu_traffic()}
-    step_bytes = decode_bytes_per_step(spec, T + wl.steps / 2)
-    step_ms = gen_ms / max(1, n_tok) if world == 1 else gen_ms / max(1, n_tok_all / world)
+            "traffic": ncu_traffic() if B == 1 else None}
+    kv_mean = float(np.mean([t + wl.steps / 2 for t in Ts]))
+    step_bytes = decode_bytes_per_step(spec, kv_mean, B)
+    steps_done = n_tok / B
+    step_ms = gen_ms / max(1.0, steps_done)
     step_roof = {"bytes_per_step": int(step_bytes), "achieved": round(step_bytes / (step_ms / 1e3) / 1e9, 1),
                  "frac": round(step_bytes / (step_ms / 1e3) / 1e9 / hbm, 4)}
 
     e2e = None
     if not args.no_e2e:
-        ids_h = torch.from_numpy(item["ids"]).pin_memory()
-        audio_h = torch.from_numpy(item["audio"]).pin_memory()
-        utterance(ids_h, audio_h)
+        ids_h = torch.from_numpy(ids_np).pin_memory()
+        audio_h = torch.from_numpy(audio_np).pin_memory()
+        utterance(ids_h, audio_h, False)
         torch.cuda.synchronize()
         t_pre, t_gen, n_e = 0.0, 0.0, 0
         reps = max(1, args.steps)
         for _ in range(reps):
             t0 = time.perf_counter()
-            dec.prefill_ids(ids_h, audio_h, item["prefix_len"])
+            if B == 1:
+                dec.prefill_ids(ids_h, audio_h, int(pre_lens[0]))
+            else:
+                dec.prefill_ids_batch_ptr(ids_h.data_ptr(), cu_ids, audio_h.data_ptr(), cu_au, pre_lens, 0)
             t1 = time.perf_counter()
-            out, _ = dec.generate(max_new)
+            if B == 1:
+                out, _ = dec.generate(max_new)
+                n_e += len(out) - 1
+            else:
+                n_e += sum(len(r[0]) - 1 for r in dec.generate_batch(max_new, B))
             t2 = time.perf_counter()
             t_pre += t1 - t0
             t_gen += t2 - t1
-            n_e += len(out) - 1
         e2e = {"value": round(n_e * world / t_gen, 1), "unit": "tok/s",
-               "prefill_tok_s": round(reps * T * world / t_pre, 1),
+               "prefill_tok_s": round(reps * T_all * world / t_pre, 1),
                "h2d_bytes_per_step": int(ids_h.numel() * 4 + audio_h.numel() * 4),
-               "d2h_bytes_per_step": int(4 + 4 * max_new)}
+               "d2h_bytes_per_step": int(B * (4 + 4 * max_new))}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -268,11 +295,12 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded random-init weights N(0,0.02), encoder rows N(0,1))",
-            "config": {"workload": wl.name, "prompt_rows": T, "layout": [pr.prefix_len, pr.n_audio, pr.suffix_len],
+            "config": {"workload": wl.name, "prompt_rows": T_all,
+                       "layout": [[p.prefix_len, p.n_audio, p.suffix_len] for p in wl.prompts][:4],
                        "decode_steps": wl.steps, "batch": wl.batch, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2: every step streams 3.4 GB of weights"},
             "prefill": {"value": round(prefill_tok_s, 1), "unit": "tok/s", "ms": round(pre_ms / args.steps, 3)},
-            "decode_ms_per_token": round(gen_ms / max(1, n_tok), 4),
+            "decode_ms_per_step": round(step_ms, 4),
             "roofline": roof, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clk, "gpu_launches": int(launches),
         }

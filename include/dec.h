@@ -142,6 +142,17 @@ dec_status dec_prefill_ids(dec_handle *h, const int32_t *ids, int32_t n_ids, con
 dec_status dec_prefill_batch(dec_handle *h, const float *embeds, const int32_t *cu_seqlens,
                              int32_t B, int32_t on_device, int32_t *first_tokens);
 
+/* Ragged batched form of dec_prefill_ids: item b has token ids
+ * ids[cu_ids[b] .. cu_ids[b+1]) and encoder rows audio[cu_audio[b] ..
+ * cu_audio[b+1]) (float32 rows of width H), assembled on the device as
+ * embed[ids[:prefix_lens[b]]] | audio rows | embed[ids[prefix_lens[b]:]].
+ * cu_ids, cu_audio: int32 [B+1] and prefix_lens: int32 [B], host memory; ids
+ * and audio in host or device memory per on_device.  first_tokens: int32 [B]. */
+dec_status dec_prefill_ids_batch(dec_handle *h, const int32_t *ids, const int32_t *cu_ids,
+                                 const float *audio, const int32_t *cu_audio,
+                                 const int32_t *prefix_lens, int32_t B, int32_t on_device,
+                                 int32_t *first_tokens);
+
 /* One greedy step of sequence 0: `token` at position n_past, its K/V written
  * at slot n_past, returns the argmax of the logits (decoder.cpp,
  * build_step_graph).  DEC_ERR_STATE before a prefill; DEC_ERR_INPUT_TOO_LONG

@@ -23,7 +23,7 @@ DEC_BF16, DEC_F32, DEC_F16 = 0, 1, 2
 
 EXPORTS = [
     "dec_workspace_size", "dec_create", "dec_destroy", "dec_reset", "dec_prefill", "dec_prefill_ids",
-    "dec_prefill_batch", "dec_step", "dec_step_batch", "dec_generate", "dec_generate_batch",
+    "dec_prefill_batch", "dec_prefill_ids_batch", "dec_step", "dec_step_batch", "dec_generate", "dec_generate_batch",
     "dec_debug_logits", "dec_set_dumps", "dec_debug_dump", "dec_launch_count", "dec_last_timings",
     "dec_last_error", "dec_status_string", "dec_profile_kernel", "dec_attn_decode_scratch_size",
     "dec_attn_decode", "dec_attn_decode_noalloc", "dec_debug_gemm",
@@ -77,6 +77,8 @@ def load_library():
         "dec_prefill_ids": ([H, c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32, POINTER(c_int32)],
                             c_int32),
         "dec_prefill_batch": ([H, c_void_p, c_void_p, c_int32, c_int32, c_void_p], c_int32),
+        "dec_prefill_ids_batch": ([H, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_void_p],
+                                  c_int32),
         "dec_step": ([H, c_int32, POINTER(c_int32)], c_int32),
         "dec_step_batch": ([H, c_void_p, c_void_p, c_void_p], c_int32),
         "dec_generate": ([H, c_int32, c_void_p, POINTER(c_int32)], c_int32),
@@ -218,6 +220,40 @@ class Decoder:
         self._check(self.lib.dec_prefill_ids(self.h, ip, n_ids, p, int(audio.shape[0]), prefix_len, dev,
                                              byref(tok)))
         return tok.value
+
+    def prefill_ids_batch(self, ids_list, audio_list, prefix_lens, on_device: bool = False) -> np.ndarray:
+        """Ragged batch of (ids, encoder rows, prefix_len) items, assembled on the device."""
+        t = self.torch
+        cu_ids = np.zeros(len(ids_list) + 1, np.int32)
+        cu_ids[1:] = np.cumsum([len(i) for i in ids_list])
+        cu_au = np.zeros(len(audio_list) + 1, np.int32)
+        cu_au[1:] = np.cumsum([int(a.shape[0]) for a in audio_list])
+        pre = np.ascontiguousarray(prefix_lens, dtype=np.int32)
+        ids = np.concatenate([np.asarray(i, np.int32) for i in ids_list]).astype(np.int32)
+        audio = np.concatenate([np.asarray(a, np.float32) for a in audio_list]).astype(np.float32)
+        if on_device:
+            ids_t = t.from_numpy(ids).to(self.device)
+            au_t = t.from_numpy(audio).to(self.device)
+            self.stream.wait_stream(t.cuda.current_stream(self.device))
+            ip, ap, keep = ids_t.data_ptr(), au_t.data_ptr(), (ids_t, au_t)
+        else:
+            ip, ap, keep = ids.ctypes.data, audio.ctypes.data, (ids, audio)
+        out = np.zeros(len(ids_list), np.int32)
+        self._check(self.lib.dec_prefill_ids_batch(self.h, ip, cu_ids.ctypes.data, ap, cu_au.ctypes.data,
+                                                   pre.ctypes.data, len(ids_list), int(on_device),
+                                                   out.ctypes.data))
+        return out
+
+    def prefill_ids_batch_ptr(self, ids_ptr, cu_ids, audio_ptr, cu_audio, prefix_lens, on_device: int) -> np.ndarray:
+        """Same, with caller-owned data pointers (device or pinned host)."""
+        cu_ids = np.ascontiguousarray(cu_ids, np.int32)
+        cu_audio = np.ascontiguousarray(cu_audio, np.int32)
+        pre = np.ascontiguousarray(prefix_lens, np.int32)
+        out = np.zeros(len(pre), np.int32)
+        self._check(self.lib.dec_prefill_ids_batch(self.h, ids_ptr, cu_ids.ctypes.data, audio_ptr,
+                                                   cu_audio.ctypes.data, pre.ctypes.data, len(pre), on_device,
+                                                   out.ctypes.data))
+        return out
 
     def prefill_batch(self, embeds_list) -> np.ndarray:
         lens = [int(e.shape[0]) for e in embeds_list]

@@ -236,8 +236,59 @@ static void gemm_swiglu(dec_handle *h, const void *A, const void *Wgu, int M, in
     }
 }
 
+// Batched step rows go through the tensor-core GEMM once there are more
+// sequences than one GEMV CTA keeps in shared memory.
+static bool batched_path(const dec_handle *h, int B) {
+    return B > kGroupB && h->use_tc && h->w_bf16 && gemm_tc_ready();
+}
+
+static void enqueue_decode_layer_tc(dec_handle *h, int l, int B, bool from_embed) {
+    const dec_hparams &hp = h->hp;
+    const DevLayer &L = h->L[l];
+    const int H = hp.hidden, F = hp.ffn, nqd = hp.n_heads * hp.head_dim;
+    cudaStream_t s = h->stream;
+    if (from_embed && l == 0) {
+        launch_embed_rows(h->embed, h->w_bf16, h->st, h->xd, B, H, s);
+        h->enq++;
+    }
+    launch_rmsnorm_rows(h->xd, L.attn_norm, hp.rms_eps, h->xn, true, B, H, s);
+    h->enq++;
+    gemm(h, h->xn, L.wqkv, h->qkvd, qkv_rows(hp), B, qkv_rows(hp), H, EPI_STORE_F32);
+
+    AttnDecArgs a{};
+    a.qkv = h->qkvd;
+    a.qn_w = L.qn;
+    a.kn_w = L.kn;
+    a.eps = hp.rms_eps;
+    a.rope = h->rope;
+    a.Kc = L.K;
+    a.Vc = L.V;
+    a.slots = (int)h->slots;
+    a.o = h->od;
+    a.o_bf16 = static_cast<__nv_bfloat16 *>(h->attn_o);
+    a.part = h->attn_part;
+    a.counter = h->attn_counter;
+    a.st = h->st;
+    a.nq = hp.n_heads;
+    a.nkv = hp.n_kv_heads;
+    a.d = hp.head_dim;
+    a.B = B;
+    a.append = 1;
+    launch_attn_decode(h->kv_f16, a, splits_for(h, B), s);
+    h->enq++;
+    gemm(h, h->attn_o, L.wo, h->xd, H, B, H, nqd, EPI_RESID_F32);
+    launch_rmsnorm_rows(h->xd, L.ffn_norm, hp.rms_eps, h->xn, true, B, H, s);
+    h->enq++;
+    gemm_swiglu(h, h->xn, L.wgu, B, F, H);
+    gemm(h, h->hbuf, L.wd, h->xd, H, B, H, F, EPI_RESID_F32);
+}
+
 // One decoder block for the step rows in xd (one row per sequence).
 static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
+    if (batched_path(h, B)) {
+        enqueue_decode_layer_tc(h, l, B, from_embed);
+        return;
+    }
     const dec_hparams &hp = h->hp;
     const DevLayer &L = h->L[l];
     const int H = hp.hidden, F = hp.ffn, nqd = hp.n_heads * hp.head_dim;
@@ -310,6 +361,14 @@ static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
 }
 
 static void enqueue_head(dec_handle *h, int B) {
+    if (batched_path(h, B)) {
+        const dec_hparams &hp = h->hp;
+        launch_rmsnorm_rows(h->xd, h->final_norm, hp.rms_eps, h->xn, true, B, hp.hidden, h->stream);
+        gemm(h, h->xn, h->embed, h->logits, hp.vocab, B, hp.vocab, hp.hidden, EPI_STORE_F32);
+        launch_argmax_rows(h->logits, B, hp.vocab, h->st, h->out_ids, hp.max_new, h->stream);
+        h->enq += 2;
+        return;
+    }
     GemvArgs g{};
     g.st = h->st;
     g.B = B;
@@ -771,6 +830,47 @@ dec_status dec_prefill_ids(dec_handle *h, const int32_t *ids, int32_t n_ids, con
     return timed_prefill(h, cu, 1, first_token);
 }
 
+dec_status dec_prefill_ids_batch(dec_handle *h, const int32_t *ids, const int32_t *cu_ids, const float *audio,
+                                 const int32_t *cu_audio, const int32_t *prefix_lens, int32_t B, int32_t on_device,
+                                 int32_t *first_tokens) {
+    if (!h || !cu_ids || !cu_audio || !prefix_lens || !first_tokens || B < 1 || B > h->hp.max_batch)
+        return fail(h, DEC_ERR_INVALID_ARG, "bad prefill_ids_batch arguments");
+    if (cu_ids[0] != 0 || cu_audio[0] != 0) return fail(h, DEC_ERR_INVALID_ARG, "offsets must start at 0");
+    std::vector<int32_t> cu(B + 1, 0);
+    for (int b = 0; b < B; ++b) {
+        const int ni = cu_ids[b + 1] - cu_ids[b], na = cu_audio[b + 1] - cu_audio[b];
+        if (ni < 0 || na < 0 || prefix_lens[b] < 0 || prefix_lens[b] > ni || ni + na < 1)
+            return fail(h, DEC_ERR_INVALID_ARG, "bad item lengths");
+        cu[b + 1] = cu[b] + ni + na;
+    }
+    if ((cu_ids[B] > 0 && !ids) || (cu_audio[B] > 0 && !audio)) return fail(h, DEC_ERR_INVALID_ARG, "null data");
+    dec_status rc = check_lengths(h, cu.data(), B);
+    if (rc != DEC_OK) return rc;
+    const int n_ids = cu_ids[B];
+    if (n_ids > 0) {
+        std::vector<int32_t> hid(n_ids);
+        if (on_device) CK(cudaMemcpy(hid.data(), ids, (size_t)n_ids * 4, cudaMemcpyDeviceToHost));
+        else std::memcpy(hid.data(), ids, (size_t)n_ids * 4);
+        for (int i = 0; i < n_ids; ++i)
+            if (hid[i] < 0 || hid[i] >= h->hp.vocab) return fail(h, DEC_ERR_INVALID_ARG, "token id out of range");
+        CK(cudaMemcpyAsync(h->ids_dev, hid.data(), (size_t)n_ids * 4, cudaMemcpyHostToDevice, h->stream));
+        CK(cudaStreamSynchronize(h->stream));
+    }
+    const size_t H = h->hp.hidden;
+    for (int b = 0; b < B; ++b) {
+        const int na = cu_audio[b + 1] - cu_audio[b], T = cu[b + 1] - cu[b];
+        float *span = h->x + ((size_t)cu[b] + prefix_lens[b]) * H;
+        if (na > 0) {
+            rc = copy_in(h, span, audio + (size_t)cu_audio[b] * H, (size_t)na * H * 4, on_device);
+            if (rc != DEC_OK) return rc;
+        }
+        launch_assemble(h->embed, h->w_bf16, h->ids_dev + cu_ids[b], span, h->x + (size_t)cu[b] * H, T, na,
+                        prefix_lens[b], (int)H, h->stream);
+        h->launches++;
+    }
+    return timed_prefill(h, cu.data(), B, first_tokens);
+}
+
 dec_status dec_prefill_batch(dec_handle *h, const float *embeds, const int32_t *cu_seqlens, int32_t B,
                              int32_t on_device, int32_t *first_tokens) {
     if (!h || !embeds || !cu_seqlens || !first_tokens) return fail(h, DEC_ERR_INVALID_ARG, "null argument");
@@ -926,7 +1026,14 @@ dec_status dec_profile_kernel(dec_handle *h, int32_t op, int32_t iters, float *a
         }
         for (int l = 0; l < hp.n_layers; ++l) {
             const DevLayer &L = h->L[l];
-            if (op == 0) {
+            if (op == 0 && batched_path(h, B)) {
+                // tensor-core projections of the batched step (GEMM + split-K reduction each)
+                gemm(h, h->xn, L.wqkv, h->qkvd, qkv_rows(hp), B, qkv_rows(hp), H, EPI_STORE_F32);
+                bytes += (double)qkv_rows(hp) * H * ws + (double)B * H * 2.0 + (double)B * qkv_rows(hp) * 4.0;
+                gemm_swiglu(h, h->xn, L.wgu, B, F, H);
+                bytes += (double)2 * F * H * ws + (double)B * H * 2.0 + (double)B * F * 2.0;
+                launches += 2;
+            } else if (op == 0) {
                 GemvArgs g{};
                 g.st = h->st;
                 g.B = B;

@@ -219,7 +219,9 @@ __global__ void __launch_bounds__(128) k_attn_decode(AttnDecArgs a, float scale)
         float A = 0.f;
 #pragma unroll 4
         for (int t = 0; t < n_used; ++t) A = fmaf(__ldcg(pb + ((size_t)t * n_rep + r) * (D + 2) + i), cw[t][r], A);
-        a.o[(size_t)b * a.nq * D + (size_t)(g * n_rep + r) * D + i] = A;
+        const size_t oi = (size_t)b * a.nq * D + (size_t)(g * n_rep + r) * D + i;
+        a.o[oi] = A;
+        if (a.o_bf16) a.o_bf16[oi] = __float2bfloat16_rn(A);
     }
     if (tid == 0) a.counter[b * nkv + g] = 0u;
 }
@@ -299,6 +301,69 @@ cudaError_t attn_op_launch(const float *q, const void *K, const void *V, bool kv
     a.kv_len = kv_len;
     launch_attn_decode_plain(kv_f16, a, S, s);
     return cudaGetLastError();
+}
+
+// ============================================================== batched-step helpers
+template <typename TW>
+__global__ void k_embed_rows(const TW *embed, SeqState *st, float *x, int H) {
+    const int b = blockIdx.x;
+    ptx::pdl_launch();
+    ptx::pdl_wait();
+    if (!row_live(st, b)) return;
+    const TW *src = embed + (size_t)st->cur_tok[b] * H;
+    for (int k = threadIdx.x; k < H; k += blockDim.x) x[(size_t)b * H + k] = to_f32(src[k]);
+}
+
+void launch_embed_rows(const void *embed, bool w_bf16, SeqState *st, float *x, int B, int H, cudaStream_t s) {
+    if (w_bf16) k_embed_rows<__nv_bfloat16><<<B, 256, 0, s>>>((const __nv_bfloat16 *)embed, st, x, H);
+    else k_embed_rows<float><<<B, 256, 0, s>>>((const float *)embed, st, x, H);
+}
+
+// One CTA per row: strict '>' scan per thread over ascending indices, then a
+// tie-aware block reduction (lowest index wins), then the greedy-state update.
+__global__ void __launch_bounds__(512) k_argmax_rows(const float *logits, int V, SeqState *st, int32_t *out_ids,
+                                                     int out_ids_cap) {
+    __shared__ float rv[16];
+    __shared__ int ri[16];
+    const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    ptx::pdl_launch();
+    ptx::pdl_wait();
+    if (!row_live(st, b)) return;
+    const float *row = logits + (size_t)b * V;
+    float bv = -INFINITY;
+    int bix = 0x7fffffff;
+    for (int i = tid; i < V; i += blockDim.x) {
+        const float v = __ldcg(row + i);
+        if (v > bv) { bv = v; bix = i; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float v = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int ix = __shfl_xor_sync(0xffffffffu, bix, o);
+        if (v > bv || (v == bv && ix < bix)) { bv = v; bix = ix; }
+    }
+    if (lane == 0) { rv[warp] = bv; ri[warp] = bix; }
+    __syncthreads();
+    if (tid == 0) {
+        for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
+            if (rv[w] > bv || (rv[w] == bv && ri[w] < bix)) { bv = rv[w]; bix = ri[w]; }
+        if (bix < 0 || bix >= V) {
+            atomicCAS(&st->error, 0, 2);
+            bix = 0;
+        }
+        st->cur_tok[b] = bix;
+        const int gcount = st->gen[b];
+        if (gcount < out_ids_cap) out_ids[(size_t)b * out_ids_cap + gcount] = bix;
+        st->gen[b] = gcount + 1;
+        const int np = st->n_past[b] + 1;
+        st->n_past[b] = np;
+        if (bix == st->eos_id || gcount + 1 >= st->max_new || np + 1 > st->kv_cap[b]) st->done[b] = 1;
+    }
+}
+
+void launch_argmax_rows(const float *logits, int B, int V, SeqState *st, int32_t *out_ids, int out_ids_cap,
+                        cudaStream_t s) {
+    k_argmax_rows<<<B, 512, 0, s>>>(logits, V, st, out_ids, out_ids_cap);
 }
 
 }  // namespace dec

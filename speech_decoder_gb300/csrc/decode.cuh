@@ -59,7 +59,15 @@ struct AttnDecArgs {
     const float *q_plain;   // [B, nq, d]
     const int32_t *kv_off;  // [B] first slot of each sequence
     const int32_t *kv_len;  // [B] visible keys (rows with len <= 0 or out of range are skipped)
+    __nv_bfloat16 *o_bf16;  // optional bf16 copy of o (input of the tensor-core O projection)
 };
+
+// Batched-step helpers (rows of several sequences through the tensor-core GEMM):
+// x[b] = embed[cur_tok[b]] for live rows; row argmax of logits [B, V] that
+// advances the greedy state exactly as the GEMV head does.
+void launch_embed_rows(const void *embed, bool w_bf16, SeqState *st, float *x, int B, int H, cudaStream_t s);
+void launch_argmax_rows(const float *logits, int B, int V, SeqState *st, int32_t *out_ids, int out_ids_cap,
+                        cudaStream_t s);
 
 void launch_gemv(int in_mode, int out_mode, bool w_bf16, const GemvArgs &a, int grid_x,
                  cudaStream_t s);

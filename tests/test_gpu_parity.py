@@ -251,3 +251,45 @@ def test_budget_and_kv_full(small):
     with pytest.raises(DecError) as e:
         dec.step(3)
     assert e.value.status == DEC_ERR_INPUT_TOO_LONG
+
+
+# ------------------------------------------------------------------ batched rows on the tensor-core path (B > 4)
+def test_batched_tc_path_prefill_steps_generate(small):
+    spec, w = small
+    rng = np.random.default_rng(21)
+    prompts = [synth.Prompt(int(rng.integers(0, 5)), int(rng.integers(1, 90)), int(rng.integers(0, 4)))
+               for _ in range(7)]
+    embs = [prompt_rows(spec, w, p, seed=22, item=i)[0] for i, p in enumerate(prompts)]
+    dec = make(spec, w, max_ctx=128, max_batch=8, max_tokens=1024, max_new=10)
+    first = dec.prefill_batch(embs)
+    got = dec.logits(7)
+    orcs = [O.Oracle(spec, w, e.shape[0] + 10) for e in embs]
+    refs = [o.prefill(e) for o, e in zip(orcs, embs)]
+    toks = []
+    for b in range(7):
+        assert rel_err(got[b], refs[b]) <= TOL_BF16
+        assert token_ok(int(first[b]), refs[b], got[b])
+        toks.append(O.argmax_lowest(refs[b]))
+    for step in range(4):
+        active = np.ones(7, np.uint8)
+        active[step % 7] = 0
+        nxt = dec.step_batch(np.array(toks, np.int32), active)
+        got = dec.logits(7)
+        for b in range(7):
+            if not active[b]:
+                assert nxt[b] == -1
+                continue
+            ref = orcs[b].step(toks[b])
+            assert rel_err(got[b], ref) <= TOL_BF16, (step, b)
+            assert token_ok(int(nxt[b]), ref, got[b])
+            toks[b] = O.argmax_lowest(ref)
+    # greedy loop with per-item EOS on the same path
+    probe, _, _ = O.greedy(O.Oracle(spec, w, embs[2].shape[0] + 10), embs[2], 10)
+    ks = [i for i in range(1, len(probe)) if probe[i] not in probe[:i]]
+    eos = probe[ks[0]] if ks else -1
+    dec2 = make(spec, w, max_ctx=128, max_batch=8, max_tokens=1024, max_new=10, eos_id=eos)
+    dec2.prefill_batch(embs)
+    out = dec2.generate_batch(10, 7)
+    for b in range(7):
+        rids, rtrunc, _ = O.greedy(O.Oracle(spec, w, embs[b].shape[0] + 10), embs[b], 10, eos_id=eos)
+        assert out[b][0] == rids and out[b][1] == rtrunc, (b, out[b], rids)
