@@ -210,7 +210,9 @@ dec_status dec_last_timings(const dec_handle *h, float *prefill_ms, float *gener
  * per layer, so consecutive launches stream different weights and no
  * launch is served from L2).  op 0: the RMSNorm + projection GEMV (q|k|v
  * and gate|up of every layer); op 1: the lm_head + argmax GEMV; op 2: the
- * split-KV attention at the current lengths.  Needs a prior prefill (it
+ * split-KV attention at the current lengths; op 3: one whole decode step
+ * (the persistent step kernel when it is in use; *avg_ms is then per step
+ * and *bytes_per_launch the step's algorithmic bytes).  Needs a prior prefill (it
  * reads and rewrites the step buffers; the KV cache and sequence state are
  * left as they were).  *avg_ms = mean duration of one launch;
  * *bytes_per_launch = algorithmic bytes one launch must move (weights,

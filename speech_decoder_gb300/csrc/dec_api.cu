@@ -16,6 +16,7 @@
 #include "decode.cuh"
 #include "gemm_tc.cuh"
 #include "prefill.cuh"
+#include "step.cuh"
 
 using namespace dec;
 
@@ -94,6 +95,10 @@ struct dec_handle {
     bool own_stream = false;
     int gemv_ctas = 1;              // GEMV CTAs per SM
     float *tc_scratch = nullptr;    // split-K partial tiles of the tensor-core GEMM
+    // persistent step kernel
+    StepLayer *step_layers = nullptr;
+    unsigned long long *step_bar = nullptr;
+    bool use_step = false;
 };
 
 // ------------------------------------------------------------------ helpers
@@ -202,6 +207,8 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     h->out_ids = b.take<int32_t>(Bm * hp.max_new);
     h->st = b.take<SeqState>(1);
     h->tc_scratch = b.take<float>(kTcScratchFloats);
+    h->step_layers = b.take<StepLayer>(hp.n_layers);
+    h->step_bar = b.take<unsigned long long>(1);
     h->dump_inj = b.take<float>(Tm * H);
     h->dump_b0 = b.take<float>(Tm * H);
     h->dump_blast = b.take<float>(Bm * H);
@@ -388,7 +395,50 @@ static void enqueue_head(dec_handle *h, int B) {
     h->enq++;
 }
 
+static StepArgs step_args(dec_handle *h, int B) {
+    const dec_hparams &hp = h->hp;
+    StepArgs a{};
+    a.L = hp.n_layers;
+    a.H = hp.hidden;
+    a.F = hp.ffn;
+    a.nq = hp.n_heads;
+    a.nkv = hp.n_kv_heads;
+    a.V = hp.vocab;
+    a.qkv_n = qkv_rows(hp);
+    a.B = B;
+    a.slots = (int)h->slots;
+    a.splits = splits_for(h, B);
+    a.eps = hp.rms_eps;
+    a.scale = (float)(1.0 / std::sqrt((double)hp.head_dim));
+    a.layers = h->step_layers;
+    a.embed = static_cast<const __nv_bfloat16 *>(h->embed);
+    a.final_norm = h->final_norm;
+    a.rope = h->rope;
+    a.x = h->xd;
+    a.qkv = h->qkvd;
+    a.o = h->od;
+    a.gu = h->gud;
+    a.logits = h->logits;
+    a.attn_part = h->attn_part;
+    a.attn_counter = h->attn_counter;
+    a.am_val = h->am_val;
+    a.am_idx = h->am_idx;
+    a.am_counter = h->am_counter;
+    a.out_ids = h->out_ids;
+    a.out_ids_cap = hp.max_new;
+    a.st = h->st;
+    a.bar = h->step_bar;
+    return a;
+}
+
+static bool step_path(const dec_handle *h, int B) { return h->use_step && B <= kGroupB; }
+
 static void enqueue_step(dec_handle *h, int B) {
+    if (step_path(h, B)) {
+        launch_step(step_args(h, B), h->num_sms, h->stream);
+        h->enq++;
+        return;
+    }
     for (int l = 0; l < h->hp.n_layers; ++l) enqueue_decode_layer(h, l, B, true);
     enqueue_head(h, B);
 }
@@ -751,6 +801,25 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
         CKC(cudaMemcpyAsync(h->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice, s));
         CKC(cudaStreamSynchronize(s));
     }
+    {
+        std::vector<StepLayer> sl(hp->n_layers);
+        for (int l = 0; l < hp->n_layers; ++l) {
+            const DevLayer &D = h->L[l];
+            sl[l] = StepLayer{static_cast<const __nv_bfloat16 *>(D.wqkv), static_cast<const __nv_bfloat16 *>(D.wo),
+                              static_cast<const __nv_bfloat16 *>(D.wgu), static_cast<const __nv_bfloat16 *>(D.wd),
+                              D.attn_norm, D.ffn_norm, D.qn, D.kn, static_cast<__half *>(D.K),
+                              static_cast<__half *>(D.V)};
+        }
+        CKC(cudaMemcpyAsync(h->step_layers, sl.data(), sl.size() * sizeof(StepLayer), cudaMemcpyHostToDevice, s));
+        CKC(cudaStreamSynchronize(s));
+        // the per-op kernel sequence is the default; SPEECH_DECODER_STEP=persistent
+        // selects the single cooperative launch per step where it is supported
+        const char *env = std::getenv("SPEECH_DECODER_STEP");
+        h->use_step = h->w_bf16 && h->kv_f16 && env && !std::strcmp(env, "persistent") &&
+                      step_supported((int)d, (int)(nq / nkv), (int)H, (int)F, (int)(nq * d),
+                                     std::min(hp->max_batch, kGroupB));
+        cudaGetLastError();
+    }
     CKC(cudaMemsetAsync(h->attn_counter, 0, (size_t)hp->max_batch * nkv * sizeof(unsigned), s));
     CKC(cudaMemsetAsync(h->am_counter, 0, 64 * sizeof(unsigned), s));
     std::memset(&h->hst, 0, sizeof(SeqState));
@@ -996,7 +1065,7 @@ dec_status dec_launch_count(const dec_handle *h, int64_t *count) {
 }
 
 dec_status dec_profile_kernel(dec_handle *h, int32_t op, int32_t iters, float *avg_ms, double *bytes_per_launch) {
-    if (!h || !avg_ms || !bytes_per_launch || iters < 1 || op < 0 || op > 2)
+    if (!h || !avg_ms || !bytes_per_launch || iters < 1 || op < 0 || op > 3)
         return fail(h, DEC_ERR_INVALID_ARG, "bad profile arguments");
     if (!h->prefilled) return fail(h, DEC_ERR_STATE, "profile needs a prefill first");
     dec_status rc = sync_state(h);
@@ -1016,6 +1085,19 @@ dec_status dec_profile_kernel(dec_handle *h, int32_t op, int32_t iters, float *a
     double bytes = 0.0;
     CK(cudaEventRecord(h->ev[2], s));
     for (int it = 0; it < iters; ++it) {
+        if (op == 3) {
+            // the whole step as one persistent launch (or the kernel sequence when it is unavailable)
+            CK(cudaMemcpyAsync(h->st, &live, sizeof(SeqState), cudaMemcpyHostToDevice, s));
+            h->enq = 0;
+            enqueue_step(h, B);
+            launches += h->enq;
+            double kv = 0.0;
+            for (int b = 0; b < B; ++b) kv += 2.0 * nkv * (double)(saved.n_past[b] + 1) * d * kvs * hp.n_layers;
+            const double per_layer = ((double)qkv_rows(hp) * H + (double)H * hp.n_heads * d + 2.0 * F * H +
+                                      (double)H * F) * ws;
+            bytes += per_layer * hp.n_layers + (double)hp.vocab * H * ws + kv;
+            continue;
+        }
         if (op == 1) {
             // keep every row live so each launch does the full work
             CK(cudaMemcpyAsync(h->st, &live, sizeof(SeqState), cudaMemcpyHostToDevice, s));
