@@ -119,7 +119,7 @@ class Clocks:
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
-    for f in ("gemv.cu", "decode.cuh", "common.cuh"):
+    for f in ("gemv.cu", "gemv_stream.cu", "decode.cuh", "common.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "speech_decoder_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -240,7 +240,9 @@ def run_ours(args):
     utterance(ids_dev, audio_dev, True)
     if B == 1:
         dec.prefill_ids(ids_dev, audio_dev, int(pre_lens[0]))
-        kname = "k_gemv_ldg<bf16, IN_NORM, OUT_STORE> (q|k|v and gate|up GEMV, one launch per layer)"
+        impl = os.environ.get("SPEECH_DECODER_GEMV", "stream")
+        kname = ("k_gemv_stream<1, IN_NORM, OUT_STORE>" if impl == "stream" else
+                 "k_gemv_ldg<bf16, IN_NORM, OUT_STORE>") + " (q|k|v and gate|up GEMV, one launch per layer)"
     else:
         dec.prefill_ids_batch_ptr(ids_dev.data_ptr(), cu_ids, audio_dev.data_ptr(), cu_au, pre_lens, 1)
         kname = "k_gemm_tc + k_splitk_reduce (q|k|v and gate|up projections of %d rows, per projection)" % B

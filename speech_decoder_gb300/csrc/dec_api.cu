@@ -95,6 +95,7 @@ struct dec_handle {
     bool own_stream = false;
     int gemv_ctas = 1;              // GEMV CTAs per SM
     float *tc_scratch = nullptr;    // split-K partial tiles of the tensor-core GEMM
+    int pf_bytes = 0;               // L2 look-ahead of the decode GEMVs, bytes per CTA
     // persistent step kernel
     StepLayer *step_layers = nullptr;
     unsigned long long *step_bar = nullptr;
@@ -154,13 +155,18 @@ static int splits_for(const dec_handle *h, int B) { return attn_decode_splits(B,
 
 static int gemv_ctas_per_sm() {
     const char *c = std::getenv("SPEECH_DECODER_GEMV_CTAS_PER_SM");
-    return c ? std::max(1, std::min(4, std::atoi(c))) : 2;
+    return c ? std::max(1, std::min(4, std::atoi(c))) : gemv_default_ctas_per_sm();
 }
 
 // Assign every device buffer from the bump allocator (base == nullptr: size only).
 static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms) {
     Bump b{base};
+    gemv_reload_env();
     h->gemv_ctas = gemv_ctas_per_sm();
+    {
+        const char *c = std::getenv("SPEECH_DECODER_GEMV_PF_KB");
+        h->pf_bytes = (c ? std::max(0, std::min(4096, std::atoi(c))) : 128) * 1024;
+    }
     const size_t ws = wsize(hp), kvs = kvsize(hp), as = ws;   // activations use the weight format
     const size_t H = hp.hidden, d = hp.head_dim, nq = hp.n_heads, nkv = hp.n_kv_heads, F = hp.ffn;
     const size_t V = hp.vocab, Tm = hp.max_tokens, Bm = hp.max_batch;
@@ -290,6 +296,15 @@ static void enqueue_decode_layer_tc(dec_handle *h, int l, int B, bool from_embed
     gemm(h, h->hbuf, L.wd, h->xd, H, B, H, F, EPI_RESID_F32);
 }
 
+// The GEMV that runs next streams W [N, K]: let this one pull its first rows into L2.
+static void set_prefetch(const dec_handle *h, GemvArgs &g, const void *W, int N, int K) {
+    if (!h->w_bf16 || h->pf_bytes <= 0) return;
+    g.pf = W;
+    g.pf_N = N;
+    g.pf_K = K;
+    g.pf_bytes = h->pf_bytes;
+}
+
 // One decoder block for the step rows in xd (one row per sequence).
 static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
     if (batched_path(h, B)) {
@@ -313,6 +328,14 @@ static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
     g.embed = h->embed;
     g.x_resid = h->xd;
     g.out = h->qkvd;
+    set_prefetch(h, g, L.wo, H, nqd);
+    if (h->w_bf16 && h->pf_bytes > 0) {
+        g.kvp_K = L.K;
+        g.kvp_V = L.V;
+        g.kvp_slots = (int)h->slots;
+        g.kvp_nkv = hp.n_kv_heads;
+        g.kvp_row_bytes = (int)(hp.head_dim * kvsize(hp));
+    }
     const bool emb = from_embed && l == 0;
     launch_gemv(emb ? IN_EMBED_NORM : IN_NORM, OUT_STORE, h->w_bf16, g, gemv_grid(g.N, h->num_sms, h->gemv_ctas), s);
 
@@ -345,14 +368,22 @@ static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
     o.K = nqd;
     o.in = h->od;
     o.out = h->xd;
+    set_prefetch(h, o, L.wgu, 2 * F, H);
     launch_gemv(IN_PLAIN, OUT_RESID, h->w_bf16, o, gemv_grid(H, h->num_sms, h->gemv_ctas), s);
 
+    // gate|up: with the producer-warp GEMV each gate row meets its up row in one
+    // stage and the kernel writes silu(gate) * up; otherwise gate|up is stored
+    // and the down projection's prologue applies SwiGLU
+    const int grid_f = gemv_grid(2 * F, h->num_sms, h->gemv_ctas);
+    const bool fused = h->w_bf16 && gemv_impl() == 4 && gemv_stream_swiglu_ok(H, std::min(B, kGroupB), F, grid_f);
     GemvArgs f1 = g;
+    f1.kvp_K = f1.kvp_V = nullptr;
     f1.W = L.wgu;
-    f1.N = 2 * F;
+    f1.N = fused ? F : 2 * F;
     f1.norm_w = L.ffn_norm;
     f1.out = h->gud;
-    launch_gemv(IN_NORM, OUT_STORE, h->w_bf16, f1, gemv_grid(2 * F, h->num_sms, h->gemv_ctas), s);
+    set_prefetch(h, f1, L.wd, H, F);
+    launch_gemv(IN_NORM, fused ? OUT_SWIGLU : OUT_STORE, h->w_bf16, f1, grid_f, s);
 
     GemvArgs f2{};
     f2.st = h->st;
@@ -363,7 +394,9 @@ static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
     f2.in = h->gud;
     f2.ffn = F;
     f2.out = h->xd;
-    launch_gemv(IN_SWIGLU, OUT_RESID, h->w_bf16, f2, gemv_grid(H, h->num_sms, h->gemv_ctas), s);
+    if (l + 1 < hp.n_layers) set_prefetch(h, f2, h->L[l + 1].wqkv, qkv_rows(hp), H);
+    else set_prefetch(h, f2, h->embed, hp.vocab, H);
+    launch_gemv(fused ? IN_PLAIN : IN_SWIGLU, OUT_RESID, h->w_bf16, f2, gemv_grid(H, h->num_sms, h->gemv_ctas), s);
     h->enq += 5;
 }
 
@@ -391,6 +424,7 @@ static void enqueue_head(dec_handle *h, int B) {
     g.counter = h->am_counter;
     g.out_ids = h->out_ids;
     g.out_ids_cap = h->hp.max_new;
+    set_prefetch(h, g, h->L[0].wqkv, qkv_rows(h->hp), h->hp.hidden);
     launch_gemv(IN_NORM, OUT_ARGMAX, h->w_bf16, g, h->lm_grid, h->stream);
     h->enq++;
 }
@@ -746,9 +780,6 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
         if ((call) != cudaSuccess) return fail_create(DEC_ERR_CUDA); \
     } while (0)
 
-    if (const char *v = std::getenv("SPEECH_DECODER_GEMV"))
-        gemv_set_impl(!std::strcmp(v, "ldg") ? 1 : !std::strcmp(v, "cpasync") ? 2 : 3);
-    if (const char *v = std::getenv("SPEECH_DECODER_GEMV_SLOTS")) gemv_set_ring(std::atoi(v));
     init_gemv_kernels();
     init_gemm_tc();
     cudaStream_t s = h->stream;

@@ -5,7 +5,9 @@
 namespace dec {
 
 enum GemvIn { IN_NORM = 0, IN_EMBED_NORM = 1, IN_PLAIN = 2, IN_SWIGLU = 3 };
-enum GemvOut { OUT_STORE = 0, OUT_RESID = 1, OUT_ARGMAX = 2 };
+// OUT_SWIGLU (producer-warp GEMV only): W is the packed gate|up matrix, N the
+// ffn features, out[b][f] = silu(gate_f) * up_f
+enum GemvOut { OUT_STORE = 0, OUT_RESID = 1, OUT_ARGMAX = 2, OUT_SWIGLU = 3 };
 
 struct GemvArgs {
     const void *W;          // [N, K] weights (bf16 or f32)
@@ -25,6 +27,14 @@ struct GemvArgs {
     unsigned *counter;
     int32_t *out_ids;       // [B, out_ids_cap]
     int out_ids_cap;
+    // the weights of the kernel that runs next ([pf_N, pf_K] bf16, may be null):
+    // each CTA pulls up to pf_bytes of its share of the rows into L2 once its
+    // own rows are in flight, so HBM keeps streaming across the launch boundary
+    const void *pf;
+    int pf_N, pf_K, pf_bytes;
+    // KV of this layer pulled into L2 for the attention that follows (may be null)
+    const void *kvp_K, *kvp_V;
+    int kvp_slots, kvp_nkv, kvp_row_bytes;
     // filled in by launch_gemv: shared-memory slots per warp, units per CTA
     int n_ring;
     int max_units;
@@ -36,8 +46,13 @@ struct GemvPlan {
     bool ok;
 };
 GemvPlan gemv_plan(int K, bool w_bf16, int nb, int N, int grid_x);
-// tuning knobs (process-wide): pipeline implementation and bulk ring sizes
+// tuning knobs (process-wide): pipeline implementation (1 registers, 2 cp.async
+// ring, 3 per-warp bulk ring, 4 producer-warp stream for bf16 weights; the
+// SPEECH_DECODER_GEMV variable ldg|cpasync|tma|stream picks the first default)
+// and bulk ring sizes
 void gemv_set_impl(int impl);
+// re-read SPEECH_DECODER_GEMV and SPEECH_DECODER_GEMV_SLOTS (each decoder creation)
+void gemv_reload_env();
 int gemv_impl();
 void gemv_set_ring(int slots);
 
@@ -60,6 +75,7 @@ struct AttnDecArgs {
     const int32_t *kv_off;  // [B] first slot of each sequence
     const int32_t *kv_len;  // [B] visible keys (rows with len <= 0 or out of range are skipped)
     __nv_bfloat16 *o_bf16;  // optional bf16 copy of o (input of the tensor-core O projection)
+
 };
 
 // Batched-step helpers (rows of several sequences through the tensor-core GEMM):
@@ -88,12 +104,32 @@ cudaError_t attn_op_launch(const float *q, const void *K, const void *V, bool kv
                            float *out, void *scratch, int num_sms, cudaStream_t s);
 int gemv_grid(int N, int num_sms, int ctas_per_sm);
 void init_gemv_kernels();
+// shared-memory opt-in of the step attention (called once per process, with init_gemv_kernels)
+void init_attn_kernels();
+// producer-warp GEMV (bf16 weights, one CTA per SM): plan, launch (false: shape
+// not supported), ring size override (0 = automatic)
+GemvPlan gemv_stream_plan(int in_mode, int K, int nb, int N, int grid_x);
+bool launch_gemv_stream(int in_mode, int out_mode, const GemvArgs &a, int grid_x, cudaStream_t s);
+void gemv_stream_set_slots(int slots);
+// the fused gate|up + SwiGLU GEMV fits (hidden K, ffn features)
+bool gemv_stream_swiglu_ok(int K, int nb, int ffn, int grid_x);
+void init_gemv_stream_kernels();
+// GEMV CTAs per SM that suit the selected implementation
+int gemv_default_ctas_per_sm();
 
 // activation rows x K floats of one GEMV CTA must fit: kGroupB * K * 4 <= kGemvMaxSmem
 constexpr int kGemvMaxSmem = 200 * 1024;
 // split-KV partitions per (sequence, kv head)
 constexpr int kAttnMaxSplits = 32;
 // keys per split at least (short sequences run few splits)
-constexpr int kAttnMinChunk = 32;
+constexpr int kAttnMinChunk = 256;
+
+// Keys [0, len) of one (sequence, kv head) are cut into splits of `chunk` keys;
+// splits [0, n_used) hold keys.
+__host__ __device__ __forceinline__ void attn_split(int len, int S, int &chunk, int &n_used) {
+    chunk = (len + S - 1) / S;
+    chunk = chunk < kAttnMinChunk ? kAttnMinChunk : chunk;
+    n_used = (len + chunk - 1) / chunk;
+}
 
 }  // namespace dec

@@ -20,6 +20,9 @@
 // or logits + argmax with the lowest index winning ties and a last-CTA
 // reduction that advances the greedy state (qwen3_asr/decoder.cpp,
 // build_step_graph: final RMSNorm, tied lm_head, argmax).
+#include <cstdlib>
+#include <cstring>
+
 #include "decode.cuh"
 #include "ptx.cuh"
 
@@ -470,12 +473,25 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_ldg(GemvArgs a) {
 }
 
 // ------------------------------------------------------------------ host side
-static int g_impl = 1;      // 1: registers, 2: ring fed by cp.async, 3: ring fed by 1-D TMA
+// 1: registers, 2: ring fed by cp.async, 3: per-warp ring fed by 1-D TMA,
+// 4: producer-warp stream (bf16 weights; f32 weights use 1)
+static int g_impl = 0;
 static int g_ring_slots = 3;
 void gemv_set_impl(int impl) {
-    if (impl >= 1 && impl <= 3) g_impl = impl;
+    if (impl >= 1 && impl <= 4) g_impl = impl;
 }
-int gemv_impl() { return g_impl; }
+void gemv_reload_env() {
+    const char *v = std::getenv("SPEECH_DECODER_GEMV");
+    g_impl = !v ? 4 : !std::strcmp(v, "ldg") ? 1 : !std::strcmp(v, "cpasync") ? 2 : !std::strcmp(v, "tma") ? 3 : 4;
+    const char *n = std::getenv("SPEECH_DECODER_GEMV_SLOTS");
+    if (n) gemv_set_ring(std::atoi(n));
+    gemv_stream_set_slots(n ? std::atoi(n) : 0);
+}
+int gemv_impl() {
+    if (g_impl == 0) gemv_reload_env();
+    return g_impl;
+}
+int gemv_default_ctas_per_sm() { return gemv_impl() == 4 ? 1 : 2; }
 void gemv_set_ring(int slots) {
     if (slots >= 2 && slots <= 7) g_ring_slots = slots;
 }
@@ -494,7 +510,7 @@ GemvPlan gemv_plan(int K, bool w_bf16, int nb, int N, int grid_x) {
     const size_t xs = ((size_t)nb * K + 3) / 4 * 16;
     const size_t part = (size_t)p.max_units * kGroupB * 4;
     const size_t ring = (size_t)kWarps * p.n_ring * kUnitBytes + (size_t)kWarps * p.n_ring * 8;
-    p.smem = (g_impl == 1 ? 0 : ring) + xs + part;
+    p.smem = (gemv_impl() == 1 || gemv_impl() == 4 ? 0 : ring) + xs + part;
     p.ok = (row_bytes % 16 == 0) && p.smem <= (size_t)kGemvMaxSmem;
     return p;
 }
@@ -511,13 +527,14 @@ static void launch_one(const GemvArgs &a, dim3 grid, size_t smem, cudaStream_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (g_impl == 1) cudaLaunchKernelEx(&cfg, k_gemv_ldg<TW, IN, OUT>, a);
+    if (g_impl == 1 || g_impl == 4) cudaLaunchKernelEx(&cfg, k_gemv_ldg<TW, IN, OUT>, a);
     else if (g_impl == 2) cudaLaunchKernelEx(&cfg, k_gemv_ring<TW, IN, OUT, false>, a);
     else cudaLaunchKernelEx(&cfg, k_gemv_ring<TW, IN, OUT, true>, a);
 }
 
 template <typename TW>
 static void launch_gemv_t(int in_mode, int out_mode, GemvArgs a, int grid_x, cudaStream_t s) {
+    if (sizeof(TW) == 2 && gemv_impl() == 4 && launch_gemv_stream(in_mode, out_mode, a, grid_x, s)) return;
     const int nb = a.B < kGroupB ? a.B : kGroupB;
     const GemvPlan p = gemv_plan(a.K, sizeof(TW) == 2, nb, a.N, grid_x);
     a.n_ring = p.n_ring;
@@ -567,6 +584,8 @@ static void init_t() {
 void init_gemv_kernels() {
     init_t<__nv_bfloat16>();
     init_t<float>();
+    init_gemv_stream_kernels();
+    init_attn_kernels();
 }
 
 }  // namespace dec

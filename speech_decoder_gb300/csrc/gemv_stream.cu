@@ -1,0 +1,660 @@
+// Weight-streaming GEMV of the decode step, fed by a producer warp (bf16
+// weights; one activation row per sequence, up to four sequences per CTA).
+//
+// One CTA per SM owns a contiguous block of weight rows.  Its producer warp
+// copies whole rows, as many as fit a 16 KB stage, into a ring of shared-memory
+// stages with 1-D bulk copies (TMA) completing on mbarriers; eight consumer
+// warps take the stages round-robin (chunk j goes to warp j % 8), each
+// finishing its rows itself: dot products against the activation rows held in
+// shared memory, a warp reduction, and the epilogue.  Weights never depend on
+// earlier kernels, so the ring is filled before the kernel waits for its
+// predecessor (programmatic dependent launch), and once the producer has issued
+// its last own row it pulls the CTA's share of the NEXT kernel's weights into
+// L2: HBM keeps streaming while the launch boundary drains.
+//
+// Block math (qwen3_asr/decoder.cpp, build_step_graph; the decoder block of the
+// page's file header): the prologue builds RMSNorm(x)*w (pre-LN norms, final
+// norm), the embedding row of the step's token (layer 0), the plain attention
+// output, or silu(gate)*up from the packed gate|up rows; the epilogue stores,
+// adds into the residual, or writes logits and takes the argmax with the lowest
+// index winning ties, the last CTA advancing the greedy state.
+#include <climits>
+
+#include "decode.cuh"
+#include "ptx.cuh"
+
+namespace dec {
+namespace {
+
+constexpr int kCW = 8;                        // consumer warps
+constexpr int kCT = kCW * 32;                 // consumer threads
+constexpr int kTT = kCT + 32;                 // + the producer warp
+constexpr int kStage = 16 * 1024;             // bytes per ring stage (whole rows)
+constexpr int kMaxStages = 12;
+constexpr int kAutoStages = 10;               // 160 KB in flight per SM covers the loaded HBM latency
+constexpr uint64_t kWaitNs = 200000000ull;    // every wait gives up after 0.2 s
+constexpr int kBarCons = 1;                   // named barrier of the consumer warps
+
+__device__ __forceinline__ void cons_sync() { ptx::named_bar_sync(kBarCons, kCT); }
+
+__device__ __forceinline__ void report(SeqState *st, int code) {
+    if (st) atomicCAS(&st->error, 0, code);
+}
+
+// activation element k of a bf16 weight row lives at xs_off(k): the 8 values of
+// a 16-byte chunk are split into low/high float4 halves (conflict-free reads)
+__device__ __forceinline__ int xs_off(int k, int CPR) {
+    const int c = k >> 3, half = (k >> 2) & 1;
+    return ((half * CPR + c) << 2) + (k & 3);
+}
+
+__host__ __device__ __forceinline__ int rows_per_stage(int K) {
+    const int rb = K * 2;
+    return rb >= kStage ? 1 : kStage / rb;
+}
+
+// OUT_SWIGLU: (gate, up) row pairs per stage, a power of two so that a chunk
+// that starts at a multiple of it never crosses a 128-feature block of the
+// packed gate|up layout; 0 = a pair does not fit one stage
+__host__ __device__ __forceinline__ int pairs_per_stage(int K) {
+    const int r = rows_per_stage(K) / 2;
+    int p = 0;
+    if (r >= 1) {
+        p = 1;
+        while (p * 2 <= r && p * 2 <= 128) p *= 2;
+    }
+    return K * 2 > kStage ? 0 : p;
+}
+
+// sum over the consumer threads
+__device__ __forceinline__ float cons_sum(float v, float *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_sum(v);
+    cons_sync();
+    if (lane == 0) red[warp] = v;
+    cons_sync();
+    float t = lane < kCW ? red[lane] : 0.f;
+    return warp_sum(t);
+}
+
+// Activation rows of this CTA's sequences into shared memory (consumer
+// threads).  The rows' loads are issued together with the liveness reads (rows
+// that turn out finished are computed and not stored); the RMSNorm weights were
+// staged in nw before the kernel waited on its predecessor.
+template <int NB, int IN>
+__device__ void prologue(const GemvArgs &a, float *xs, const float *nw, int b0, int *live, int CPR, float *sred) {
+    const int K = a.K, tid = threadIdx.x;
+    if (tid < kGroupB) live[tid] = tid < NB && b0 + tid < a.B && row_live(a.st, b0 + tid);
+    if (IN == IN_EMBED_NORM) cons_sync();                 // the token ids come from the state
+    // loads in flight per thread and row: one pass over K = 2048, and over
+    // K = 6144 (down projection inputs) for a single row
+    constexpr int P = (IN == IN_SWIGLU || IN == IN_PLAIN) && NB == 1 ? 24 : 8;
+    float ss[NB];
+#pragma unroll
+    for (int bi = 0; bi < NB; ++bi) ss[bi] = 0.f;
+    for (int k0 = tid; k0 < K; k0 += P * kCT) {
+        float v[NB][P];
+#pragma unroll
+        for (int bi = 0; bi < NB; ++bi) {
+            const int b = b0 + bi;
+            const bool ex = b < a.B && (IN != IN_EMBED_NORM || live[bi]);
+            if (IN == IN_SWIGLU) {
+                // packed gate|up: block j of 256 outputs = 128 gate rows, then the 128 up rows
+                const float *gu = a.in + (size_t)b * 2 * a.ffn;
+                float g[P], u[P];
+#pragma unroll
+                for (int i = 0; i < P; ++i) {
+                    const int f = k0 + i * kCT, blk = f >> 7, j = f & 127;
+                    g[i] = ex && f < K ? gu[blk * 256 + j] : 0.f;
+                    u[i] = ex && f < K ? gu[blk * 256 + 128 + j] : 0.f;
+                }
+#pragma unroll
+                for (int i = 0; i < P; ++i) v[bi][i] = g[i] / (1.f + expf(-g[i])) * u[i];
+            } else if (IN == IN_EMBED_NORM) {
+                const __nv_bfloat16 *er =
+                    reinterpret_cast<const __nv_bfloat16 *>(a.embed) + (size_t)(ex ? a.st->cur_tok[b] : 0) * K;
+#pragma unroll
+                for (int i = 0; i < P; ++i) {
+                    const int k = k0 + i * kCT;
+                    v[bi][i] = ex && k < K ? __bfloat162float(er[k]) : 0.f;
+                }
+            } else {
+                const float *src = a.in + (size_t)b * K;
+#pragma unroll
+                for (int i = 0; i < P; ++i) {
+                    const int k = k0 + i * kCT;
+                    v[bi][i] = ex && k < K ? src[k] : 0.f;
+                }
+            }
+        }
+#pragma unroll
+        for (int bi = 0; bi < NB; ++bi) {
+            float *xr = xs + (size_t)bi * K;
+#pragma unroll
+            for (int i = 0; i < P; ++i) {
+                const int k = k0 + i * kCT;
+                if (k < K) {
+                    xr[xs_off(k, CPR)] = v[bi][i];
+                    ss[bi] += v[bi][i] * v[bi][i];
+                    if (IN == IN_EMBED_NORM && blockIdx.x == 0 && b0 + bi < a.B && live[bi])
+                        a.x_resid[(size_t)(b0 + bi) * K + k] = v[bi][i];
+                }
+            }
+        }
+    }
+    cons_sync();                                          // live[] and the rows are visible
+    if (IN == IN_PLAIN || IN == IN_SWIGLU) return;
+#pragma unroll
+    for (int bi = 0; bi < NB; ++bi) {
+        if (!live[bi]) continue;                          // uniform
+        const float r = rsqrtf(cons_sum(ss[bi], sred) / (float)K + a.eps);
+        float *xr = xs + (size_t)bi * K;
+        for (int k = tid; k < K; k += kCT) {
+            const int o = xs_off(k, CPR);
+            xr[o] = xr[o] * r * nw[k];
+        }
+    }
+}
+
+__device__ __forceinline__ void fma8(const float (&f)[8], const float4 &lo, const float4 &hi, float &acc) {
+    acc = fmaf(f[0], lo.x, acc);
+    acc = fmaf(f[1], lo.y, acc);
+    acc = fmaf(f[2], lo.z, acc);
+    acc = fmaf(f[3], lo.w, acc);
+    acc = fmaf(f[4], hi.x, acc);
+    acc = fmaf(f[5], hi.y, acc);
+    acc = fmaf(f[6], hi.z, acc);
+    acc = fmaf(f[7], hi.w, acc);
+}
+
+// Epilogue of one finished row (lane 0 of the warp that computed it).
+template <int NB, int OUT>
+__device__ __forceinline__ void row_out(const GemvArgs &a, int row, int b0, const int *live, const float (&acc)[NB],
+                                        float (&best_v)[NB], int (&best_i)[NB]) {
+#pragma unroll
+    for (int bi = 0; bi < NB; ++bi) {
+        if (!live[bi]) continue;
+        const size_t o = (size_t)(b0 + bi) * a.N + row;
+        if (OUT == OUT_STORE) a.out[o] = acc[bi];
+        if (OUT == OUT_RESID) a.out[o] += acc[bi];
+        if (OUT == OUT_ARGMAX) {
+            if (a.out) a.out[o] = acc[bi];
+            if (acc[bi] > best_v[bi]) {                    // rows ascend per warp: lowest index on ties
+                best_v[bi] = acc[bi];
+                best_i[bi] = row;
+            }
+        }
+    }
+}
+
+// Rows [row0, row0 + nr) of one stage; two rows share each activation read.
+template <int NB, int OUT>
+__device__ __forceinline__ void stage_rows(const GemvArgs &a, const uint4 *stage, int row0, int nr, int CPR, int b0,
+                                           const float *xs, const int *live, float (&best_v)[NB],
+                                           int (&best_i)[NB]) {
+    const int lane = threadIdx.x & 31, K = a.K;
+    int rr = 0;
+    for (; rr + 1 < nr; rr += 2) {
+        const uint4 *w0 = stage + (size_t)rr * CPR, *w1 = w0 + CPR;
+        float a0[NB], a1[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) a0[b] = a1[b] = 0.f;
+#pragma unroll 2
+        for (int c = lane; c < CPR; c += 32) {
+            float f0[8], f1[8];
+            unpack16(w0[c], f0, (const __nv_bfloat16 *)nullptr);
+            unpack16(w1[c], f1, (const __nv_bfloat16 *)nullptr);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const float4 *x4 = reinterpret_cast<const float4 *>(xs + (size_t)b * K);
+                const float4 lo = x4[c], hi = x4[CPR + c];
+                fma8(f0, lo, hi, a0[b]);
+                fma8(f1, lo, hi, a1[b]);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            a0[b] = warp_sum(a0[b]);
+            a1[b] = warp_sum(a1[b]);
+        }
+        if (lane == 0) {
+            row_out<NB, OUT>(a, row0 + rr, b0, live, a0, best_v, best_i);
+            row_out<NB, OUT>(a, row0 + rr + 1, b0, live, a1, best_v, best_i);
+        }
+    }
+    if (rr < nr) {
+        const uint4 *w0 = stage + (size_t)rr * CPR;
+        float a0[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) a0[b] = 0.f;
+#pragma unroll 4
+        for (int c = lane; c < CPR; c += 32) {
+            float f0[8];
+            unpack16(w0[c], f0, (const __nv_bfloat16 *)nullptr);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const float4 *x4 = reinterpret_cast<const float4 *>(xs + (size_t)b * K);
+                fma8(f0, x4[c], x4[CPR + c], a0[b]);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) a0[b] = warp_sum(a0[b]);
+        if (lane == 0) row_out<NB, OUT>(a, row0 + rr, b0, live, a0, best_v, best_i);
+    }
+}
+
+// OUT_SWIGLU: pairs [j0, j0 + n): gate rows first, then the n up rows; each
+// warp writes silu(gate) * up per feature.
+template <int NB>
+__device__ __forceinline__ void stage_pairs(const GemvArgs &a, const uint4 *stage, int j0, int n, int CPR, int b0,
+                                            const float *xs, const int *live) {
+    const int lane = threadIdx.x & 31, K = a.K;
+    for (int i = 0; i < n; ++i) {
+        const uint4 *wg = stage + (size_t)i * CPR, *wu = stage + (size_t)(n + i) * CPR;
+        float ag[NB], au[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) ag[b] = au[b] = 0.f;
+#pragma unroll 2
+        for (int c = lane; c < CPR; c += 32) {
+            float f0[8], f1[8];
+            unpack16(wg[c], f0, (const __nv_bfloat16 *)nullptr);
+            unpack16(wu[c], f1, (const __nv_bfloat16 *)nullptr);
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const float4 *x4 = reinterpret_cast<const float4 *>(xs + (size_t)b * K);
+                const float4 lo = x4[c], hi = x4[CPR + c];
+                fma8(f0, lo, hi, ag[b]);
+                fma8(f1, lo, hi, au[b]);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            ag[b] = warp_sum(ag[b]);
+            au[b] = warp_sum(au[b]);
+        }
+        if (lane == 0) {
+#pragma unroll
+            for (int b = 0; b < NB; ++b)
+                if (live[b]) a.out[(size_t)(b0 + b) * a.N + j0 + i] = ag[b] / (1.f + expf(-ag[b])) * au[b];
+        }
+    }
+}
+
+}  // namespace
+
+template <int NB, int IN, int OUT>
+__global__ void __launch_bounds__(kTT, 2) k_gemv_stream(GemvArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ __align__(8) uint64_t full[kMaxStages];
+    __shared__ __align__(8) uint64_t empty[kMaxStages];
+    __shared__ volatile int issued_s, abort_s;
+    __shared__ int first_fail_s, any_s;
+    __shared__ int live_s[kGroupB];
+    __shared__ float sred[32];
+    __shared__ float wv[kCW * kGroupB];
+    __shared__ int wi[kCW * kGroupB];
+    __shared__ float rv[kTT / 32];
+    __shared__ int ri[kTT / 32];
+    __shared__ unsigned ticket_s;
+
+    const int NS = a.n_ring;
+    const int K = a.K, CPR = K / 8;
+    const size_t rb = (size_t)K * 2;
+    // units: weight rows, or (gate, up) pairs for OUT_SWIGLU (a.N = ffn
+    // features; each CTA's range starts at a multiple of R)
+    constexpr bool kPair = OUT == OUT_SWIGLU;
+    const int R = kPair ? pairs_per_stage(K) : rows_per_stage(K);
+    int r0, r1;
+    if (kPair) {
+        const long long U = (a.N + R - 1) / R;
+        r0 = (int)min((long long)a.N, R * (U * blockIdx.x / gridDim.x));
+        r1 = (int)min((long long)a.N, R * (U * (blockIdx.x + 1) / gridDim.x));
+    } else {
+        r0 = (int)((long long)a.N * blockIdx.x / gridDim.x);
+        r1 = (int)((long long)a.N * (blockIdx.x + 1) / gridDim.x);
+    }
+    const int n_chunks = (r1 - r0 + R - 1) / R;
+    const int b0 = blockIdx.y * kGroupB;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float *xs = reinterpret_cast<float *>(smem + (size_t)NS * kStage);
+    float *nw = xs + (size_t)NB * K;                      // RMSNorm weight (norm prologues)
+    const unsigned char *W = reinterpret_cast<const unsigned char *>(a.W);
+    constexpr bool kNorm = IN == IN_NORM || IN == IN_EMBED_NORM;
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        issued_s = 0;
+        abort_s = 0;
+        first_fail_s = INT_MAX;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    ptx::pdl_launch();
+
+    // chunk g (units r0 + g R ...) into stage g % NS; producer lane 0 only
+    auto issue = [&](int g) {
+        const int slot = g % NS, u = r0 + g * R, n = min(R, r1 - u);
+        unsigned char *dst = smem + (size_t)slot * kStage;
+        if (kPair) {
+            // gate rows of features [u, u + n), then their up rows
+            const size_t grow = (size_t)(u >> 7) * 256 + (u & 127);
+            const uint32_t half = (uint32_t)(n * rb);
+            ptx::mbar_expect_tx(&full[slot], 2 * half);
+            ptx::bulk_g2s(dst, W + grow * rb, half, &full[slot]);
+            ptx::bulk_g2s(dst + half, W + (grow + 128) * rb, half, &full[slot]);
+        } else {
+            const uint32_t bytes = (uint32_t)(n * rb);
+            ptx::mbar_expect_tx(&full[slot], bytes);
+            ptx::bulk_g2s(dst, W + (size_t)u * rb, bytes, &full[slot]);
+        }
+        __threadfence_block();
+        issued_s = g + 1;
+    };
+    const int pre = min(NS, n_chunks);
+    if (warp == kCW && lane == 0) {
+        for (int g = 0; g < pre; ++g) issue(g);          // weights: no dependency on earlier kernels
+        // this layer's cached keys and values, for the attention that follows:
+        // one (sequence, kv head, K or V) range per CTA, pulled into L2.  The
+        // state may still be changing (a hint only); ranges are clamped to the pool.
+        if (a.kvp_K) {
+            const int n_reg = a.B * a.kvp_nkv * 2;
+            for (int ri = blockIdx.x; ri < n_reg; ri += gridDim.x) {
+                const int b = ri / (2 * a.kvp_nkv), g = (ri >> 1) % a.kvp_nkv;
+                const volatile SeqState *st = a.st;
+                if (!st->active[b] || st->done[b]) continue;
+                const int off = st->kv_off[b];
+                int len = st->n_past[b];
+                if (off < 0 || off >= a.kvp_slots || len <= 0) continue;
+                len = min(len, a.kvp_slots - off);
+                const size_t rbk = (size_t)a.kvp_row_bytes;
+                const unsigned char *base = reinterpret_cast<const unsigned char *>((ri & 1) ? a.kvp_V : a.kvp_K) +
+                                            ((size_t)g * a.kvp_slots + off) * rbk;
+                const size_t bytes = (size_t)len * rbk;
+                for (size_t o = 0; o < bytes; o += 32768)
+                    ptx::bulk_prefetch_l2(base + o, (uint32_t)(bytes - o < 32768 ? bytes - o : 32768));
+            }
+        }
+    }
+
+    if (warp < kCW) {
+        if (kNorm)                                        // weights: no dependency either
+            for (int k = tid; k < K; k += kCT) nw[k] = a.norm_w[k];
+        ptx::pdl_wait();
+        prologue<NB, IN>(a, xs, nw, b0, live_s, CPR, sred);
+        if (tid == 0) {
+            int any = 0;
+            for (int b = 0; b < NB; ++b) any |= live_s[b];
+            any_s = any;
+        }
+    }
+    __syncthreads();
+    const bool any = any_s != 0;
+
+    float best_v[NB];
+    int best_i[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+        best_v[b] = -INFINITY;
+        best_i[b] = INT_MAX;
+    }
+    if (warp == kCW) {
+        if (lane == 0 && any) {
+            for (int g = pre; g < n_chunks; ++g) {
+                // chunk g - NS was issued only after chunk g - 2NS had been
+                // consumed, so this parity names exactly one phase of the slot
+                const int slot = g % NS;
+                const uint32_t par = ((g / NS) - 1) & 1;
+                bool ok = ptx::mbar_try_wait(&empty[slot], par);
+                if (!ok) {
+                    const uint64_t t0 = ptx::now_ns();
+                    while (!ok && !abort_s && ptx::now_ns() - t0 <= kWaitNs) ok = ptx::mbar_try_wait(&empty[slot], par);
+                }
+                if (!ok) {
+                    if (!abort_s) {
+                        report(a.st, 8);
+                        abort_s = 1;
+                    }
+                    break;
+                }
+                issue(g);
+            }
+        }
+        // own rows all issued: pull this CTA's share of the next kernel's weights into L2
+        if (lane == 0 && a.pf) {
+            const size_t prb = (size_t)a.pf_K * 2;
+            const long long p0 = (long long)a.pf_N * blockIdx.x / gridDim.x;
+            const long long p1 = (long long)a.pf_N * (blockIdx.x + 1) / gridDim.x;
+            size_t bytes = (size_t)(p1 - p0) * prb;
+            if (bytes > (size_t)a.pf_bytes) bytes = (size_t)a.pf_bytes & ~size_t(15);
+            const unsigned char *src = reinterpret_cast<const unsigned char *>(a.pf) + (size_t)p0 * prb;
+            for (size_t o = 0; o < bytes; o += 32768)
+                ptx::bulk_prefetch_l2(src + o, (uint32_t)(bytes - o < 32768 ? bytes - o : 32768));
+        }
+    } else if (any) {
+        // Chunk j goes to warp j % 8.  A warp may run more than one ring lap
+        // ahead of the slowest one, so before the parity wait it waits until
+        // the producer has ISSUED chunk j: that happens only after chunk j - NS
+        // was consumed, hence landed, so the slot is then in chunk j's phase.
+        for (int j = warp; j < n_chunks; j += kCW) {
+            const int slot = j % NS;
+            bool ok = !abort_s;
+            if (ok && issued_s <= j) {
+                const uint64_t t0 = ptx::now_ns();
+                while (issued_s <= j && !abort_s && ptx::now_ns() - t0 <= kWaitNs) {
+                }
+                ok = issued_s > j;
+            }
+            ok = ok && ptx::mbar_wait_ns(&full[slot], (j / NS) & 1, kWaitNs);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) {
+                if (lane == 0) {
+                    if (!abort_s) {
+                        report(a.st, 9);
+                        abort_s = 1;
+                    }
+                    atomicMin(&first_fail_s, j);
+                }
+                break;
+            }
+            const int row0 = r0 + j * R;
+            const uint4 *stage = reinterpret_cast<const uint4 *>(smem + (size_t)slot * kStage);
+            if (kPair)
+                stage_pairs<NB>(a, stage, row0, min(R, r1 - row0), CPR, b0, xs, live_s);
+            else
+                stage_rows<NB, OUT>(a, stage, row0, min(R, r1 - row0), CPR, b0, xs, live_s, best_v, best_i);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&empty[slot]);
+        }
+    }
+    __syncthreads();
+    // copies that were issued but not consumed (no live row, or a wait that
+    // gave up) must land before the CTA exits
+    if (tid == 0 && (!any || abort_s)) {
+        const int first = any ? first_fail_s : 0;
+        for (int g = first; g < issued_s; ++g) ptx::mbar_wait_ns(&full[g % NS], (g / NS) & 1, kWaitNs);
+    }
+    if (OUT != OUT_ARGMAX) return;
+
+    // ---- argmax across warps and CTAs; the last CTA advances the greedy state
+    if (warp < kCW && lane == 0) {
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+            wv[warp * kGroupB + b] = best_v[b];
+            wi[warp * kGroupB + b] = best_i[b];
+        }
+    }
+    __syncthreads();
+    const int G = gridDim.x;
+    if (tid < NB && live_s[tid]) {
+        float bv = -INFINITY;
+        int bix = INT_MAX;
+        for (int w = 0; w < kCW; ++w) {
+            const float v = wv[w * kGroupB + tid];
+            const int ix = wi[w * kGroupB + tid];
+            if (v > bv || (v == bv && ix < bix)) {
+                bv = v;
+                bix = ix;
+            }
+        }
+        a.part_val[(size_t)(b0 + tid) * G + blockIdx.x] = bv;
+        a.part_idx[(size_t)(b0 + tid) * G + blockIdx.x] = bix;
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) ticket_s = atomicAdd(a.counter, 1u);
+    __syncthreads();
+    if (ticket_s != gridDim.x * gridDim.y - 1) return;
+    __threadfence();
+    for (int b = 0; b < a.B; ++b) {
+        if (!row_live(a.st, b)) continue;
+        float bv = -INFINITY;
+        int bix = INT_MAX;
+        for (int i = tid; i < G; i += kTT) {
+            const float v = __ldcg(a.part_val + (size_t)b * G + i);
+            const int ix = __ldcg(a.part_idx + (size_t)b * G + i);
+            if (v > bv || (v == bv && ix < bix)) {
+                bv = v;
+                bix = ix;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float v = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int ix = __shfl_xor_sync(0xffffffffu, bix, o);
+            if (v > bv || (v == bv && ix < bix)) {
+                bv = v;
+                bix = ix;
+            }
+        }
+        if (lane == 0) {
+            rv[warp] = bv;
+            ri[warp] = bix;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            for (int w = 1; w < kTT / 32; ++w)
+                if (rv[w] > bv || (rv[w] == bv && ri[w] < bix)) {
+                    bv = rv[w];
+                    bix = ri[w];
+                }
+            SeqState *st = a.st;
+            if (bix < 0 || bix >= a.N) {                        // every logit NaN
+                report(st, 2);
+                bix = 0;
+            }
+            st->cur_tok[b] = bix;
+            const int gcount = st->gen[b];
+            if (gcount < a.out_ids_cap) a.out_ids[(size_t)b * a.out_ids_cap + gcount] = bix;
+            st->gen[b] = gcount + 1;
+            const int np = st->n_past[b] + 1;
+            st->n_past[b] = np;
+            if (bix == st->eos_id || gcount + 1 >= st->max_new || np + 1 > st->kv_cap[b]) st->done[b] = 1;
+        }
+        __syncthreads();
+    }
+    if (tid == 0) *a.counter = 0u;
+}
+
+// ------------------------------------------------------------------ host side
+static int g_stream_slots = 0;          // 0: as many as keep two CTAs per SM
+
+void gemv_stream_set_slots(int slots) {
+    if (slots == 0 || (slots >= 2 && slots <= kMaxStages)) g_stream_slots = slots;
+}
+
+GemvPlan gemv_stream_plan(int in_mode, int K, int nb, int N, int grid_x) {
+    GemvPlan p{};
+    const bool norm = in_mode == IN_NORM || in_mode == IN_EMBED_NORM;
+    const size_t xs = ((size_t)(nb + (norm ? 1 : 0)) * K * 4 + 15) / 16 * 16;
+    int ns = g_stream_slots ? g_stream_slots : kAutoStages;
+    while (ns > 2 && (size_t)ns * kStage + xs > (size_t)kGemvMaxSmem) --ns;
+    p.n_ring = ns;
+    p.max_units = (N + grid_x - 1) / grid_x;
+    p.smem = (size_t)ns * kStage + xs;
+    p.ok = K % 8 == 0 && K >= 8 && p.smem <= (size_t)kGemvMaxSmem;
+    return p;
+}
+
+template <int NB, int IN, int OUT>
+static void launch_nb(const GemvArgs &a, dim3 grid, size_t smem, cudaStream_t s) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kTT);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaLaunchKernelEx(&cfg, k_gemv_stream<NB, IN, OUT>, a);
+}
+
+template <int IN, int OUT>
+static void launch_io(GemvArgs a, int grid_x, cudaStream_t s) {
+    const int nb = a.B < kGroupB ? a.B : kGroupB;
+    const GemvPlan p = gemv_stream_plan(IN, a.K, nb, a.N, grid_x);
+    a.n_ring = p.n_ring;
+    a.max_units = p.max_units;
+    const dim3 grid(grid_x, (a.B + kGroupB - 1) / kGroupB);
+    switch (nb) {
+    case 1: launch_nb<1, IN, OUT>(a, grid, p.smem, s); break;
+    case 2: launch_nb<2, IN, OUT>(a, grid, p.smem, s); break;
+    case 3: launch_nb<3, IN, OUT>(a, grid, p.smem, s); break;
+    default: launch_nb<4, IN, OUT>(a, grid, p.smem, s); break;
+    }
+}
+
+bool launch_gemv_stream(int in_mode, int out_mode, const GemvArgs &a, int grid_x, cudaStream_t s) {
+    const int nb = a.B < kGroupB ? a.B : kGroupB;
+    if (!gemv_stream_plan(in_mode, a.K, nb, a.N, grid_x).ok) return false;
+#define DEC_STREAM_CASE(I, O)            \
+    if (in_mode == I && out_mode == O) { \
+        launch_io<I, O>(a, grid_x, s);   \
+        return true;                     \
+    }
+    DEC_STREAM_CASE(IN_NORM, OUT_STORE)
+    DEC_STREAM_CASE(IN_EMBED_NORM, OUT_STORE)
+    DEC_STREAM_CASE(IN_PLAIN, OUT_RESID)
+    DEC_STREAM_CASE(IN_SWIGLU, OUT_RESID)
+    DEC_STREAM_CASE(IN_NORM, OUT_ARGMAX)
+    if (in_mode == IN_NORM && out_mode == OUT_SWIGLU && pairs_per_stage(a.K) > 0) {
+        launch_io<IN_NORM, OUT_SWIGLU>(a, grid_x, s);
+        return true;
+    }
+#undef DEC_STREAM_CASE
+    return false;
+}
+
+template <int NB, int IN, int OUT>
+static void init_nb() {
+    auto fn = k_gemv_stream<NB, IN, OUT>;
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
+    cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+}
+
+bool gemv_stream_swiglu_ok(int K, int nb, int ffn, int grid_x) {
+    return pairs_per_stage(K) > 0 && gemv_stream_plan(IN_NORM, K, nb, ffn, grid_x).ok;
+}
+
+template <int IN, int OUT>
+static void init_io() {
+    init_nb<1, IN, OUT>();
+    init_nb<2, IN, OUT>();
+    init_nb<3, IN, OUT>();
+    init_nb<4, IN, OUT>();
+}
+
+void init_gemv_stream_kernels() {
+    init_io<IN_NORM, OUT_STORE>();
+    init_io<IN_EMBED_NORM, OUT_STORE>();
+    init_io<IN_PLAIN, OUT_RESID>();
+    init_io<IN_SWIGLU, OUT_RESID>();
+    init_io<IN_NORM, OUT_ARGMAX>();
+    init_io<IN_NORM, OUT_SWIGLU>();
+}
+
+}  // namespace dec
