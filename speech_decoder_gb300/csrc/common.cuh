@@ -27,6 +27,14 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 }
 template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
 
+// Second bf16 plane of an activation: the rounding residual v - bf16(v), so
+// that hi + lo carries about 16 mantissa bits (the tensor-core GEMM reads both).
+__device__ __forceinline__ void store_planes(__nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t i, float v) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    hi[i] = h;
+    if (lo) lo[i] = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
 // Unpack 16 bytes into floats.
 __device__ __forceinline__ void unpack16(const uint4 &u, float (&f)[8], const __nv_bfloat16 *) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};

@@ -58,6 +58,8 @@ struct dec_handle {
     // prefill activations
     float *x = nullptr, *qkv = nullptr, *gu = nullptr;
     void *xn = nullptr, *q16 = nullptr, *attn_o = nullptr, *hbuf = nullptr;
+    // bf16 builds: second planes (rounding residuals) of the tensor-core GEMM inputs
+    void *xn_lo = nullptr, *attn_o_lo = nullptr, *hbuf_lo = nullptr;
     int32_t *row_pos = nullptr, *row_slot = nullptr, *last_row = nullptr, *ids_dev = nullptr;
     // decode activations and scratch
     float *xd = nullptr, *qkvd = nullptr, *od = nullptr, *gud = nullptr, *logits = nullptr;
@@ -189,12 +191,17 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     }
     h->rope = b.take<float2>((size_t)hp.max_ctx * (d / 2));
     h->x = b.take<float>(Tm * H);
-    h->xn = b.take<char>(Tm * std::max(H, F) * as);
+    const size_t Ta = std::max(Tm, Bm);                   // rows of the GEMM inputs (prompt rows or step rows)
+    const size_t lo = as == 2 ? 1 : 0;
+    h->xn = b.take<char>(Ta * std::max(H, F) * as);
+    h->xn_lo = lo ? b.take<char>(Ta * std::max(H, F) * as) : nullptr;
     h->qkv = b.take<float>(Tm * qkv_rows(hp));
     h->q16 = b.take<char>(Tm * nq * d * kvs);
-    h->attn_o = b.take<char>(Tm * nq * d * as);
+    h->attn_o = b.take<char>(Ta * nq * d * as);
+    h->attn_o_lo = lo ? b.take<char>(Ta * nq * d * as) : nullptr;
     h->gu = b.take<float>(Tm * 2 * F);
-    h->hbuf = b.take<char>(Tm * F * as);
+    h->hbuf = b.take<char>(Ta * F * as);
+    h->hbuf_lo = lo ? b.take<char>(Ta * F * as) : nullptr;
     h->row_pos = b.take<int32_t>(Tm);
     h->row_slot = b.take<int32_t>(Tm);
     h->last_row = b.take<int32_t>(Bm);
@@ -227,24 +234,26 @@ static int *dev_error(dec_handle *h) { return &h->st->error; }
 
 // Prompt-row projection C[M, N] (=|+=) A[M, K] W[N, K]^T: tcgen05 for bf16
 // weights, CUDA cores for the fp32 debug build.
-static void gemm(dec_handle *h, const void *A, const void *W, float *C, int ldc, int M, int N, int K, int epi) {
-    if (h->use_tc && h->w_bf16 && gemm_tc_plan(M, N, K, 1, h->num_sms, kTcScratchFloats).ok)
-        launch_gemm_tc(A, M, W, N, K, 1, epi, C, ldc, nullptr, 0, h->tc_scratch, kTcScratchFloats, dev_error(h),
-                       h->num_sms, h->stream);   // a launch error surfaces at the end of the pass
+// A_lo: the second bf16 plane of A (bf16 builds), read by the tensor-core path.
+static void gemm(dec_handle *h, const void *A, const void *A_lo, const void *W, float *C, int ldc, int M, int N, int K,
+                 int epi) {
+    if (h->use_tc && h->w_bf16 && gemm_tc_plan(M, N, K, 1, h->num_sms, kTcScratchFloats, 0, A_lo ? 2 : 1).ok)
+        launch_gemm_tc(A, A_lo, M, W, N, K, 1, epi, C, ldc, nullptr, nullptr, 0, h->tc_scratch, kTcScratchFloats,
+                       dev_error(h), h->num_sms, h->stream);   // a launch error surfaces at the end of the pass
     else
         launch_gemm_simt(A, h->w_bf16, W, h->w_bf16, C, ldc, M, N, K, epi, h->stream);
     h->enq++;
 }
 
-// Gate|up projection and SwiGLU into h->hbuf.
-static void gemm_swiglu(dec_handle *h, const void *A, const void *Wgu, int M, int F, int K) {
-    if (h->use_tc && h->w_bf16 && gemm_tc_plan(M, 2 * F, K, 2, h->num_sms, kTcScratchFloats).ok) {
-        launch_gemm_tc(A, M, Wgu, 2 * F, K, 2, EPI_SWIGLU_BF16, nullptr, 0, h->hbuf, F, h->tc_scratch,
-                       kTcScratchFloats, dev_error(h), h->num_sms, h->stream);
+// Gate|up projection and SwiGLU into h->hbuf (and its second plane).
+static void gemm_swiglu(dec_handle *h, const void *A, const void *A_lo, const void *Wgu, int M, int F, int K) {
+    if (h->use_tc && h->w_bf16 && gemm_tc_plan(M, 2 * F, K, 2, h->num_sms, kTcScratchFloats, 0, A_lo ? 2 : 1).ok) {
+        launch_gemm_tc(A, A_lo, M, Wgu, 2 * F, K, 2, EPI_SWIGLU_BF16, nullptr, 0, h->hbuf, h->hbuf_lo, F,
+                       h->tc_scratch, kTcScratchFloats, dev_error(h), h->num_sms, h->stream);
         h->enq++;
     } else {
         launch_gemm_simt(A, h->w_bf16, Wgu, h->w_bf16, h->gu, 2 * F, M, 2 * F, K, EPI_STORE_F32, h->stream);
-        launch_swiglu(h->gu, h->hbuf, h->w_bf16, M, F, h->stream);
+        launch_swiglu(h->gu, h->hbuf, h->hbuf_lo, h->w_bf16, M, F, h->stream);
         h->enq += 2;
     }
 }
@@ -264,9 +273,9 @@ static void enqueue_decode_layer_tc(dec_handle *h, int l, int B, bool from_embed
         launch_embed_rows(h->embed, h->w_bf16, h->st, h->xd, B, H, s);
         h->enq++;
     }
-    launch_rmsnorm_rows(h->xd, L.attn_norm, hp.rms_eps, h->xn, true, B, H, s);
+    launch_rmsnorm_rows(h->xd, L.attn_norm, hp.rms_eps, h->xn, h->xn_lo, true, B, H, s);
     h->enq++;
-    gemm(h, h->xn, L.wqkv, h->qkvd, qkv_rows(hp), B, qkv_rows(hp), H, EPI_STORE_F32);
+    gemm(h, h->xn, h->xn_lo, L.wqkv, h->qkvd, qkv_rows(hp), B, qkv_rows(hp), H, EPI_STORE_F32);
 
     AttnDecArgs a{};
     a.qkv = h->qkvd;
@@ -279,6 +288,7 @@ static void enqueue_decode_layer_tc(dec_handle *h, int l, int B, bool from_embed
     a.slots = (int)h->slots;
     a.o = h->od;
     a.o_bf16 = static_cast<__nv_bfloat16 *>(h->attn_o);
+    a.o_bf16_lo = static_cast<__nv_bfloat16 *>(h->attn_o_lo);
     a.part = h->attn_part;
     a.counter = h->attn_counter;
     a.st = h->st;
@@ -289,11 +299,11 @@ static void enqueue_decode_layer_tc(dec_handle *h, int l, int B, bool from_embed
     a.append = 1;
     launch_attn_decode(h->kv_f16, a, splits_for(h, B), s);
     h->enq++;
-    gemm(h, h->attn_o, L.wo, h->xd, H, B, H, nqd, EPI_RESID_F32);
-    launch_rmsnorm_rows(h->xd, L.ffn_norm, hp.rms_eps, h->xn, true, B, H, s);
+    gemm(h, h->attn_o, h->attn_o_lo, L.wo, h->xd, H, B, H, nqd, EPI_RESID_F32);
+    launch_rmsnorm_rows(h->xd, L.ffn_norm, hp.rms_eps, h->xn, h->xn_lo, true, B, H, s);
     h->enq++;
-    gemm_swiglu(h, h->xn, L.wgu, B, F, H);
-    gemm(h, h->hbuf, L.wd, h->xd, H, B, H, F, EPI_RESID_F32);
+    gemm_swiglu(h, h->xn, h->xn_lo, L.wgu, B, F, H);
+    gemm(h, h->hbuf, h->hbuf_lo, L.wd, h->xd, H, B, H, F, EPI_RESID_F32);
 }
 
 // The GEMV that runs next streams W [N, K]: let this one pull its first rows into L2.
@@ -403,8 +413,8 @@ static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
 static void enqueue_head(dec_handle *h, int B) {
     if (batched_path(h, B)) {
         const dec_hparams &hp = h->hp;
-        launch_rmsnorm_rows(h->xd, h->final_norm, hp.rms_eps, h->xn, true, B, hp.hidden, h->stream);
-        gemm(h, h->xn, h->embed, h->logits, hp.vocab, B, hp.vocab, hp.hidden, EPI_STORE_F32);
+        launch_rmsnorm_rows(h->xd, h->final_norm, hp.rms_eps, h->xn, h->xn_lo, true, B, hp.hidden, h->stream);
+        gemm(h, h->xn, h->xn_lo, h->embed, h->logits, hp.vocab, B, hp.vocab, hp.hidden, EPI_STORE_F32);
         launch_argmax_rows(h->logits, B, hp.vocab, h->st, h->out_ids, hp.max_new, h->stream);
         h->enq += 2;
         return;
@@ -547,8 +557,8 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
     }
     for (int l = 0; l < hp.n_layers; ++l) {
         const DevLayer &L = h->L[l];
-        launch_rmsnorm_rows(h->x, L.attn_norm, hp.rms_eps, h->xn, h->w_bf16, total, H, s);
-        gemm(h, h->xn, L.wqkv, h->qkv, qkv_rows(hp), total, qkv_rows(hp), H, EPI_STORE_F32);
+        launch_rmsnorm_rows(h->x, L.attn_norm, hp.rms_eps, h->xn, h->xn_lo, h->w_bf16, total, H, s);
+        gemm(h, h->xn, h->xn_lo, L.wqkv, h->qkv, qkv_rows(hp), total, qkv_rows(hp), H, EPI_STORE_F32);
         RopeKvArgs r{};
         r.qkv = h->qkv;
         r.qn_w = L.qn;
@@ -575,16 +585,17 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
             a.row_pos = h->row_pos;
             a.row_slot = h->row_slot;
             a.o = h->attn_o;
+            a.o_lo = h->attn_o_lo;
             a.slots = (int)h->slots;
             a.T = total;
             a.nq = hp.n_heads;
             a.nkv = hp.n_kv_heads;
             a.d = hp.head_dim;
             launch_attn_prefill_simt(h->kv_f16, h->w_bf16, a, s);
-            gemm(h, h->attn_o, L.wo, h->x, H, total, H, nqd, EPI_RESID_F32);
-            launch_rmsnorm_rows(h->x, L.ffn_norm, hp.rms_eps, h->xn, h->w_bf16, total, H, s);
-            gemm_swiglu(h, h->xn, L.wgu, total, F, H);
-            gemm(h, h->hbuf, L.wd, h->x, H, total, H, F, EPI_RESID_F32);
+            gemm(h, h->attn_o, h->attn_o_lo, L.wo, h->x, H, total, H, nqd, EPI_RESID_F32);
+            launch_rmsnorm_rows(h->x, L.ffn_norm, hp.rms_eps, h->xn, h->xn_lo, h->w_bf16, total, H, s);
+            gemm_swiglu(h, h->xn, h->xn_lo, L.wgu, total, F, H);
+            gemm(h, h->hbuf, h->hbuf_lo, L.wd, h->x, H, total, H, F, EPI_RESID_F32);
             h->enq += 2;
             if (h->dumps && l == 0) {
                 CK(cudaMemcpyAsync(h->dump_b0, h->x, (size_t)total * H * 4, cudaMemcpyDeviceToDevice, s));
@@ -600,7 +611,7 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
     }
     if (h->dumps) {
         CK(cudaMemcpyAsync(h->dump_blast, h->xd, (size_t)B * H * 4, cudaMemcpyDeviceToDevice, s));
-        launch_rmsnorm_rows(h->xd, h->final_norm, hp.rms_eps, h->dump_final, false, B, H, s);
+        launch_rmsnorm_rows(h->xd, h->final_norm, hp.rms_eps, h->dump_final, nullptr, false, B, H, s);
     }
     enqueue_head(h, B);
     CK(cudaGetLastError());
@@ -1141,10 +1152,10 @@ dec_status dec_profile_kernel(dec_handle *h, int32_t op, int32_t iters, float *a
             const DevLayer &L = h->L[l];
             if (op == 0 && batched_path(h, B)) {
                 // tensor-core projections of the batched step (GEMM + split-K reduction each)
-                gemm(h, h->xn, L.wqkv, h->qkvd, qkv_rows(hp), B, qkv_rows(hp), H, EPI_STORE_F32);
-                bytes += (double)qkv_rows(hp) * H * ws + (double)B * H * 2.0 + (double)B * qkv_rows(hp) * 4.0;
-                gemm_swiglu(h, h->xn, L.wgu, B, F, H);
-                bytes += (double)2 * F * H * ws + (double)B * H * 2.0 + (double)B * F * 2.0;
+                gemm(h, h->xn, h->xn_lo, L.wqkv, h->qkvd, qkv_rows(hp), B, qkv_rows(hp), H, EPI_STORE_F32);
+                bytes += (double)qkv_rows(hp) * H * ws + (double)B * H * 4.0 + (double)B * qkv_rows(hp) * 4.0;
+                gemm_swiglu(h, h->xn, h->xn_lo, L.wgu, B, F, H);
+                bytes += (double)2 * F * H * ws + (double)B * H * 4.0 + (double)B * F * 4.0;
                 launches += 2;
             } else if (op == 0) {
                 GemvArgs g{};
@@ -1253,8 +1264,8 @@ dec_status dec_debug_gemm(const void *X, int32_t T, const void *W, int32_t n_fea
     if (use_tc) {
         const int groups = epi == 2 ? 2 : 1;
         if (!gemm_tc_plan(T, n_feat, K, groups, sms, floats, splits).ok) return DEC_ERR_INVALID_ARG;
-        cudaError_t e = launch_gemm_tc(X, T, W, n_feat, K, groups, epi, C, ldc, Hout, ldh, static_cast<float *>(scratch),
-                                       floats, nullptr, sms, s, splits);
+        cudaError_t e = launch_gemm_tc(X, nullptr, T, W, n_feat, K, groups, epi, C, ldc, Hout, nullptr, ldh,
+                                       static_cast<float *>(scratch), floats, nullptr, sms, s, splits);
         if (e != cudaSuccess) cudaGetLastError();
         return e == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
     }

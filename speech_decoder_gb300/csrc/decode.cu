@@ -168,7 +168,7 @@ __device__ void attn_finish(const AttnDecArgs &a, AttnSmem<D, W> &sm, int b, int
             }
             const size_t oi = (size_t)b * a.nq * D + (size_t)(g * n_rep + r) * D + i;
             a.o[oi] = A / L;
-            if (a.o_bf16) a.o_bf16[oi] = __float2bfloat16_rn(A / L);
+            if (a.o_bf16) store_planes(a.o_bf16, a.o_bf16_lo, oi, A / L);
         }
         return;
     }
@@ -227,7 +227,7 @@ __device__ void attn_finish(const AttnDecArgs &a, AttnSmem<D, W> &sm, int b, int
         for (int t = 0; t < n_used; ++t) A = fmaf(__ldcg(pb + ((size_t)t * n_rep + r) * (D + 2) + i), sm.cw[t][r], A);
         const size_t oi = (size_t)b * a.nq * D + (size_t)(g * n_rep + r) * D + i;
         a.o[oi] = A;
-        if (a.o_bf16) a.o_bf16[oi] = __float2bfloat16_rn(A);
+        if (a.o_bf16) store_planes(a.o_bf16, a.o_bf16_lo, oi, A);
     }
     if (tid == 0) a.counter[b * nkv + g] = 0u;
 }

@@ -75,6 +75,7 @@ struct AttnDecArgs {
     const int32_t *kv_off;  // [B] first slot of each sequence
     const int32_t *kv_len;  // [B] visible keys (rows with len <= 0 or out of range are skipped)
     __nv_bfloat16 *o_bf16;  // optional bf16 copy of o (input of the tensor-core O projection)
+    __nv_bfloat16 *o_bf16_lo;  // with o_bf16: the bf16 rounding residual (may be null)
 
 };
 

@@ -15,6 +15,14 @@
 // (model.cpp, load: pack_gate_up; decoder.cpp header: SwiGLU on packed
 // gate_up).
 //
+// Activations in two planes: X = X_hi + X_lo, both bf16 (X_lo the bf16
+// rounding of the residual x - X_hi), so the product carries about 16
+// mantissa bits of each activation while the weights stay bf16; every K step
+// issues one MMA per plane into the same accumulator.  Over 28 blocks a single
+// bf16 rounding of every projection input alone moves the logits by about
+// 2.4e-2 of their largest magnitude; with both planes the activations add
+// next to nothing to the error.
+//
 // When a GEMM has fewer output tiles than SMs (short prompts), K is split
 // across CTAs; each split writes its partial tile to scratch and a second,
 // fully parallel kernel sums the splits in split order (deterministic) and
@@ -34,11 +42,12 @@ constexpr uint32_t kTcPolls = 1u << 24; // bounded mbarrier waits
 struct TcArgs {
     int n_feat, T, K;
     int groups;                  // 1, or 2 for gate|up blocks
+    int planes;                  // activation planes: 1 (X) or 2 (X_hi, X_lo)
     int BN, n_stages, k_tiles, splits, kt_per_split;
     int epi;
     float *C;
     int ldc;
-    __nv_bfloat16 *Hout;
+    __nv_bfloat16 *Hout, *Hout_lo;  // SwiGLU output planes (Hout_lo may be null)
     int ldh;
     float *part;
     int *err;
@@ -103,7 +112,10 @@ __device__ __forceinline__ void tc_report(int *err, int code) {
 __device__ __forceinline__ void epi_store(const TcArgs &a, int f, int t, float v, float up) {
     if (t >= a.T) return;
     if (a.epi == EPI_SWIGLU_BF16) {
-        a.Hout[(size_t)t * a.ldh + f] = __float2bfloat16_rn(v / (1.f + expf(-v)) * up);
+        const float h = v / (1.f + expf(-v)) * up;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(h);
+        a.Hout[(size_t)t * a.ldh + f] = hi;
+        if (a.Hout_lo) a.Hout_lo[(size_t)t * a.ldh + f] = __float2bfloat16_rn(h - __bfloat162float(hi));
     } else if (f < a.n_feat) {
         float *c = a.C + (size_t)t * a.ldc + f;
         if (a.epi == EPI_STORE_F32) *c = v;
@@ -112,13 +124,14 @@ __device__ __forceinline__ void epi_store(const TcArgs &a, int f, int t, float v
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, TcArgs a) {
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+              const __grid_constant__ CUtensorMap tmB2, TcArgs a) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = a.n_stages;
     const uint32_t a_bytes = (uint32_t)a.groups * 16384u, b_bytes = (uint32_t)a.BN * 128u;
-    const uint32_t stage_bytes = a_bytes + b_bytes;
+    const uint32_t stage_bytes = a_bytes + (uint32_t)a.planes * b_bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * stage_bytes);
     uint64_t *empty = full + S;
     uint64_t *done = empty + S;
@@ -167,6 +180,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             unsigned char *st = smem + (size_t)s * stage_bytes;
             tma_load_2d(st, &tmA, (kt0 + i) * kBK, m0, &full[s]);
             tma_load_2d(st + a_bytes, &tmB, (kt0 + i) * kBK, n0, &full[s]);
+            if (a.planes == 2) tma_load_2d(st + a_bytes + b_bytes, &tmB2, (kt0 + i) * kBK, n0, &full[s]);
             issued = i + 1;
         }
     } else if (warp == 1 && lane == 0) {
@@ -182,10 +196,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t abase = ptx::smem_u32(smem + (size_t)s * stage_bytes), bbase = abase + a_bytes;
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
-                const uint64_t bdesc = sw128_desc(bbase + kk * 32);
-                for (int g = 0; g < a.groups; ++g)
-                    mma_bf16(tmem + (uint32_t)(g * a.BN), sw128_desc(abase + g * 16384 + kk * 32), bdesc, a.idesc,
-                             (i | kk) != 0);
+                for (int pl = 0; pl < a.planes; ++pl) {
+                    const uint64_t bdesc = sw128_desc(bbase + pl * b_bytes + kk * 32);
+                    for (int g = 0; g < a.groups; ++g)
+                        mma_bf16(tmem + (uint32_t)(g * a.BN), sw128_desc(abase + g * 16384 + kk * 32), bdesc, a.idesc,
+                                 (i | kk | pl) != 0);
+                }
             }
             mma_commit(&empty[s]);                     // stage free once these MMAs have read it
         }
@@ -300,13 +316,16 @@ static bool make_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t K,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-TcPlan gemm_tc_plan(int T, int n_feat, int K, int groups, int num_sms, size_t scratch_floats, int force_splits) {
+TcPlan gemm_tc_plan(int T, int n_feat, int K, int groups, int num_sms, size_t scratch_floats, int force_splits,
+                    int planes) {
     TcPlan p{};
-    p.ok = g_tc_ready && T >= 1 && K % kBK == 0 && n_feat % (128 * groups) == 0;
+    p.ok = g_tc_ready && T >= 1 && K % kBK == 0 && n_feat % (128 * groups) == 0 && (planes == 1 || planes == 2);
     if (!p.ok) return p;
-    const int BN = T <= 256 ? ((T + 15) / 16) * 16 : 256;
+    // two activation planes: N tiles of at most 128 tokens keep three or more stages
+    const int bn_max = planes == 2 ? 128 : 256;
+    const int BN = T <= bn_max ? ((T + 15) / 16) * 16 : bn_max;
     p.BN = BN;
-    const size_t stage = (size_t)groups * 16384 + (size_t)BN * 128;
+    const size_t stage = (size_t)groups * 16384 + (size_t)planes * BN * 128;
     const size_t budget = (size_t)g_max_dyn_smem - 1024 - 256;     // alignment pad + barriers
     p.n_stages = (int)std::min<size_t>(8, budget / stage);
     if (p.n_stages < 2) {
@@ -331,20 +350,23 @@ TcPlan gemm_tc_plan(int T, int n_feat, int K, int groups, int num_sms, size_t sc
     return p;
 }
 
-cudaError_t launch_gemm_tc(const void *X, int T, const void *W, int n_feat, int K, int groups, int epi, float *C,
-                           int ldc, void *Hout, int ldh, float *scratch, size_t scratch_floats, int *err, int num_sms,
-                           cudaStream_t s, int force_splits) {
-    const TcPlan p = gemm_tc_plan(T, n_feat, K, groups, num_sms, scratch_floats, force_splits);
+cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K, int groups,
+                           int epi, float *C, int ldc, void *Hout, void *Hout_lo, int ldh, float *scratch,
+                           size_t scratch_floats, int *err, int num_sms, cudaStream_t s, int force_splits) {
+    const int planes = X_lo ? 2 : 1;
+    const TcPlan p = gemm_tc_plan(T, n_feat, K, groups, num_sms, scratch_floats, force_splits, planes);
     if (!p.ok) return cudaErrorInvalidValue;
-    CUtensorMap mA, mB;
+    CUtensorMap mA, mB, mB2;
     if (!make_map(&mA, W, (uint64_t)n_feat, (uint64_t)K, 128u * groups) ||
-        !make_map(&mB, X, (uint64_t)T, (uint64_t)K, (uint32_t)p.BN))
+        !make_map(&mB, X, (uint64_t)T, (uint64_t)K, (uint32_t)p.BN) ||
+        !make_map(&mB2, X_lo ? X_lo : X, (uint64_t)T, (uint64_t)K, (uint32_t)p.BN))
         return cudaErrorInvalidValue;
     TcArgs a{};
     a.n_feat = groups == 2 ? n_feat / 2 : n_feat;
     a.T = T;
     a.K = K;
     a.groups = groups;
+    a.planes = planes;
     a.BN = p.BN;
     a.n_stages = p.n_stages;
     a.k_tiles = p.k_tiles;
@@ -354,6 +376,7 @@ cudaError_t launch_gemm_tc(const void *X, int T, const void *W, int n_feat, int 
     a.C = C;
     a.ldc = ldc;
     a.Hout = static_cast<__nv_bfloat16 *>(Hout);
+    a.Hout_lo = static_cast<__nv_bfloat16 *>(Hout_lo);
     a.ldh = ldh;
     a.part = scratch;
     a.err = err;
@@ -361,7 +384,7 @@ cudaError_t launch_gemm_tc(const void *X, int T, const void *W, int n_feat, int 
     a.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(p.BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
     a.tmem_cols = (uint32_t)p.tmem_cols;
     dim3 grid(p.mt, p.nt, p.splits);
-    k_gemm_tc<<<grid, kTcThreads, p.smem, s>>>(mA, mB, a);
+    k_gemm_tc<<<grid, kTcThreads, p.smem, s>>>(mA, mB, mB2, a);
     if (p.splits > 1) {
         const long long threads = (long long)p.mt * p.nt * p.BN * 32;
         k_splitk_reduce<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(a, p.mt);

@@ -16,16 +16,19 @@ struct TcPlan {
 };
 
 // Y = X W^T for X [T, K] (bf16 rows of the prompt) and W [n_feat, K] (bf16
-// weights).  epi: EPI_STORE_F32 writes C[t][f]; EPI_RESID_F32 adds into C;
+// weights).  X_lo (may be null) is a second bf16 plane of the same shape with
+// X + X_lo the activation (the bf16 rounding residual): both planes enter the
+// product.  epi: EPI_STORE_F32 writes C[t][f]; EPI_RESID_F32 adds into C;
 // EPI_SWIGLU_BF16 (groups = 2, W packed in blocks of 128 gate rows + 128 up
-// rows) writes Hout[t][f] = silu(gate) * up for f < n_feat / 2.
+// rows) writes Hout[t][f] = bf16(silu(gate) * up) for f < n_feat / 2 and, if
+// Hout_lo is not null, the bf16 rounding residual into Hout_lo.
 // scratch holds split-K partial tiles, summed by a second kernel in split
 // order; err receives a device error code if a bounded wait expires.
 TcPlan gemm_tc_plan(int T, int n_feat, int K, int groups, int num_sms, size_t scratch_floats,
-                    int force_splits = 0);
-cudaError_t launch_gemm_tc(const void *X, int T, const void *W, int n_feat, int K, int groups, int epi, float *C,
-                           int ldc, void *Hout, int ldh, float *scratch, size_t scratch_floats, int *err, int num_sms,
-                           cudaStream_t s, int force_splits = 0);
+                    int force_splits = 0, int planes = 1);
+cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K, int groups,
+                           int epi, float *C, int ldc, void *Hout, void *Hout_lo, int ldh, float *scratch,
+                           size_t scratch_floats, int *err, int num_sms, cudaStream_t s, int force_splits = 0);
 void init_gemm_tc();
 bool gemm_tc_ready();
 

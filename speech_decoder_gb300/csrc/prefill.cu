@@ -13,7 +13,7 @@ namespace dec {
 // ------------------------------------------------------------------ RMSNorm
 template <typename TO>
 __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float *x, const float *w, float eps, TO *out,
-                                                      int H) {
+                                                      TO *out_lo, int H) {
     __shared__ float red[32];
     const size_t t = blockIdx.x;
     const float *xr = x + t * H;
@@ -21,14 +21,19 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float *x, const floa
     for (int k = threadIdx.x; k < H; k += blockDim.x) ss += xr[k] * xr[k];
     ss = block_sum(ss, red);
     const float r = rsqrtf(ss / (float)H + eps);
-    for (int k = threadIdx.x; k < H; k += blockDim.x) out[t * H + k] = from_f32<TO>(xr[k] * r * w[k]);
+    for (int k = threadIdx.x; k < H; k += blockDim.x) {
+        const float v = xr[k] * r * w[k];
+        if constexpr (sizeof(TO) == 2) store_planes(out, out_lo, t * H + k, v);
+        else out[t * H + k] = v;
+    }
 }
 
-void launch_rmsnorm_rows(const float *x, const float *w, float eps, void *out, bool act_bf16, int T, int H,
-                         cudaStream_t s) {
+void launch_rmsnorm_rows(const float *x, const float *w, float eps, void *out, void *out_lo, bool act_bf16, int T,
+                         int H, cudaStream_t s) {
     if (T <= 0) return;
-    if (act_bf16) k_rmsnorm_rows<__nv_bfloat16><<<T, 256, 0, s>>>(x, w, eps, (__nv_bfloat16 *)out, H);
-    else k_rmsnorm_rows<float><<<T, 256, 0, s>>>(x, w, eps, (float *)out, H);
+    if (act_bf16)
+        k_rmsnorm_rows<__nv_bfloat16><<<T, 256, 0, s>>>(x, w, eps, (__nv_bfloat16 *)out, (__nv_bfloat16 *)out_lo, H);
+    else k_rmsnorm_rows<float><<<T, 256, 0, s>>>(x, w, eps, (float *)out, nullptr, H);
 }
 
 // ------------------------------------------------------------------ SIMT GEMM
@@ -103,23 +108,25 @@ void launch_gemm_simt(const void *A, bool a_bf16, const void *W, bool w_bf16, fl
 
 // ------------------------------------------------------------------ SwiGLU
 template <typename TO>
-__global__ void k_swiglu(const float *gu, TO *h, int T, int F) {
+__global__ void k_swiglu(const float *gu, TO *h, TO *h_lo, int T, int F) {
     const size_t n = (size_t)T * F;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
         const size_t t = i / F;
         const int f = (int)(i % F), blk = f >> 7, j = f & 127;
         const float *row = gu + t * 2 * F;
         const float g = row[blk * 256 + j], u = row[blk * 256 + 128 + j];
-        h[i] = from_f32<TO>(g / (1.f + expf(-g)) * u);
+        const float v = g / (1.f + expf(-g)) * u;
+        if constexpr (sizeof(TO) == 2) store_planes(h, h_lo, i, v);
+        else h[i] = v;
     }
 }
 
-void launch_swiglu(const float *gu, void *h, bool act_bf16, int T, int F, cudaStream_t s) {
+void launch_swiglu(const float *gu, void *h, void *h_lo, bool act_bf16, int T, int F, cudaStream_t s) {
     if (T <= 0) return;
     const size_t n = (size_t)T * F;
     const int grid = (int)((n + 255) / 256 < 65535 * 4 ? (n + 255) / 256 : 65535 * 4);
-    if (act_bf16) k_swiglu<__nv_bfloat16><<<grid, 256, 0, s>>>(gu, (__nv_bfloat16 *)h, T, F);
-    else k_swiglu<float><<<grid, 256, 0, s>>>(gu, (float *)h, T, F);
+    if (act_bf16) k_swiglu<__nv_bfloat16><<<grid, 256, 0, s>>>(gu, (__nv_bfloat16 *)h, (__nv_bfloat16 *)h_lo, T, F);
+    else k_swiglu<float><<<grid, 256, 0, s>>>(gu, (float *)h, nullptr, T, F);
 }
 
 // ------------------------------------------------------------------ Q/K norm + RoPE + KV write
@@ -237,10 +244,15 @@ __global__ void __launch_bounds__(256) k_attn_prefill_simt(AttnPrefillArgs a, fl
         l = l * corr + ls;
         m = mb;
     }
-    TO *o = reinterpret_cast<TO *>(a.o) + (size_t)t * a.nq * D + (size_t)h * D + lane * PL;
+    const size_t oi = (size_t)t * a.nq * D + (size_t)h * D + lane * PL;
     const float inv = 1.f / l;
 #pragma unroll
-    for (int e = 0; e < PL; ++e) o[e] = from_f32<TO>(acc[e] * inv);
+    for (int e = 0; e < PL; ++e) {
+        if constexpr (sizeof(TO) == 2)
+            store_planes(reinterpret_cast<__nv_bfloat16 *>(a.o), reinterpret_cast<__nv_bfloat16 *>(a.o_lo), oi + e,
+                         acc[e] * inv);
+        else reinterpret_cast<float *>(a.o)[oi + e] = acc[e] * inv;
+    }
 }
 
 template <typename TKV, typename TO>

@@ -4,16 +4,18 @@
 
 namespace dec {
 
-// rows of x (float32 [T, H]) -> RMSNorm(x) * w in bf16 (act_bf16) or float32
-void launch_rmsnorm_rows(const float *x, const float *w, float eps, void *out, bool act_bf16, int T,
+// rows of x (float32 [T, H]) -> RMSNorm(x) * w in bf16 (act_bf16; out_lo, if not
+// null, receives the bf16 rounding residual) or float32
+void launch_rmsnorm_rows(const float *x, const float *w, float eps, void *out, void *out_lo, bool act_bf16, int T,
                          int H, cudaStream_t s);
 
 // C[M, N] (float32, row stride ldc) = or += A[M, K] . W[N, K]^T on CUDA cores
 void launch_gemm_simt(const void *A, bool a_bf16, const void *W, bool w_bf16, float *C, int ldc,
                       int M, int N, int K, int epi, cudaStream_t s);
 
-// h[t, f] = silu(gate) * up from the packed gate|up rows (blocks of 128 + 128)
-void launch_swiglu(const float *gu, void *h, bool act_bf16, int T, int F, cudaStream_t s);
+// h[t, f] = silu(gate) * up from the packed gate|up rows (blocks of 128 + 128);
+// h_lo as for launch_rmsnorm_rows
+void launch_swiglu(const float *gu, void *h, void *h_lo, bool act_bf16, int T, int F, cudaStream_t s);
 
 struct RopeKvArgs {
     const float *qkv;          // [T, (nq + 2 nkv) d]
@@ -33,6 +35,7 @@ struct AttnPrefillArgs {
     const void *Kc, *Vc;       // pool [nkv][slots][d]
     const int32_t *row_pos, *row_slot;
     void *o;                   // [T, nq d] (bf16 or f32)
+    void *o_lo;                // bf16 rounding residual of o (bf16 output; may be null)
     int slots, T, nq, nkv, d;
 };
 void launch_attn_prefill_simt(bool kv_f16, bool out_bf16, const AttnPrefillArgs &a, cudaStream_t s);
