@@ -16,6 +16,7 @@ decoder has no data-path exchange); rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import csv
 import hashlib
 import json
@@ -46,6 +47,9 @@ def parse():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--layers", type=int, default=0,
+                   help="profiling only: keep the workload's shapes but run this many blocks "
+                        "(the JSON line then names the reduced model and is not a benchmark value)")
     return p.parse_args()
 
 
@@ -117,6 +121,14 @@ class Clocks:
                 "samples": len(sm)}
 
 
+def workload_for(args):
+    wl = synth.workload(args.workload)
+    if args.layers > 0:
+        m = dataclasses.replace(wl.model, n_layers=args.layers, name=f"{wl.model.name}-{args.layers}blocks")
+        wl = dataclasses.replace(wl, model=m, name=f"{wl.name}-{args.layers}blocks")
+    return wl
+
+
 def kernel_sha() -> str:
     h = hashlib.sha256()
     for f in ("gemv.cu", "gemv_stream.cu", "decode.cuh", "common.cuh", "ptx.cuh"):
@@ -169,7 +181,7 @@ def run_ours(args):
     __graft_entry__.build()
     from speech_decoder_gb300.binding import Decoder
 
-    wl = synth.workload(args.workload)
+    wl = workload_for(args)
     spec = wl.model
     w = synth.model_weights(spec, seed=wl.seed)
     items = workload_inputs(wl, w)
@@ -340,7 +352,7 @@ def run_reference(args):
     if rank != 0:
         return
     import oracle as O
-    wl = synth.workload(args.workload)
+    wl = workload_for(args)
     spec = wl.model
     w = synth.model_weights(spec, seed=wl.seed)
     item = synth.prompt_inputs(spec, wl.prompts[0], seed=wl.seed, item=0)

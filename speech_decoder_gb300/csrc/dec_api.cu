@@ -61,6 +61,13 @@ struct dec_handle {
     // bf16 builds: second planes (rounding residuals) of the tensor-core GEMM inputs
     void *xn_lo = nullptr, *attn_o_lo = nullptr, *hbuf_lo = nullptr;
     int32_t *row_pos = nullptr, *row_slot = nullptr, *last_row = nullptr, *ids_dev = nullptr;
+    // tensor-core prompt attention: V^T of the layer's prompt rows [nkv d][vt_ld]
+    // (fp16, zeroed once), each row's V^T column, query tiles, per-item offsets
+    void *vt = nullptr;
+    int vt_ld = 0;
+    int32_t *row_vtcol = nullptr, *item_kv_off = nullptr, *item_vt_col = nullptr;
+    int4 *attn_tiles = nullptr;
+    bool tc_attn = false;
     // decode activations and scratch
     float *xd = nullptr, *qkvd = nullptr, *od = nullptr, *gud = nullptr, *logits = nullptr;
     float *attn_part = nullptr;
@@ -81,7 +88,8 @@ struct dec_handle {
     int n_seq = 0;
     bool prefilled = false;
     int logits_rows = 0;
-    std::vector<int32_t> h_row_pos, h_row_slot, h_last_row;
+    std::vector<int32_t> h_row_pos, h_row_slot, h_last_row, h_row_vtcol, h_item_kv_off, h_item_vt_col;
+    std::vector<int4> h_tiles;
     // graphs
     cudaGraphExec_t step_exec = nullptr;
     int step_B = -1;
@@ -205,6 +213,13 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     h->row_pos = b.take<int32_t>(Tm);
     h->row_slot = b.take<int32_t>(Tm);
     h->last_row = b.take<int32_t>(Bm);
+    // items start at multiples of 128 columns of V^T
+    h->vt_ld = (int)(((Tm + 128 * Bm) + 127) / 128 * 128);
+    h->vt = kvs == 2 && d == 128 ? b.take<char>(nkv * d * (size_t)h->vt_ld * 2) : nullptr;
+    h->row_vtcol = b.take<int32_t>(Tm);
+    h->item_kv_off = b.take<int32_t>(Bm);
+    h->item_vt_col = b.take<int32_t>(Bm);
+    h->attn_tiles = b.take<int4>(Tm / 128 + Bm + 1);
     h->ids_dev = b.take<int32_t>(Tm);
     h->xd = b.take<float>(Bm * H);
     h->qkvd = b.take<float>(Bm * qkv_rows(hp));
@@ -524,6 +539,11 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
     h->h_row_pos.resize(total);
     h->h_row_slot.resize(total);
     h->h_last_row.resize(B);
+    h->h_row_vtcol.resize(total);
+    h->h_item_kv_off.resize(B);
+    h->h_item_vt_col.resize(B);
+    h->h_tiles.clear();
+    int vt_col = 0;
     SeqState &st = h->hst;
     std::memset(&st, 0, sizeof(st));
     int off = 0;
@@ -533,7 +553,12 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
         for (int t = 0; t < T; ++t) {
             h->h_row_pos[cu[b] + t] = t;
             h->h_row_slot[cu[b] + t] = off + t;
+            h->h_row_vtcol[cu[b] + t] = vt_col + t;
         }
+        h->h_item_kv_off[b] = off;
+        h->h_item_vt_col[b] = vt_col;
+        for (int q0 = 0; q0 < T; q0 += 128) h->h_tiles.push_back(make_int4(cu[b] + q0, q0, std::min(128, T - q0), b));
+        vt_col += (T + 127) / 128 * 128;
         h->h_last_row[b] = cu[b + 1] - 1;
         st.n_past[b] = T - 1;            // the head pass processes the last row
         st.kv_off[b] = off;
@@ -547,6 +572,16 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
     CK(cudaMemcpyAsync(h->row_pos, h->h_row_pos.data(), total * 4, cudaMemcpyHostToDevice, s));
     CK(cudaMemcpyAsync(h->row_slot, h->h_row_slot.data(), total * 4, cudaMemcpyHostToDevice, s));
     CK(cudaMemcpyAsync(h->last_row, h->h_last_row.data(), B * 4, cudaMemcpyHostToDevice, s));
+    if (h->tc_attn) {
+        // longest causal ranges first: the tail of the grid is short tiles
+        std::stable_sort(h->h_tiles.begin(), h->h_tiles.end(),
+                         [](const int4 &u, const int4 &v) { return u.y + u.z > v.y + v.z; });
+        CK(cudaMemcpyAsync(h->row_vtcol, h->h_row_vtcol.data(), total * 4, cudaMemcpyHostToDevice, s));
+        CK(cudaMemcpyAsync(h->item_kv_off, h->h_item_kv_off.data(), B * 4, cudaMemcpyHostToDevice, s));
+        CK(cudaMemcpyAsync(h->item_vt_col, h->h_item_vt_col.data(), B * 4, cudaMemcpyHostToDevice, s));
+        CK(cudaMemcpyAsync(h->attn_tiles, h->h_tiles.data(), h->h_tiles.size() * sizeof(int4),
+                           cudaMemcpyHostToDevice, s));
+    }
     CK(cudaMemcpyAsync(h->st, &st, sizeof(SeqState), cudaMemcpyHostToDevice, s));
 
     if (h->dumps) {
@@ -575,6 +610,11 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
         r.nq = hp.n_heads;
         r.nkv = hp.n_kv_heads;
         r.d = hp.head_dim;
+        if (h->tc_attn && l + 1 < hp.n_layers) {
+            r.vt = h->vt;
+            r.row_vtcol = h->row_vtcol;
+            r.vt_ld = h->vt_ld;
+        }
         launch_qk_rope_kv(h->kv_f16, r, s);
         h->enq += 2;
         if (l + 1 < hp.n_layers) {
@@ -591,7 +631,27 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
             a.nq = hp.n_heads;
             a.nkv = hp.n_kv_heads;
             a.d = hp.head_dim;
-            launch_attn_prefill_simt(h->kv_f16, h->w_bf16, a, s);
+            if (h->tc_attn) {
+                AttnPrefillTcArgs t{};
+                t.q = h->q16;
+                t.Kc = L.K;
+                t.vt = h->vt;
+                t.tiles = h->attn_tiles;
+                t.kv_off = h->item_kv_off;
+                t.vt_col = h->item_vt_col;
+                t.o = static_cast<__nv_bfloat16 *>(h->attn_o);
+                t.o_lo = static_cast<__nv_bfloat16 *>(h->attn_o_lo);
+                t.err = dev_error(h);
+                t.q_rows = total;
+                t.nq = hp.n_heads;
+                t.nkv = hp.n_kv_heads;
+                t.slots = (int)h->slots;
+                t.vt_ld = h->vt_ld;
+                t.scale = (float)(1.0 / std::sqrt((double)hp.head_dim));
+                launch_attn_prefill_tc(t, (int)h->h_tiles.size(), s);
+            } else {
+                launch_attn_prefill_simt(h->kv_f16, h->w_bf16, a, s);
+            }
             gemm(h, h->attn_o, h->attn_o_lo, L.wo, h->x, H, total, H, nqd, EPI_RESID_F32);
             launch_rmsnorm_rows(h->x, L.ffn_norm, hp.rms_eps, h->xn, h->xn_lo, h->w_bf16, total, H, s);
             gemm_swiglu(h, h->xn, h->xn_lo, L.wgu, total, F, H);
@@ -793,6 +853,7 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
 
     init_gemv_kernels();
     init_gemm_tc();
+    init_attn_prefill_tc();
     cudaStream_t s = h->stream;
     const size_t ws = wsize(*hp), H = hp->hidden, F = hp->ffn, d = hp->head_dim;
     const size_t nq = hp->n_heads, nkv = hp->n_kv_heads;
@@ -863,6 +924,13 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
         cudaGetLastError();
     }
     CKC(cudaMemsetAsync(h->attn_counter, 0, (size_t)hp->max_batch * nkv * sizeof(unsigned), s));
+    {
+        // tensor-core prompt attention: V^T columns past a sequence's keys meet
+        // zero probabilities and must hold finite values, so the scratch starts at 0
+        const char *pa = std::getenv("SPEECH_DECODER_PREFILL_ATTN");
+        h->tc_attn = h->use_tc && h->vt && attn_prefill_tc_ok((int)d, h->kv_f16) && !(pa && !std::strcmp(pa, "simt"));
+        if (h->vt) CKC(cudaMemsetAsync(h->vt, 0, (size_t)nkv * d * h->vt_ld * 2, s));
+    }
     CKC(cudaMemsetAsync(h->am_counter, 0, 64 * sizeof(unsigned), s));
     std::memset(&h->hst, 0, sizeof(SeqState));
     h->hst.eos_id = hp->eos_id;

@@ -32,6 +32,7 @@
 
 #include "gemm_tc.cuh"
 #include "ptx.cuh"
+#include "tc.cuh"
 
 namespace dec {
 
@@ -53,55 +54,6 @@ struct TcArgs {
     int *err;
     uint32_t idesc, tmem_cols;
 };
-
-// ------------------------------------------------------------------ PTX helpers
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);     // start address
-    d |= (uint64_t)1 << 16;                        // leading byte offset (unused for swizzled K-major)
-    d |= (uint64_t)(1024 >> 4) << 32;              // stride byte offset: 8 rows x 128 B
-    d |= (uint64_t)1 << 46;                        // descriptor version for sm_100 family
-    d |= (uint64_t)2 << 61;                        // 128-byte swizzle
-    return d;
-}
-
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            ptx::smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(ptx::smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, int accum) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                     ptx::smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
 
 __device__ __forceinline__ void tc_report(int *err, int code) {
     if (err) atomicCAS(err, 0, code);
@@ -199,7 +151,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 for (int pl = 0; pl < a.planes; ++pl) {
                     const uint64_t bdesc = sw128_desc(bbase + pl * b_bytes + kk * 32);
                     for (int g = 0; g < a.groups; ++g)
-                        mma_bf16(tmem + (uint32_t)(g * a.BN), sw128_desc(abase + g * 16384 + kk * 32), bdesc, a.idesc,
+                        mma_f16(tmem + (uint32_t)(g * a.BN), sw128_desc(abase + g * 16384 + kk * 32), bdesc, a.idesc,
                                  (i | kk | pl) != 0);
                 }
             }

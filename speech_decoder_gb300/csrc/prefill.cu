@@ -160,10 +160,13 @@ __global__ void __launch_bounds__(256) k_qk_rope_kv(RopeKvArgs a) {
         norm_rope_lane<PL>(v, a.kn_w, a.eps, D, rope_row, lane);
         TKV *K = reinterpret_cast<TKV *>(a.Kc) + slot;
         TKV *V = reinterpret_cast<TKV *>(a.Vc) + slot;
+        TKV *vt = a.vt ? reinterpret_cast<TKV *>(a.vt) + (size_t)(g * D + lane * PL) * a.vt_ld + a.row_vtcol[t] : nullptr;
 #pragma unroll
         for (int e = 0; e < PL; ++e) {
             K[e] = from_f32<TKV>(v[e]);
-            V[e] = from_f32<TKV>(row[(size_t)(a.nq + a.nkv + g) * D + lane * PL + e]);
+            const TKV x = from_f32<TKV>(row[(size_t)(a.nq + a.nkv + g) * D + lane * PL + e]);
+            V[e] = x;
+            if (vt) vt[(size_t)e * a.vt_ld] = x;
         }
     }
 }

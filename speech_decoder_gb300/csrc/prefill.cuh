@@ -27,8 +27,32 @@ struct RopeKvArgs {
     void *q_out;               // [T, nq, d] (f16 or f32, same type as the cache)
     void *Kc, *Vc;             // this layer's pool [nkv][slots][d]
     int slots, T, nq, nkv, d;
+    // optional (fp16 KV): V transposed, vt[(g d + e) vt_ld + row_vtcol[t]], for
+    // the tensor-core attention
+    void *vt;
+    const int32_t *row_vtcol;
+    int vt_ld;
 };
 void launch_qk_rope_kv(bool kv_f16, const RopeKvArgs &a, cudaStream_t s);
+
+// Tensor-core causal attention of the prompt rows (fp16 KV, head_dim 128).
+// tiles[i] = (first global row, first position in its sequence, rows <= 128,
+// item); keys of item b sit at pool slots kv_off[b] + position and at V^T
+// columns vt_col[b] + position (vt_col a multiple of 128).
+struct AttnPrefillTcArgs {
+    const void *q;             // [q_rows][nq][d] fp16 (normed, roped)
+    const void *Kc;            // pool [nkv][slots][d] fp16
+    const void *vt;            // [nkv d][vt_ld] fp16
+    const int4 *tiles;
+    const int32_t *kv_off, *vt_col;
+    __nv_bfloat16 *o, *o_lo;   // [rows][nq d] two bf16 planes (o_lo may be null)
+    int *err;                  // device error code if a bounded wait expires
+    int q_rows, nq, nkv, slots, vt_ld;
+    float scale;
+};
+void init_attn_prefill_tc();
+bool attn_prefill_tc_ok(int d, bool kv_f16);
+cudaError_t launch_attn_prefill_tc(const AttnPrefillTcArgs &a, int n_tiles, cudaStream_t s);
 
 struct AttnPrefillArgs {
     const void *q;             // [T, nq, d] roped queries (cache type)
