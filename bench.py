@@ -253,8 +253,8 @@ def run_ours(args):
     if B == 1:
         dec.prefill_ids(ids_dev, audio_dev, int(pre_lens[0]))
         impl = os.environ.get("SPEECH_DECODER_GEMV", "stream")
-        kname = ("k_gemv_stream<1, IN_NORM, OUT_STORE>" if impl == "stream" else
-                 "k_gemv_ldg<bf16, IN_NORM, OUT_STORE>") + " (q|k|v and gate|up GEMV, one launch per layer)"
+        kname = ("k_gemv_stream" if impl == "stream" else "k_gemv_ldg") + \
+            " (the step's q|k|v, o, gate|up+SwiGLU and down GEMVs, every layer in order)"
     else:
         dec.prefill_ids_batch_ptr(ids_dev.data_ptr(), cu_ids, audio_dev.data_ptr(), cu_au, pre_lens, 1)
         kname = "k_gemm_tc + k_splitk_reduce (q|k|v and gate|up projections of %d rows, per projection)" % B

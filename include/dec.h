@@ -208,8 +208,9 @@ dec_status dec_last_timings(const dec_handle *h, float *prefill_ms, float *gener
 /* Time one family of decode kernels in isolation on the handle's stream
  * (CUDA events around `iters` rounds; each round launches the kernel once
  * per layer, so consecutive launches stream different weights and no
- * launch is served from L2).  op 0: the RMSNorm + projection GEMV (q|k|v
- * and gate|up of every layer); op 1: the lm_head + argmax GEMV; op 2: the
+ * launch is served from L2).  op 0: the step's projection GEMVs of every
+ * layer in step order (q|k|v, o, gate|up with SwiGLU, down), without the
+ * attention between them; op 1: the lm_head + argmax GEMV; op 2: the
  * split-KV attention at the current lengths; op 3: one whole decode step
  * (the persistent step kernel when it is in use; *avg_ms is then per step
  * and *bytes_per_launch the step's algorithmic bytes).  Needs a prior prefill (it

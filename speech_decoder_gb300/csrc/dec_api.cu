@@ -331,16 +331,13 @@ static void set_prefetch(const dec_handle *h, GemvArgs &g, const void *W, int N,
 }
 
 // One decoder block for the step rows in xd (one row per sequence).
-static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
-    if (batched_path(h, B)) {
-        enqueue_decode_layer_tc(h, l, B, from_embed);
-        return;
-    }
+// The decode step's launches of one block (one row per sequence).  Each
+// projection helper returns the launch's algorithmic bytes (weights once, the
+// activation rows in and out) for the profiler.
+static double layer_qkv(dec_handle *h, int l, int B, bool from_embed) {
     const dec_hparams &hp = h->hp;
     const DevLayer &L = h->L[l];
-    const int H = hp.hidden, F = hp.ffn, nqd = hp.n_heads * hp.head_dim;
-    cudaStream_t s = h->stream;
-
+    const int H = hp.hidden, nqd = hp.n_heads * hp.head_dim;
     GemvArgs g{};
     g.st = h->st;
     g.B = B;
@@ -362,8 +359,15 @@ static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
         g.kvp_row_bytes = (int)(hp.head_dim * kvsize(hp));
     }
     const bool emb = from_embed && l == 0;
-    launch_gemv(emb ? IN_EMBED_NORM : IN_NORM, OUT_STORE, h->w_bf16, g, gemv_grid(g.N, h->num_sms, h->gemv_ctas), s);
+    launch_gemv(emb ? IN_EMBED_NORM : IN_NORM, OUT_STORE, h->w_bf16, g, gemv_grid(g.N, h->num_sms, h->gemv_ctas),
+                h->stream);
+    h->enq++;
+    return (double)g.N * H * wsize(hp) + (double)B * (H + g.N) * 4.0;
+}
 
+static void layer_attn(dec_handle *h, int l, int B) {
+    const dec_hparams &hp = h->hp;
+    const DevLayer &L = h->L[l];
     AttnDecArgs a{};
     a.qkv = h->qkvd;
     a.qn_w = L.qn;
@@ -382,8 +386,14 @@ static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
     a.d = hp.head_dim;
     a.B = B;
     a.append = 1;
-    launch_attn_decode(h->kv_f16, a, splits_for(h, B), s);
+    launch_attn_decode(h->kv_f16, a, splits_for(h, B), h->stream);
+    h->enq++;
+}
 
+static double layer_o(dec_handle *h, int l, int B) {
+    const dec_hparams &hp = h->hp;
+    const DevLayer &L = h->L[l];
+    const int H = hp.hidden, F = hp.ffn, nqd = hp.n_heads * hp.head_dim;
     GemvArgs o{};
     o.st = h->st;
     o.B = B;
@@ -394,22 +404,47 @@ static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
     o.in = h->od;
     o.out = h->xd;
     set_prefetch(h, o, L.wgu, 2 * F, H);
-    launch_gemv(IN_PLAIN, OUT_RESID, h->w_bf16, o, gemv_grid(H, h->num_sms, h->gemv_ctas), s);
+    launch_gemv(IN_PLAIN, OUT_RESID, h->w_bf16, o, gemv_grid(H, h->num_sms, h->gemv_ctas), h->stream);
+    h->enq++;
+    return (double)H * nqd * wsize(hp) + (double)B * (nqd + 2 * H) * 4.0;
+}
 
-    // gate|up: with the producer-warp GEMV each gate row meets its up row in one
-    // stage and the kernel writes silu(gate) * up; otherwise gate|up is stored
-    // and the down projection's prologue applies SwiGLU
-    const int grid_f = gemv_grid(2 * F, h->num_sms, h->gemv_ctas);
-    const bool fused = h->w_bf16 && gemv_impl() == 4 && gemv_stream_swiglu_ok(H, std::min(B, kGroupB), F, grid_f);
-    GemvArgs f1 = g;
-    f1.kvp_K = f1.kvp_V = nullptr;
+// gate|up: with the producer-warp GEMV each gate row meets its up row in one
+// stage and the kernel writes silu(gate) * up; otherwise gate|up is stored and
+// the down projection's prologue applies SwiGLU
+static bool swiglu_fused(const dec_handle *h, int B) {
+    const int H = h->hp.hidden, F = h->hp.ffn;
+    return h->w_bf16 && gemv_impl() == 4 &&
+           gemv_stream_swiglu_ok(H, std::min(B, kGroupB), F, gemv_grid(2 * F, h->num_sms, h->gemv_ctas));
+}
+
+static double layer_gu(dec_handle *h, int l, int B) {
+    const dec_hparams &hp = h->hp;
+    const DevLayer &L = h->L[l];
+    const int H = hp.hidden, F = hp.ffn;
+    const bool fused = swiglu_fused(h, B);
+    GemvArgs f1{};
+    f1.st = h->st;
+    f1.B = B;
+    f1.eps = hp.rms_eps;
+    f1.K = H;
+    f1.in = h->xd;
     f1.W = L.wgu;
     f1.N = fused ? F : 2 * F;
     f1.norm_w = L.ffn_norm;
     f1.out = h->gud;
     set_prefetch(h, f1, L.wd, H, F);
-    launch_gemv(IN_NORM, fused ? OUT_SWIGLU : OUT_STORE, h->w_bf16, f1, grid_f, s);
+    launch_gemv(IN_NORM, fused ? OUT_SWIGLU : OUT_STORE, h->w_bf16, f1, gemv_grid(2 * F, h->num_sms, h->gemv_ctas),
+                h->stream);
+    h->enq++;
+    return (double)2 * F * H * wsize(hp) + (double)B * (H + f1.N) * 4.0;
+}
 
+static double layer_down(dec_handle *h, int l, int B) {
+    const dec_hparams &hp = h->hp;
+    const DevLayer &L = h->L[l];
+    const int H = hp.hidden, F = hp.ffn;
+    const bool fused = swiglu_fused(h, B);
     GemvArgs f2{};
     f2.st = h->st;
     f2.B = B;
@@ -421,8 +456,22 @@ static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
     f2.out = h->xd;
     if (l + 1 < hp.n_layers) set_prefetch(h, f2, h->L[l + 1].wqkv, qkv_rows(hp), H);
     else set_prefetch(h, f2, h->embed, hp.vocab, H);
-    launch_gemv(fused ? IN_PLAIN : IN_SWIGLU, OUT_RESID, h->w_bf16, f2, gemv_grid(H, h->num_sms, h->gemv_ctas), s);
-    h->enq += 5;
+    launch_gemv(fused ? IN_PLAIN : IN_SWIGLU, OUT_RESID, h->w_bf16, f2, gemv_grid(H, h->num_sms, h->gemv_ctas),
+                h->stream);
+    h->enq++;
+    return (double)H * F * wsize(hp) + (double)B * ((fused ? 1 : 2) * F + 2 * H) * 4.0;
+}
+
+static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
+    if (batched_path(h, B)) {
+        enqueue_decode_layer_tc(h, l, B, from_embed);
+        return;
+    }
+    layer_qkv(h, l, B, from_embed);
+    layer_attn(h, l, B);
+    layer_o(h, l, B);
+    layer_gu(h, l, B);
+    layer_down(h, l, B);
 }
 
 static void enqueue_head(dec_handle *h, int B) {
@@ -1226,25 +1275,12 @@ dec_status dec_profile_kernel(dec_handle *h, int32_t op, int32_t iters, float *a
                 bytes += (double)2 * F * H * ws + (double)B * H * 4.0 + (double)B * F * 4.0;
                 launches += 2;
             } else if (op == 0) {
-                GemvArgs g{};
-                g.st = h->st;
-                g.B = B;
-                g.eps = hp.rms_eps;
-                g.K = H;
-                g.in = h->xd;
-                g.W = L.wqkv;
-                g.N = qkv_rows(hp);
-                g.norm_w = L.attn_norm;
-                g.out = h->qkvd;
-                launch_gemv(IN_NORM, OUT_STORE, h->w_bf16, g, gemv_grid(g.N, h->num_sms, h->gemv_ctas), s);
-                bytes += (double)g.N * H * ws + (double)B * (H + g.N) * 4.0;
-                g.W = L.wgu;
-                g.N = 2 * F;
-                g.norm_w = L.ffn_norm;
-                g.out = h->gud;
-                launch_gemv(IN_NORM, OUT_STORE, h->w_bf16, g, gemv_grid(g.N, h->num_sms, h->gemv_ctas), s);
-                bytes += (double)g.N * H * ws + (double)B * (H + g.N) * 4.0;
-                launches += 2;
+                // the step's four projection GEMVs of the layer, as the step launches them
+                bytes += layer_qkv(h, l, B, false);
+                bytes += layer_o(h, l, B);
+                bytes += layer_gu(h, l, B);
+                bytes += layer_down(h, l, B);
+                launches += 4;
             } else {
                 AttnDecArgs a{};
                 a.qkv = h->qkvd;
