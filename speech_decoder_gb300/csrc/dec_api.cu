@@ -175,7 +175,7 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     h->gemv_ctas = gemv_ctas_per_sm();
     {
         const char *c = std::getenv("SPEECH_DECODER_GEMV_PF_KB");
-        h->pf_bytes = (c ? std::max(0, std::min(4096, std::atoi(c))) : 128) * 1024;
+        h->pf_bytes = (c ? std::max(0, std::min(4096, std::atoi(c))) : 64) * 1024;
     }
     const size_t ws = wsize(hp), kvs = kvsize(hp), as = ws;   // activations use the weight format
     const size_t H = hp.hidden, d = hp.head_dim, nq = hp.n_heads, nkv = hp.n_kv_heads, F = hp.ffn;

@@ -119,7 +119,7 @@ void init_gemv_stream_kernels();
 int gemv_default_ctas_per_sm();
 
 // activation rows x K floats of one GEMV CTA must fit: kGroupB * K * 4 <= kGemvMaxSmem
-constexpr int kGemvMaxSmem = 200 * 1024;
+constexpr int kGemvMaxSmem = 216 * 1024;
 // split-KV partitions per (sequence, kv head)
 constexpr int kAttnMaxSplits = 32;
 // keys per split at least (short sequences run few splits)

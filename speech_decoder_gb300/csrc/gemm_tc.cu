@@ -117,10 +117,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Programmatic dependent launch: the weight tiles (A) do not depend on the
+    // preceding kernel, so the first stages' A loads are issued before the
+    // dependency wait; activations (B) and every global write come after it.
+    ptx::pdl_launch();
     int issued = 0;    // producer: stages issued (for the drain on abort)
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------------- TMA producer
-        for (int i = 0; i < nk; ++i) {
+        const int pre = min(S, nk);
+        for (int i = 0; i < pre; ++i) {
+            ptx::mbar_expect_tx(&full[i], stage_bytes);
+            tma_load_2d(smem + (size_t)i * stage_bytes, &tmA, (kt0 + i) * kBK, m0, &full[i]);
+        }
+        ptx::pdl_wait();
+        for (int i = 0; i < pre; ++i) {
+            unsigned char *st = smem + (size_t)i * stage_bytes;
+            tma_load_2d(st + a_bytes, &tmB, (kt0 + i) * kBK, n0, &full[i]);
+            if (a.planes == 2) tma_load_2d(st + a_bytes + b_bytes, &tmB2, (kt0 + i) * kBK, n0, &full[i]);
+        }
+        issued = pre;
+        for (int i = pre; i < nk; ++i) {
             const int s = i % S;
             if (i >= S && !ptx::mbar_wait_bounded(&empty[s], ((i / S) - 1) & 1, kTcPolls)) {
                 tc_report(a.err, 4);
@@ -160,6 +176,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         mma_commit(done);                               // accumulator final
     } else if (warp >= 2) {
         // ---------------------------------------------------------- epilogue
+        ptx::pdl_wait();
         const bool ok = ptx::mbar_wait_bounded(done, 0, kTcPolls);
         if (!ok) tc_report(a.err, 6);
         tc_fence_after();
@@ -203,6 +220,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // thread per (tile, token column, 4 consecutive features): reads are
 // 512-byte coalesced per column and every load of a thread is independent.
 __global__ void __launch_bounds__(256) k_splitk_reduce(TcArgs a, int mt) {
+    ptx::pdl_launch();
+    ptx::pdl_wait();
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const int per_tile = a.BN * 32;
     const int tile = (int)(idx / per_tile), rem = (int)(idx % per_tile);
@@ -288,8 +307,10 @@ TcPlan gemm_tc_plan(int T, int n_feat, int K, int groups, int num_sms, size_t sc
     p.nt = (T + BN - 1) / BN;
     p.k_tiles = K / kBK;
     const int tiles = p.mt * p.nt;
+    // split K so that every SM has a CTA, in ONE wave (a second, partial wave
+    // of split CTAs would leave most SMs idle for a whole CTA's time)
     int splits = 1;
-    if (tiles < num_sms) splits = std::max(1, std::min(p.k_tiles / 2, (num_sms + tiles - 1) / tiles));
+    if (tiles < num_sms) splits = std::max(1, std::min(p.k_tiles / 2, num_sms / tiles));
     if (force_splits > 0) splits = std::min(force_splits, p.k_tiles);
     // the scratch for partial tiles bounds the split count
     while (splits > 1 && (size_t)tiles * splits * groups * BN * 128 > scratch_floats) --splits;
@@ -335,13 +356,25 @@ cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W
     // instruction descriptor: f32 accumulate, bf16 A and B, both K-major, N = BN, M = 128
     a.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(p.BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
     a.tmem_cols = (uint32_t)p.tmem_cols;
-    dim3 grid(p.mt, p.nt, p.splits);
-    k_gemm_tc<<<grid, kTcThreads, p.smem, s>>>(mA, mB, mB2, a);
-    if (p.splits > 1) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(p.mt, p.nt, p.splits);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc, mA, mB, mB2, a);
+    if (e == cudaSuccess && p.splits > 1) {
         const long long threads = (long long)p.mt * p.nt * p.BN * 32;
-        k_splitk_reduce<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(a, p.mt);
+        cfg.gridDim = dim3((unsigned)((threads + 255) / 256));
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = 0;
+        e = cudaLaunchKernelEx(&cfg, k_splitk_reduce, a, p.mt);
     }
-    return cudaPeekAtLastError();
+    return e != cudaSuccess ? e : cudaPeekAtLastError();
 }
 
 }  // namespace dec

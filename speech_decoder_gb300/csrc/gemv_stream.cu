@@ -31,7 +31,7 @@ constexpr int kCT = kCW * 32;                 // consumer threads
 constexpr int kTT = kCT + 32;                 // + the producer warp
 constexpr int kStage = 16 * 1024;             // bytes per ring stage (whole rows)
 constexpr int kMaxStages = 12;
-constexpr int kAutoStages = 10;               // 160 KB in flight per SM covers the loaded HBM latency
+constexpr int kAutoStages = 12;               // 192 KB in flight per SM covers the loaded HBM latency
 constexpr uint64_t kWaitNs = 200000000ull;    // every wait gives up after 0.2 s
 constexpr int kBarCons = 1;                   // named barrier of the consumer warps
 
