@@ -34,6 +34,7 @@ constexpr int kThreads = 192;
 constexpr uint32_t kAtom = 128 * 128;    // one 64-wide swizzle atom of a 128-row fp16 tile (bytes)
 constexpr uint32_t kTile = 2 * kAtom;    // a 128 x 128 fp16 tile
 constexpr uint64_t kWaitNs = 200000000ull;
+constexpr uint32_t kTmemCols = 512;      // S of even key tiles, O, S of odd key tiles (one CTA per SM)
 
 struct Smem {                            // offsets into the 1024-aligned dynamic shared memory
     static constexpr uint32_t q = 0;
@@ -44,7 +45,7 @@ struct Smem {                            // offsets into the 1024-aligned dynami
 };
 
 struct Sync {
-    uint64_t q_full, kv_full[2], kv_empty[2], s_full, p_ready, pv_done;
+    uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], p_ready, pv_done;
     uint32_t tmem;
     int abort;
 };
@@ -79,17 +80,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&sy.kv_full[s], 1);
             ptx::mbar_init(&sy.kv_empty[s], 1);
         }
-        ptx::mbar_init(&sy.s_full, 1);
+        ptx::mbar_init(&sy.s_full[0], 1);
+        ptx::mbar_init(&sy.s_full[1], 1);
         ptx::mbar_init(&sy.p_ready, 128);
         ptx::mbar_init(&sy.pv_done, 1);
         sy.abort = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(&sy.tmem, 256);
+    if (warp == 1) tmem_alloc(&sy.tmem, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tS = sy.tmem, tO = sy.tmem + 128;
+    // TMEM columns: S of even key tiles [0, 128), O [128, 256), S of odd tiles [256, 384)
+    const uint32_t tO = sy.tmem + 128;
+    auto tS = [&](int j) { return sy.tmem + ((j & 1) ? 256u : 0u); };
     const uint32_t sbase = ptx::smem_u32(sm);
 
     int issued = 0;                              // producer: key tiles issued (drained on abort)
@@ -111,19 +115,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1 && lane == 0) {
         // ---------------------------------------------------------- MMA issuer
+        // S of tile j + 1 is issued before P of tile j is awaited, so the tensor
+        // core computes the next scores while the softmax warps work on these
         const uint32_t idesc = mma_idesc_f16(false, kBQ, kBK);     // both MMAs are 128 x 128 (x 16)
-        if (wait_bar(sy, &sy.q_full, 0, a.err, 22)) {
+        auto issue_s = [&](int j) -> bool {
+            const int s = j & 1;
+            if (!wait_bar(sy, &sy.kv_full[s], (j >> 1) & 1, a.err, 23)) return false;
+            tc_fence_after();
+            const uint32_t qb = sbase + Smem::q, kb = sbase + Smem::k + s * kTile;
+#pragma unroll
+            for (int k = 0; k < kD / 16; ++k) {
+                const uint32_t off = (k >> 2) * kAtom + (k & 3) * 32;
+                mma_f16(tS(j), sw128_desc(qb + off), sw128_desc(kb + off), idesc, k > 0);
+            }
+            mma_commit(&sy.s_full[s]);
+            return true;
+        };
+        if (wait_bar(sy, &sy.q_full, 0, a.err, 22) && issue_s(0)) {
             for (int j = 0; j < n_kt; ++j) {
                 const int s = j & 1;
-                if (!wait_bar(sy, &sy.kv_full[s], (j >> 1) & 1, a.err, 23)) break;
-                tc_fence_after();
-                const uint32_t qb = sbase + Smem::q, kb = sbase + Smem::k + s * kTile;
-#pragma unroll
-                for (int k = 0; k < kD / 16; ++k) {
-                    const uint32_t off = (k >> 2) * kAtom + (k & 3) * 32;
-                    mma_f16(tS, sw128_desc(qb + off), sw128_desc(kb + off), idesc, k > 0);
-                }
-                mma_commit(&sy.s_full);
+                if (j + 1 < n_kt && !issue_s(j + 1)) break;
                 if (!wait_bar(sy, &sy.p_ready, j & 1, a.err, 24)) break;
                 tc_fence_after();
                 const uint32_t pb = sbase + Smem::p, vb = sbase + Smem::vt + s * kTile;
@@ -149,17 +160,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kt && ok; ++j) {
-            ok = __all_sync(0xffffffffu, wait_bar(sy, &sy.s_full, j & 1, a.err, 25));
+            ok = __all_sync(0xffffffffu, wait_bar(sy, &sy.s_full[j & 1], (j >> 1) & 1, a.err, 25));
             if (!ok) break;
             tc_fence_after();
             float sv[kBK];
-#pragma unroll
-            for (int c = 0; c < kBK; c += 16) {
-                float t[16];
-                tmem_ld16(tS + lane_off + c, t);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) sv[c + i] = t[i];
-            }
+            tmem_ld128(tS(j) + lane_off, sv);
             float mx = -INFINITY;
 #pragma unroll
             for (int c = 0; c < kBK; ++c) {
@@ -170,6 +175,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float m_new = fmaxf(m, mx);
             const float corr = m_new == -INFINITY ? 1.f : exp2f(m - m_new);
             float ls = 0.f;
+#pragma unroll
+            for (int c = 0; c < kBK; ++c) {
+                sv[c] = m_new == -INFINITY ? 0.f : exp2f(sv[c] - m_new);
+                ls += sv[c];
+            }
+            l = l * corr + ls;
+            m = m_new;
             // the previous P . V has finished reading P and writing O
             if (j > 0) {
                 ok = __all_sync(0xffffffffu, wait_bar(sy, &sy.pv_done, (j - 1) & 1, a.err, 26));
@@ -182,27 +194,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t w[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float p0 = m_new == -INFINITY ? 0.f : exp2f(sv[8 * c8 + 2 * i] - m_new);
-                    const float p1 = m_new == -INFINITY ? 0.f : exp2f(sv[8 * c8 + 2 * i + 1] - m_new);
-                    ls += p0 + p1;
-                    const __half2 hp = __floats2half2_rn(p0, p1);
+                    const __half2 hp = __floats2half2_rn(sv[8 * c8 + 2 * i], sv[8 * c8 + 2 * i + 1]);
                     w[i] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
                 const int at = c8 >> 3, ch = c8 & 7;
                 *reinterpret_cast<uint4 *>(prow + at * kAtom + sw128_offset(r, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            l = l * corr + ls;
-            m = m_new;
             if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {   // rescale the running output (whole warp)
+                float t[kD];
+                tmem_ld128(tO + lane_off, t);
 #pragma unroll
-                for (int c = 0; c < kD; c += 16) {
-                    float t[16];
-                    tmem_ld16(tO + lane_off + c, t);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) t[i] *= corr;
-                    tmem_st16(tO + lane_off + c, t);
-                }
-                tmem_st_wait();
+                for (int i = 0; i < kD; ++i) t[i] *= corr;
+                tmem_st128(tO + lane_off, t);
             }
             fence_async_smem();
             tc_fence_before();
@@ -214,10 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv = row_ok ? 1.f / l : 0.f;
             const size_t base = (size_t)(row0 + r) * a.nq * kD + (size_t)h * kD;
             __nv_bfloat16 *hi = a.o + base, *lo = a.o_lo ? a.o_lo + base : nullptr;
+            float o[kD];
+            tmem_ld128(tO + lane_off, o);
 #pragma unroll
             for (int c = 0; c < kD; c += 16) {
-                float t[16];
-                tmem_ld16(tO + lane_off + c, t);
+                const float *t = o + c;
                 uint32_t wh[8], wl[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -248,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(sy.tmem, 256);
+    if (warp == 1) tmem_dealloc(sy.tmem, kTmemCols);
 }
 
 // ------------------------------------------------------------------ host side

@@ -185,8 +185,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int f = (a.epi == EPI_SWIGLU_BF16 ? blockIdx.x * 128 : m0) + r;
         const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
         const int ncols = a.groups * a.BN;
+        // TMEM is read 32 columns per load where the tile allows (one wait per
+        // load), 16 for a remainder
         if (a.splits == 1) {
-            for (int c = 0; c < a.BN; c += 16) {
+            int c = 0;
+            for (; c + 32 <= a.BN; c += 32) {
+                float v[32], u[32];
+                tmem_ld32(tq + c, v);
+                if (a.groups == 2) tmem_ld32(tq + a.BN + c, u);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) epi_store(a, f, n0 + c + j, v[j], a.groups == 2 ? u[j] : 0.f);
+            }
+            for (; c < a.BN; c += 16) {
                 float v[16], u[16];
                 tmem_ld16(tq + c, v);
                 if (a.groups == 2) tmem_ld16(tq + a.BN + c, u);
@@ -197,7 +207,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // split-K: park the partial tile; k_splitk_reduce sums the splits
             const int tile = blockIdx.y * gridDim.x + blockIdx.x;
             float *mine = a.part + ((size_t)tile * a.splits + blockIdx.z) * ncols * 128;
-            for (int c = 0; c < ncols; c += 16) {
+            int c = 0;
+            for (; c + 32 <= ncols; c += 32) {
+                float v[32];
+                tmem_ld32(tq + c, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) mine[(size_t)(c + j) * 128 + r] = v[j];
+            }
+            for (; c < ncols; c += 16) {
                 float v[16];
                 tmem_ld16(tq + c, v);
 #pragma unroll
