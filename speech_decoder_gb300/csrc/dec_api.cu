@@ -252,8 +252,10 @@ static int *dev_error(dec_handle *h) { return &h->st->error; }
 // A_lo: the second bf16 plane of A (bf16 builds), read by the tensor-core path.
 static void gemm(dec_handle *h, const void *A, const void *A_lo, const void *W, float *C, int ldc, int M, int N, int K,
                  int epi) {
-    if (h->use_tc && h->w_bf16 && gemm_tc_plan(M, N, K, 1, h->num_sms, kTcScratchFloats, 0, A_lo ? 2 : 1).ok)
-        launch_gemm_tc(A, A_lo, M, W, N, K, 1, epi, C, ldc, nullptr, nullptr, 0, h->tc_scratch, kTcScratchFloats,
+    // long prompts: 256 weight rows per CTA share each activation tile
+    const int groups = M > 256 && N % 256 == 0 ? 2 : 1;
+    if (h->use_tc && h->w_bf16 && gemm_tc_plan(M, N, K, groups, h->num_sms, kTcScratchFloats, 0, A_lo ? 2 : 1).ok)
+        launch_gemm_tc(A, A_lo, M, W, N, K, groups, epi, C, ldc, nullptr, nullptr, 0, h->tc_scratch, kTcScratchFloats,
                        dev_error(h), h->num_sms, h->stream);   // a launch error surfaces at the end of the pass
     else
         launch_gemm_simt(A, h->w_bf16, W, h->w_bf16, C, ldc, M, N, K, epi, h->stream);

@@ -189,19 +189,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // load), 16 for a remainder
         if (a.splits == 1) {
             int c = 0;
+            // two groups outside SwiGLU: rows m0 + 128 + r in the second TMEM range
+            const bool pair = a.groups == 2 && a.epi != EPI_SWIGLU_BF16;
             for (; c + 32 <= a.BN; c += 32) {
                 float v[32], u[32];
                 tmem_ld32(tq + c, v);
                 if (a.groups == 2) tmem_ld32(tq + a.BN + c, u);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) epi_store(a, f, n0 + c + j, v[j], a.groups == 2 ? u[j] : 0.f);
+                for (int j = 0; j < 32; ++j) {
+                    epi_store(a, f, n0 + c + j, v[j], a.groups == 2 ? u[j] : 0.f);
+                    if (pair) epi_store(a, f + 128, n0 + c + j, u[j], 0.f);
+                }
             }
             for (; c < a.BN; c += 16) {
                 float v[16], u[16];
                 tmem_ld16(tq + c, v);
                 if (a.groups == 2) tmem_ld16(tq + a.BN + c, u);
 #pragma unroll
-                for (int j = 0; j < 16; ++j) epi_store(a, f, n0 + c + j, v[j], a.groups == 2 ? u[j] : 0.f);
+                for (int j = 0; j < 16; ++j) {
+                    epi_store(a, f, n0 + c + j, v[j], a.groups == 2 ? u[j] : 0.f);
+                    if (pair) epi_store(a, f + 128, n0 + c + j, u[j], 0.f);
+                }
             }
         } else {
             // split-K: park the partial tile; k_splitk_reduce sums the splits
@@ -262,6 +270,12 @@ __global__ void __launch_bounds__(256) k_splitk_reduce(TcArgs a, int mt) {
     epi_store(a, f + 1, t, g.y, u.y);
     epi_store(a, f + 2, t, g.z, u.z);
     epi_store(a, f + 3, t, g.w, u.w);
+    if (a.groups == 2 && a.epi != EPI_SWIGLU_BF16) {       // 256-row tile: the second 128 rows
+        epi_store(a, f + 128, t, u.x, 0.f);
+        epi_store(a, f + 129, t, u.y, 0.f);
+        epi_store(a, f + 130, t, u.z, 0.f);
+        epi_store(a, f + 131, t, u.w, 0.f);
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -352,7 +366,7 @@ cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W
         !make_map(&mB2, X_lo ? X_lo : X, (uint64_t)T, (uint64_t)K, (uint32_t)p.BN))
         return cudaErrorInvalidValue;
     TcArgs a{};
-    a.n_feat = groups == 2 ? n_feat / 2 : n_feat;
+    a.n_feat = epi == EPI_SWIGLU_BF16 ? n_feat / 2 : n_feat;
     a.T = T;
     a.K = K;
     a.groups = groups;

@@ -21,7 +21,10 @@ struct TcPlan {
 // product.  epi: EPI_STORE_F32 writes C[t][f]; EPI_RESID_F32 adds into C;
 // EPI_SWIGLU_BF16 (groups = 2, W packed in blocks of 128 gate rows + 128 up
 // rows) writes Hout[t][f] = bf16(silu(gate) * up) for f < n_feat / 2 and, if
-// Hout_lo is not null, the bf16 rounding residual into Hout_lo.
+// Hout_lo is not null, the bf16 rounding residual into Hout_lo.  groups = 2
+// with the other epilogues makes each CTA own 256 weight rows (two 128-row
+// MMA tiles sharing every activation tile: half the activation traffic per
+// FLOP, for long prompts); n_feat must then be a multiple of 256.
 // scratch holds split-K partial tiles, summed by a second kernel in split
 // order; err receives a device error code if a bounded wait expires.
 TcPlan gemm_tc_plan(int T, int n_feat, int K, int groups, int num_sms, size_t scratch_floats,
