@@ -61,6 +61,19 @@ def dist_env():
     return rank, world, local
 
 
+def combine_ranks(times_ms, counts, world, device="cpu"):
+    """Whole-job numbers of independent replicas: the slowest rank's times
+    (max over ranks) and the units of all ranks (sum).  world == 1 returns the
+    inputs; otherwise every rank must call it (torch.distributed collective)."""
+    import torch
+    t = torch.tensor(list(times_ms), dtype=torch.float64, device=device)
+    c = torch.tensor(list(counts), dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.all_reduce(c, op=torch.distributed.ReduceOp.SUM)
+    return t.tolist(), c.tolist()
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -237,13 +250,8 @@ def run_ours(args):
     launches = dec.launch_count() - n0
     clk = clocks.stop() if clocks else None
     total_ms = e0.elapsed_time(e1)
-    vals = torch.tensor([total_ms, gen_ms, pre_ms], dtype=torch.float64, device=dev)
-    toks = torch.tensor([n_tok, args.steps * T_all], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(vals, op=torch.distributed.ReduceOp.MAX)
-        torch.distributed.all_reduce(toks, op=torch.distributed.ReduceOp.SUM)
-    total_ms, gen_ms, pre_ms = vals.tolist()
-    n_tok_all, n_pre_all = toks.tolist()
+    (total_ms, gen_ms, pre_ms), (n_tok_all, n_pre_all) = combine_ranks(
+        [total_ms, gen_ms, pre_ms], [n_tok, args.steps * T_all], world, dev)
     decode_tok_s = n_tok_all / (gen_ms / 1e3)
     prefill_tok_s = n_pre_all / (pre_ms / 1e3)
 

@@ -125,6 +125,22 @@ dec_status dec_reset(dec_handle *h);
 dec_status dec_prefill(dec_handle *h, const float *embeds, int32_t T, int32_t on_device,
                        int32_t *first_token);
 
+/* Chunked prefill of one sequence: embeds float32 [T, H] are the next T
+ * prompt rows, at positions [p, p + T) where p counts the rows of earlier
+ * chunks since the last reset or whole-prompt prefill; every block attends to
+ * the cached keys of the earlier chunks (causal over the whole prompt).  The
+ * sequence owns KV slots [0, max_ctx).  final_chunk != 0 also runs the head on
+ * the last row: *first_token = the prompt's greedy token and the handle is
+ * ready for dec_step / dec_generate, exactly as after dec_prefill of the whole
+ * prompt; otherwise *first_token = -1, only the KV cache advances, and steps
+ * return DEC_ERR_STATE until a final chunk.  DEC_ERR_INPUT_TOO_LONG if
+ * p + T + max_new > max_ctx or T > max_tokens (no work done; the chunked
+ * prompt is abandoned on any error).  The pages' long-prompt path feeds the
+ * prompt in chunks against the growing KV cache (MOSS: chunked prefill with
+ * chunked == single-shot logits). */
+dec_status dec_prefill_chunk(dec_handle *h, const float *embeds, int32_t T, int32_t on_device,
+                             int32_t final_chunk, int32_t *first_token);
+
 /* Prefill one sequence from token ids and encoder rows, assembling the rows
  * on the device: rows = embed[ids[0:prefix_len]] | audio | embed[ids[prefix_len:]]
  * (decoder.cpp, build_prefill_graph: get_rows + 3-way concat).

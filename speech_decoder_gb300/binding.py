@@ -22,7 +22,7 @@ DEC_ERR_OUTPUT_TRUNCATED, DEC_ERR_CUDA, DEC_ERR_STATE, DEC_ERR_DEVICE = 4, 5, 6,
 DEC_BF16, DEC_F32, DEC_F16 = 0, 1, 2
 
 EXPORTS = [
-    "dec_workspace_size", "dec_create", "dec_destroy", "dec_reset", "dec_prefill", "dec_prefill_ids",
+    "dec_workspace_size", "dec_create", "dec_destroy", "dec_reset", "dec_prefill", "dec_prefill_chunk", "dec_prefill_ids",
     "dec_prefill_batch", "dec_prefill_ids_batch", "dec_step", "dec_step_batch", "dec_generate", "dec_generate_batch",
     "dec_debug_logits", "dec_set_dumps", "dec_debug_dump", "dec_launch_count", "dec_last_timings",
     "dec_last_error", "dec_status_string", "dec_profile_kernel", "dec_attn_decode_scratch_size",
@@ -74,6 +74,7 @@ def load_library():
         "dec_destroy": ([H], None),
         "dec_reset": ([H], c_int32),
         "dec_prefill": ([H, c_void_p, c_int32, c_int32, POINTER(c_int32)], c_int32),
+        "dec_prefill_chunk": ([H, c_void_p, c_int32, c_int32, c_int32, POINTER(c_int32)], c_int32),
         "dec_prefill_ids": ([H, c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32, POINTER(c_int32)],
                             c_int32),
         "dec_prefill_batch": ([H, c_void_p, c_void_p, c_int32, c_int32, c_void_p], c_int32),
@@ -199,6 +200,14 @@ class Decoder:
         tok = c_int32()
         self._check(self.lib.dec_prefill(self.h, p, int(embeds.shape[0]), dev, byref(tok)))
         return tok.value
+
+    def prefill_chunk(self, embeds, final: bool = False):
+        """Next rows of a chunked prompt; returns the prompt's first token on
+        the final chunk, None before it."""
+        p, dev, keep = self._rows(embeds)
+        tok = c_int32()
+        self._check(self.lib.dec_prefill_chunk(self.h, p, int(embeds.shape[0]), dev, int(bool(final)), byref(tok)))
+        return tok.value if final else None
 
     def prefill_ids(self, ids, audio, prefix_len: int) -> int:
         """ids and audio both on the device (torch CUDA tensors) or both on the

@@ -87,6 +87,7 @@ struct dec_handle {
     SeqState hst{};
     int n_seq = 0;
     bool prefilled = false;
+    int chunk_pos = 0;              // chunked prefill: rows of sequence 0 already in the KV cache
     int logits_rows = 0;
     std::vector<int32_t> h_row_pos, h_row_slot, h_last_row, h_row_vtcol, h_item_kv_off, h_item_vt_col;
     std::vector<int4> h_tiles;
@@ -214,7 +215,7 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     h->row_slot = b.take<int32_t>(Tm);
     h->last_row = b.take<int32_t>(Bm);
     // items start at multiples of 128 columns of V^T
-    h->vt_ld = (int)(((Tm + 128 * Bm) + 127) / 128 * 128);
+    h->vt_ld = (int)(((std::max(Tm + 128 * Bm, (size_t)hp.max_ctx + 128)) + 127) / 128 * 128);
     h->vt = kvs == 2 && d == 128 ? b.take<char>(nkv * d * (size_t)h->vt_ld * 2) : nullptr;
     h->row_vtcol = b.take<int32_t>(Tm);
     h->item_kv_off = b.take<int32_t>(Bm);
@@ -580,7 +581,16 @@ static dec_status sync_state(dec_handle *h) {
 
 // ------------------------------------------------------------------ prefill
 // Rows are already in h->x (sum T_b rows); cu has B + 1 offsets.
-static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t *first_tokens) {
+// Chunked prefill of sequence 0: its rows start at position p0 of a context
+// that owns KV slots [0, max_ctx); a non-final chunk writes the KV of every
+// block and stops (no head).
+struct Chunk {
+    bool on = false;
+    int p0 = 0;
+    bool final = true;
+};
+
+static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t *first_tokens, Chunk ck = Chunk()) {
     const dec_hparams &hp = h->hp;
     const int total = cu[B];
     const int H = hp.hidden, F = hp.ffn, nqd = hp.n_heads * hp.head_dim;
@@ -598,20 +608,22 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
     SeqState &st = h->hst;
     std::memset(&st, 0, sizeof(st));
     int off = 0;
+    const int p0 = ck.on ? ck.p0 : 0;        // position of the first row (B == 1 when chunked)
     for (int b = 0; b < B; ++b) {
         const int T = cu[b + 1] - cu[b];
-        const int cap = T + hp.max_new;
+        const int cap = ck.on ? hp.max_ctx : T + hp.max_new;
         for (int t = 0; t < T; ++t) {
-            h->h_row_pos[cu[b] + t] = t;
-            h->h_row_slot[cu[b] + t] = off + t;
-            h->h_row_vtcol[cu[b] + t] = vt_col + t;
+            h->h_row_pos[cu[b] + t] = p0 + t;
+            h->h_row_slot[cu[b] + t] = off + p0 + t;
+            h->h_row_vtcol[cu[b] + t] = vt_col + p0 + t;
         }
         h->h_item_kv_off[b] = off;
         h->h_item_vt_col[b] = vt_col;
-        for (int q0 = 0; q0 < T; q0 += 128) h->h_tiles.push_back(make_int4(cu[b] + q0, q0, std::min(128, T - q0), b));
-        vt_col += (T + 127) / 128 * 128;
+        for (int q0 = 0; q0 < T; q0 += 128)
+            h->h_tiles.push_back(make_int4(cu[b] + q0, p0 + q0, std::min(128, T - q0), b));
+        vt_col += (p0 + T + 127) / 128 * 128;
         h->h_last_row[b] = cu[b + 1] - 1;
-        st.n_past[b] = T - 1;            // the head pass processes the last row
+        st.n_past[b] = p0 + T - 1;       // the head pass processes the last row
         st.kv_off[b] = off;
         st.kv_cap[b] = cap;
         st.active[b] = 1;
@@ -665,9 +677,16 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
             r.vt = h->vt;
             r.row_vtcol = h->row_vtcol;
             r.vt_ld = h->vt_ld;
+            // a later chunk also attends to the keys of the earlier ones: their
+            // V rows come back from the pool into the transposed scratch
+            if (p0 > 0) {
+                launch_vt_from_pool(L.V, h->vt, h->vt_ld, (int)h->slots, hp.n_kv_heads, 0, p0, 0, s);
+                h->enq++;
+            }
         }
         launch_qk_rope_kv(h->kv_f16, r, s);
         h->enq += 2;
+        if (l + 1 == hp.n_layers && ck.on && !ck.final) break;   // KV of every block written; no head
         if (l + 1 < hp.n_layers) {
             AttnPrefillArgs a{};
             a.q = h->q16;
@@ -720,6 +739,15 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
             enqueue_decode_layer(h, l, B, false);
         }
     }
+    if (ck.on && !ck.final) {
+        CK(cudaGetLastError());
+        h->launches += h->enq;
+        dec_status rc = sync_state(h);
+        if (rc != DEC_OK) return rc;
+        h->prefilled = false;
+        for (int b = 0; b < B; ++b) first_tokens[b] = -1;
+        return DEC_OK;
+    }
     if (h->dumps) {
         CK(cudaMemcpyAsync(h->dump_blast, h->xd, (size_t)B * H * 4, cudaMemcpyDeviceToDevice, s));
         launch_rmsnorm_rows(h->xd, h->final_norm, hp.rms_eps, h->dump_final, nullptr, false, B, H, s);
@@ -753,9 +781,10 @@ static dec_status check_lengths(dec_handle *h, const int32_t *cu, int B) {
     return DEC_OK;
 }
 
-static dec_status timed_prefill(dec_handle *h, const int32_t *cu, int B, int32_t *first) {
+static dec_status timed_prefill(dec_handle *h, const int32_t *cu, int B, int32_t *first, Chunk ck = Chunk()) {
+    if (!ck.on) h->chunk_pos = 0;            // a whole-prompt prefill ends any chunked one
     cudaEventRecord(h->ev[0], h->stream);
-    dec_status rc = prefill_rows(h, cu, B, first);
+    dec_status rc = prefill_rows(h, cu, B, first, ck);
     cudaEventRecord(h->ev[1], h->stream);
     cudaEventSynchronize(h->ev[1]);
     cudaEventElapsedTime(&h->prefill_ms, h->ev[0], h->ev[1]);
@@ -1005,6 +1034,7 @@ void dec_destroy(dec_handle *h) {
 dec_status dec_reset(dec_handle *h) {
     if (!h) return DEC_ERR_INVALID_ARG;
     h->prefilled = false;
+    h->chunk_pos = 0;
     h->n_seq = 0;
     h->logits_rows = 0;
     std::memset(&h->hst, 0, sizeof(SeqState));
@@ -1029,6 +1059,30 @@ dec_status dec_prefill(dec_handle *h, const float *embeds, int32_t T, int32_t on
     rc = copy_in(h, h->x, embeds, (size_t)T * h->hp.hidden * 4, on_device);
     if (rc != DEC_OK) return rc;
     return timed_prefill(h, cu, 1, first_token);
+}
+
+dec_status dec_prefill_chunk(dec_handle *h, const float *embeds, int32_t T, int32_t on_device, int32_t final_chunk,
+                             int32_t *first_token) {
+    if (!h || !embeds || !first_token || T < 1) return fail(h, DEC_ERR_INVALID_ARG, "bad prefill_chunk arguments");
+    const dec_hparams &hp = h->hp;
+    const int p0 = h->chunk_pos;
+    h->chunk_pos = 0;                        // any error abandons the chunked prompt
+    if (T > hp.max_tokens) return fail(h, DEC_ERR_INPUT_TOO_LONG, "chunk rows exceed max_tokens");
+    if ((long long)p0 + T + hp.max_new > hp.max_ctx)
+        return fail(h, DEC_ERR_INPUT_TOO_LONG,
+                    "context of " + std::to_string(p0 + T) + " rows + generation budget " + std::to_string(hp.max_new) +
+                        " exceeds the context of " + std::to_string(hp.max_ctx));
+    dec_status rc = copy_in(h, h->x, embeds, (size_t)T * hp.hidden * 4, on_device);
+    if (rc != DEC_OK) return rc;
+    const int32_t cu[2] = {0, T};
+    Chunk ck;
+    ck.on = true;
+    ck.p0 = p0;
+    ck.final = final_chunk != 0;
+    rc = timed_prefill(h, cu, 1, first_token, ck);
+    if (rc != DEC_OK) return rc;
+    h->chunk_pos = ck.final ? 0 : p0 + T;
+    return DEC_OK;
 }
 
 dec_status dec_prefill_ids(dec_handle *h, const int32_t *ids, int32_t n_ids, const float *audio, int32_t n_audio,

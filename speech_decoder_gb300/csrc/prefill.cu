@@ -184,6 +184,34 @@ void launch_qk_rope_kv(bool kv_f16, const RopeKvArgs &a, cudaStream_t s) {
     }
 }
 
+// ------------------------------------------------------------------ V^T of cached keys
+// vt[(g d + e) vt_ld + vt_col0 + j] = V[g][kv_off + j][e] for j < n_keys: tiles
+// of 32 keys x 32 dims through shared memory (reads along dims, writes along keys).
+template <int D>
+__global__ void __launch_bounds__(256) k_vt_from_pool(const __half *V, __half *vt, int vt_ld, int slots, int kv_off,
+                                                      int n_keys, int vt_col0) {
+    __shared__ __half tile[32][33];
+    const int g = blockIdx.z, j0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+    const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;        // 8 rows of 32 threads
+    for (int i = ty; i < 32; i += 8) {
+        const int j = j0 + i;
+        tile[i][tx] = j < n_keys ? V[((size_t)g * slots + kv_off + j) * D + e0 + tx] : __float2half(0.f);
+    }
+    __syncthreads();
+    for (int i = ty; i < 32; i += 8) {
+        const int j = j0 + tx;
+        if (j < n_keys) vt[(size_t)(g * D + e0 + i) * vt_ld + vt_col0 + j] = tile[tx][i];
+    }
+}
+
+void launch_vt_from_pool(const void *V, void *vt, int vt_ld, int slots, int nkv, int kv_off, int n_keys, int vt_col0,
+                         cudaStream_t s) {
+    if (n_keys <= 0) return;
+    dim3 grid((n_keys + 31) / 32, 128 / 32, nkv);
+    k_vt_from_pool<128><<<grid, 256, 0, s>>>(static_cast<const __half *>(V), static_cast<__half *>(vt), vt_ld, slots,
+                                             kv_off, n_keys, vt_col0);
+}
+
 // ------------------------------------------------------------------ causal attention (CUDA cores)
 // One warp per (query row, head); warps of a CTA share the head so that the
 // keys they stream are reused from L1.  Online softmax in fp32.

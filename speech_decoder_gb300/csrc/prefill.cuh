@@ -51,6 +51,10 @@ struct AttnPrefillTcArgs {
     float scale;
 };
 void init_attn_prefill_tc();
+// fp16 V of keys [0, n_keys) of one sequence (pool slots kv_off + j, head_dim
+// 128) into the transposed scratch at columns vt_col0 + j
+void launch_vt_from_pool(const void *V, void *vt, int vt_ld, int slots, int nkv, int kv_off, int n_keys, int vt_col0,
+                         cudaStream_t s);
 bool attn_prefill_tc_ok(int d, bool kv_f16);
 cudaError_t launch_attn_prefill_tc(const AttnPrefillTcArgs &a, int n_tiles, cudaStream_t s);
 

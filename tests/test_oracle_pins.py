@@ -248,6 +248,22 @@ def test_prefill_then_step_equals_longer_prefill():
         assert np.allclose(a.K[l][:8], b.K[l][:8], atol=1e-12)
 
 
+def test_chunked_forward_equals_single_forward():
+    """Chunked prefill (rows fed in pieces against the growing KV cache) gives
+    the hidden states of a single pass over all rows: the pin for the CUDA
+    path's dec_prefill_chunk."""
+    spec, w = _tiny()
+    rng = np.random.default_rng(13)
+    emb = rng.standard_normal((23, spec.hidden))
+    one = O.Oracle(spec, w, 32)
+    h1 = one.forward(emb)
+    chunked = O.Oracle(spec, w, 32)
+    parts = [chunked.forward(emb[a:b]) for a, b in ((0, 5), (5, 16), (16, 23))]
+    assert np.allclose(np.concatenate(parts), h1, atol=1e-11, rtol=0)
+    for l in range(spec.n_layers):
+        assert np.allclose(chunked.K[l][:23], one.K[l][:23], atol=1e-12)
+
+
 def test_model_is_causal():
     spec, w = _tiny()
     rng = np.random.default_rng(12)
