@@ -286,6 +286,20 @@ dec_status dec_attn_decode_noalloc(const float *q, const void *K, const void *V,
                                    int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,
                                    float *out, void *stream);
 
+/* Perception projection of encoder rows (canary_qwen/model.cpp, forward
+ * shape: FastConformer encoder -> perception projection Linear(1024, 2048) +
+ * bias -> rows scattered into the prompt): out[t][f] = sum_k W[f][k] enc[t][k]
+ * + bias[f].  Device pointers: enc float32 [T, d_in]; W bf16 [d_out, d_in]
+ * (HF [out, in]); bias float32 [d_out]; out float32 [T, d_out] (may be the
+ * encoder rows that dec_prefill_ids then reads with on_device = 1).  The
+ * activation enters the tensor-core GEMM as two bf16 planes (value and
+ * rounding residual).  d_in a multiple of 64, d_out a multiple of 128;
+ * scratch: caller-owned device memory of at least 2 * align256(T d_in 2) + 16 MiB
+ * (DEC_ERR_OOM otherwise).  Runs on `stream` (NULL = legacy default stream);
+ * returns after the launch. */
+dec_status dec_perception_project(const float *enc, int32_t T, int32_t d_in, const void *W, const float *bias,
+                                  int32_t d_out, float *out, void *scratch, size_t scratch_bytes, void *stream);
+
 /* Standalone kernel (test hook): one prompt-row projection of the prefill,
  * C = X W^T (epi 0: store, epi 1: add into C) or, with gate|up packed in
  * blocks of 128 rows (epi 2), Hout = silu(gate) * up in bf16.  X bf16 [T, K],

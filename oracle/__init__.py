@@ -4,7 +4,7 @@ Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline leg may
 import this package; the CUDA library never does.
 """
 from .decoder import (Oracle, argmax_lowest, assemble_prompt, attention, greedy, linear,
-                      rms_norm, rope_neox, silu, swiglu_ffn)
+                      perception_projection, rms_norm, rope_neox, silu, swiglu_ffn)
 
 __all__ = ["Oracle", "argmax_lowest", "assemble_prompt", "attention", "greedy", "linear",
-           "rms_norm", "rope_neox", "silu", "swiglu_ffn"]
+           "perception_projection", "rms_norm", "rope_neox", "silu", "swiglu_ffn"]

@@ -107,6 +107,13 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, q_pos: np.ndarray) ->
     return out
 
 
+def perception_projection(enc: np.ndarray, W: np.ndarray, bias: np.ndarray) -> np.ndarray:
+    """The step just before the decoder (canary_qwen/model.cpp, forward shape:
+    "perception projection (Linear(1024, 2048) + bias)"): encoder rows enc
+    [T, d_in] to prompt rows W enc + bias, W in the [out, in] layout."""
+    return linear(enc, W) + _f64(bias)[None, :]
+
+
 def silu(z: np.ndarray) -> np.ndarray:
     """SiLU(z) = z / (1 + exp(-z))."""
     z = _f64(z)

@@ -26,7 +26,7 @@ EXPORTS = [
     "dec_prefill_batch", "dec_prefill_ids_batch", "dec_step", "dec_step_batch", "dec_generate", "dec_generate_batch",
     "dec_debug_logits", "dec_set_dumps", "dec_debug_dump", "dec_launch_count", "dec_last_timings",
     "dec_last_error", "dec_status_string", "dec_profile_kernel", "dec_attn_decode_scratch_size",
-    "dec_attn_decode", "dec_attn_decode_noalloc", "dec_debug_gemm",
+    "dec_attn_decode", "dec_attn_decode_noalloc", "dec_debug_gemm", "dec_perception_project",
 ]
 
 
@@ -97,6 +97,8 @@ def load_library():
                                      c_int32, c_int32, c_int32, c_void_p, c_void_p], c_int32),
         "dec_debug_gemm": ([c_void_p, c_int32, c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int32, c_void_p,
                             c_int32, c_int32, c_int32, c_void_p, c_size_t, c_void_p], c_int32),
+        "dec_perception_project": ([c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
+                                    c_size_t, c_void_p], c_int32),
         "dec_last_error": ([H], c_char_p),
         "dec_status_string": ([c_int32], c_char_p),
     }

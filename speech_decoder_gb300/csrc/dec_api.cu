@@ -1410,6 +1410,31 @@ dec_status dec_attn_decode(const float *q, const void *K, const void *V, int32_t
     return e == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
 }
 
+dec_status dec_perception_project(const float *enc, int32_t T, int32_t d_in, const void *W, const float *bias,
+                                  int32_t d_out, float *out, void *scratch, size_t scratch_bytes, void *stream) {
+    if (!enc || !W || !bias || !out || !scratch || T < 1 || d_in < 64 || d_in % 64 || d_out < 128 || d_out % 128)
+        return DEC_ERR_INVALID_ARG;
+    const size_t plane = ((size_t)T * d_in * 2 + 255) / 256 * 256;
+    if (scratch_bytes < 2 * plane + (size_t(16) << 20)) return DEC_ERR_OOM;
+    const int sms = current_sms();
+    if (sms <= 0) return DEC_ERR_CUDA;
+    init_gemm_tc();
+    if (!gemm_tc_ready()) return DEC_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    char *base = static_cast<char *>(scratch);
+    void *hi = base, *lo = base + plane;
+    float *part = reinterpret_cast<float *>(base + 2 * plane);
+    const size_t floats = (scratch_bytes - 2 * plane) / 4;
+    launch_split_planes(enc, hi, lo, (size_t)T * d_in, s);
+    cudaError_t e = launch_gemm_tc(hi, lo, T, W, d_out, d_in, 1, EPI_BIAS_F32, out, d_out, nullptr, nullptr, 0, part,
+                                   floats, nullptr, sms, s, 0, bias);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return DEC_ERR_CUDA;
+    }
+    return cudaGetLastError() == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
+}
+
 dec_status dec_debug_gemm(const void *X, int32_t T, const void *W, int32_t n_feat, int32_t K, int32_t epi, float *C,
                           int32_t ldc, void *Hout, int32_t ldh, int32_t use_tc, int32_t splits, void *scratch,
                           size_t scratch_bytes, void *stream) {

@@ -51,6 +51,7 @@ struct TcArgs {
     __nv_bfloat16 *Hout, *Hout_lo;  // SwiGLU output planes (Hout_lo may be null)
     int ldh;
     float *part;
+    const float *bias;           // EPI_BIAS_F32
     int *err;
     uint32_t idesc, tmem_cols;
 };
@@ -71,6 +72,7 @@ __device__ __forceinline__ void epi_store(const TcArgs &a, int f, int t, float v
     } else if (f < a.n_feat) {
         float *c = a.C + (size_t)t * a.ldc + f;
         if (a.epi == EPI_STORE_F32) *c = v;
+        else if (a.epi == EPI_BIAS_F32) *c = v + a.bias[f];
         else *c += v;
     }
 }
@@ -356,7 +358,9 @@ TcPlan gemm_tc_plan(int T, int n_feat, int K, int groups, int num_sms, size_t sc
 
 cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K, int groups,
                            int epi, float *C, int ldc, void *Hout, void *Hout_lo, int ldh, float *scratch,
-                           size_t scratch_floats, int *err, int num_sms, cudaStream_t s, int force_splits) {
+                           size_t scratch_floats, int *err, int num_sms, cudaStream_t s, int force_splits,
+                           const float *bias) {
+    if (epi == EPI_BIAS_F32 && !bias) return cudaErrorInvalidValue;
     const int planes = X_lo ? 2 : 1;
     const TcPlan p = gemm_tc_plan(T, n_feat, K, groups, num_sms, scratch_floats, force_splits, planes);
     if (!p.ok) return cudaErrorInvalidValue;
@@ -383,6 +387,7 @@ cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W
     a.Hout_lo = static_cast<__nv_bfloat16 *>(Hout_lo);
     a.ldh = ldh;
     a.part = scratch;
+    a.bias = bias;
     a.err = err;
     // instruction descriptor: f32 accumulate, bf16 A and B, both K-major, N = BN, M = 128
     a.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(p.BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);

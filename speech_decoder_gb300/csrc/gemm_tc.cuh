@@ -7,7 +7,7 @@
 namespace dec {
 
 // Epilogues of the prefill projections (shared with the CUDA-core GEMM).
-enum GemmEpi { EPI_STORE_F32 = 0, EPI_RESID_F32 = 1, EPI_SWIGLU_BF16 = 2 };
+enum GemmEpi { EPI_STORE_F32 = 0, EPI_RESID_F32 = 1, EPI_SWIGLU_BF16 = 2, EPI_BIAS_F32 = 3 };
 
 struct TcPlan {
     bool ok;
@@ -29,9 +29,11 @@ struct TcPlan {
 // order; err receives a device error code if a bounded wait expires.
 TcPlan gemm_tc_plan(int T, int n_feat, int K, int groups, int num_sms, size_t scratch_floats,
                     int force_splits = 0, int planes = 1);
+// EPI_BIAS_F32 writes C[t][f] = y + bias[f].
 cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K, int groups,
                            int epi, float *C, int ldc, void *Hout, void *Hout_lo, int ldh, float *scratch,
-                           size_t scratch_floats, int *err, int num_sms, cudaStream_t s, int force_splits = 0);
+                           size_t scratch_floats, int *err, int num_sms, cudaStream_t s, int force_splits = 0,
+                           const float *bias = nullptr);
 void init_gemm_tc();
 bool gemm_tc_ready();
 

@@ -36,6 +36,19 @@ void launch_rmsnorm_rows(const float *x, const float *w, float eps, void *out, v
     else k_rmsnorm_rows<float><<<T, 256, 0, s>>>(x, w, eps, (float *)out, nullptr, H);
 }
 
+// ------------------------------------------------------------------ two bf16 planes
+__global__ void k_split_planes(const float *x, __nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t n) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        store_planes(hi, lo, i, x[i]);
+}
+
+void launch_split_planes(const float *x, void *hi, void *lo, size_t n, cudaStream_t s) {
+    if (n == 0) return;
+    const size_t blocks = (n + 255) / 256;
+    k_split_planes<<<(unsigned)(blocks < 65535 * 8 ? blocks : 65535 * 8), 256, 0, s>>>(
+        x, static_cast<__nv_bfloat16 *>(hi), static_cast<__nv_bfloat16 *>(lo), n);
+}
+
 // ------------------------------------------------------------------ SIMT GEMM
 // 64x64 output tile per CTA, 16-deep k slices staged through shared memory,
 // 4x4 outputs per thread.  K must be a multiple of 16.

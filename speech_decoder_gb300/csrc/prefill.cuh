@@ -9,6 +9,9 @@ namespace dec {
 void launch_rmsnorm_rows(const float *x, const float *w, float eps, void *out, void *out_lo, bool act_bf16, int T,
                          int H, cudaStream_t s);
 
+// n float32 values -> bf16 hi = bf16(v) and lo = bf16(v - hi)
+void launch_split_planes(const float *x, void *hi, void *lo, size_t n, cudaStream_t s);
+
 // C[M, N] (float32, row stride ldc) = or += A[M, K] . W[N, K]^T on CUDA cores
 void launch_gemm_simt(const void *A, bool a_bf16, const void *W, bool w_bf16, float *C, int ldc,
                       int M, int N, int K, int epi, cudaStream_t s);

@@ -163,3 +163,35 @@ def test_gemm_simt_matches_oracle_linear(lib):
     X = _bf16(rng.standard_normal((45, 512)))
     W = _bf16(rng.standard_normal((384, 512)) * 0.02)
     assert rel_err(run_gemm(lib, X, W, 0, 0), O.linear(X, W)) <= 1e-5
+
+
+# ------------------------------------------------------------------ perception projection
+@pytest.mark.parametrize("T", [1, 138, 301])
+def test_perception_projection_matches_oracle(lib, T):
+    """Linear(1024, 2048) + bias of encoder rows (bf16 weights, fp32 rows) on
+    the tensor cores against the oracle's fp64 projection of the same values."""
+    import torch
+    from speech_decoder_gb300 import synth
+    rng = np.random.default_rng(50 + T)
+    d_in, d_out = 1024, 2048
+    enc = rng.standard_normal((T, d_in)).astype(np.float32)
+    W = synth.round_bf16((rng.standard_normal((d_out, d_in)) * 0.02).astype(np.float32))
+    bias = rng.standard_normal(d_out).astype(np.float32)
+    dev = "cuda:0"
+    t_enc = torch.from_numpy(enc).to(dev)
+    t_W = torch.from_numpy(W).to(torch.bfloat16).to(dev)
+    t_b = torch.from_numpy(bias).to(dev)
+    out = torch.full((T, d_out), 3.0, dtype=torch.float32, device=dev)
+    n = 2 * ((T * d_in * 2 + 255) // 256 * 256) + (16 << 20)
+    scratch = torch.empty(n, dtype=torch.uint8, device=dev)
+    st = lib.dec_perception_project(t_enc.data_ptr(), T, d_in, t_W.data_ptr(), t_b.data_ptr(), d_out, out.data_ptr(),
+                                    scratch.data_ptr(), n, torch.cuda.current_stream().cuda_stream)
+    assert st == 0, st
+    torch.cuda.synchronize()
+    ref = O.perception_projection(enc.astype(np.float64), W.astype(np.float64), bias)
+    e = rel_err(out.cpu().numpy(), ref)
+    assert e <= 1e-4, e
+    # too little scratch is refused before any work
+    assert lib.dec_perception_project(t_enc.data_ptr(), T, d_in, t_W.data_ptr(), t_b.data_ptr(), d_out,
+                                      out.data_ptr(), scratch.data_ptr(), 1024,
+                                      torch.cuda.current_stream().cuda_stream) == 2

@@ -169,6 +169,21 @@ def test_gqa_equals_mha_with_repeated_kv():
 
 
 # ------------------------------------------------------------------ SwiGLU
+def test_perception_projection_closed_forms():
+    """W = 0 gives the bias on every row; a one-hot W row copies one input
+    column; bias is per output feature (not per row)."""
+    rng = np.random.default_rng(21)
+    enc = rng.standard_normal((5, 8))
+    bias = rng.standard_normal(6)
+    assert np.array_equal(O.perception_projection(enc, np.zeros((6, 8)), bias), np.tile(bias, (5, 1)))
+    W = np.zeros((6, 8))
+    W[2, 7] = 1.0
+    W[4, 0] = -2.0
+    y = O.perception_projection(enc, W, np.zeros(6))
+    assert np.array_equal(y[:, 2], enc[:, 7]) and np.array_equal(y[:, 4], -2.0 * enc[:, 0])
+    assert np.count_nonzero(y[:, [0, 1, 3, 5]]) == 0
+
+
 def test_silu_values():
     assert O.silu(np.array(0.0)) == 0.0
     assert abs(O.silu(np.array(1.0)) - 0.7310585786300049) < 1e-15
