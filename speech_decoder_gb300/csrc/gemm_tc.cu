@@ -325,8 +325,10 @@ TcPlan gemm_tc_plan(int T, int n_feat, int K, int groups, int num_sms, size_t sc
     TcPlan p{};
     p.ok = g_tc_ready && T >= 1 && K % kBK == 0 && n_feat % (128 * groups) == 0 && (planes == 1 || planes == 2);
     if (!p.ok) return p;
-    // two activation planes: N tiles of at most 128 tokens keep three or more stages
-    const int bn_max = planes == 2 ? 128 : 256;
+    // two activation planes: N tiles of at most 128 tokens keep three or more
+    // stages; a prompt of up to 256 rows stays one N tile (the weights, the
+    // bytes that bound a short prompt, are then read once)
+    const int bn_max = planes == 2 && T > 256 ? 128 : 256;
     const int BN = T <= bn_max ? ((T + 15) / 16) * 16 : bn_max;
     p.BN = BN;
     const size_t stage = (size_t)groups * 16384 + (size_t)planes * BN * 128;
