@@ -162,7 +162,14 @@ static std::string validate(const dec_hparams *hp) {
     return "";
 }
 
-static int splits_for(const dec_handle *h, int B) { return attn_decode_splits(B, h->hp.n_kv_heads, h->num_sms); }
+// Split-KV partitions of the step attention: a split holds at least
+// kAttnMinChunk keys, so more splits than the longest context can fill would
+// only launch CTAs that exit at once (the step graph is captured once, so the
+// bound is the context capacity, not the current length).
+static int splits_for(const dec_handle *h, int B) {
+    const int by_ctx = (h->hp.max_ctx + kAttnMinChunk - 1) / kAttnMinChunk;
+    return std::max(1, std::min(attn_decode_splits(B, h->hp.n_kv_heads, h->num_sms), by_ctx));
+}
 
 static int gemv_ctas_per_sm() {
     const char *c = std::getenv("SPEECH_DECODER_GEMV_CTAS_PER_SM");
