@@ -27,6 +27,25 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 }
 template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
 
+// Launch with programmatic stream serialization: the kernel may start while
+// its predecessor drains and must call griddepcontrol.wait before it reads
+// the predecessor's results or writes anything the predecessor reads.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Second bf16 plane of an activation: the rounding residual v - bf16(v), so
 // that hi + lo carries about 16 mantissa bits (the tensor-core GEMM reads both).
 __device__ __forceinline__ void store_planes(__nv_bfloat16 *hi, __nv_bfloat16 *lo, size_t i, float v) {

@@ -343,12 +343,22 @@ constexpr int attn_tile_keys() {
 
 // NREP: query heads per KV head (1 or 2) for the grouped scoring; 0 = any
 // n_rep <= kMaxRep with the lane-per-dims scoring (W = kAW warps)
-template <typename TKV, int D, int NREP>
-__global__ void __launch_bounds__((NREP ? kSW : kAW) * 32) k_attn_step(AttnDecArgs a, float scale) {
-    constexpr int W = NREP ? kSW : kAW;
+// Two CTA sizes: SMALL = false (one CTA per SM: 16 warps, 256-key tiles) for
+// a few sequences; SMALL = true (8 warps, 128-key tiles, about half the shared
+// memory, two CTAs per SM) for batched rows, whose many (sequence, head,
+// split) CTAs would otherwise run in several waves.
+template <bool SMALL, int NREP>
+__host__ __device__ constexpr int attn_step_warps() {
+    return SMALL ? kAW : (NREP ? kSW : kAW);
+}
+
+template <typename TKV, int D, int NREP, bool SMALL>
+__global__ void __launch_bounds__(attn_step_warps<SMALL, NREP>() * 32, SMALL ? 2 : 1)
+    k_attn_step(AttnDecArgs a, float scale) {
+    constexpr int W = attn_step_warps<SMALL, NREP>();
     constexpr int PL = D / 32;
     constexpr int DL = D / kLG;
-    constexpr int T = attn_tile_keys<TKV, D>();
+    constexpr int T = SMALL ? attn_tile_keys<TKV, D>() / 2 : attn_tile_keys<TKV, D>();
     extern __shared__ __align__(128) unsigned char dsm[];
     TKV *Ks = reinterpret_cast<TKV *>(dsm);
     TKV *Vs = Ks + (size_t)T * D;
@@ -554,30 +564,39 @@ __global__ void __launch_bounds__((NREP ? kSW : kAW) * 32) k_attn_step(AttnDecAr
     attn_finish<D, W>(a, sm, b, g, s, S, n_used, n_rep);
 }
 
-template <typename TKV, int D, int NREP>
+template <typename TKV, int D, int NREP, bool SMALL>
 constexpr size_t attn_step_smem() {
-    return 2 * (size_t)attn_tile_keys<TKV, D>() * D * sizeof(TKV) + sizeof(AttnSmem<D, NREP ? kSW : kAW>);
+    return 2 * (size_t)(SMALL ? attn_tile_keys<TKV, D>() / 2 : attn_tile_keys<TKV, D>()) * D * sizeof(TKV) +
+           sizeof(AttnSmem<D, attn_step_warps<SMALL, NREP>()>);
 }
 
-template <typename TKV, int D, int NREP>
+template <typename TKV, int D, int NREP, bool SMALL>
 static void launch_step_attn(cudaLaunchConfig_t cfg, const AttnDecArgs &a, float scale) {
-    cfg.blockDim = dim3((NREP ? kSW : kAW) * 32);
-    cfg.dynamicSmemBytes = attn_step_smem<TKV, D, NREP>();
-    cudaLaunchKernelEx(&cfg, k_attn_step<TKV, D, NREP>, a, scale);
+    cfg.blockDim = dim3(attn_step_warps<SMALL, NREP>() * 32);
+    cfg.dynamicSmemBytes = attn_step_smem<TKV, D, NREP, SMALL>();
+    cudaLaunchKernelEx(&cfg, k_attn_step<TKV, D, NREP, SMALL>, a, scale);
+}
+
+template <typename TKV, int D, bool SMALL>
+static void launch_step_attn_rep(cudaLaunchConfig_t cfg, const AttnDecArgs &a, float scale) {
+    const int n_rep = a.nq / a.nkv;
+    if (n_rep == 1) launch_step_attn<TKV, D, 1, SMALL>(cfg, a, scale);
+    else if (n_rep == 2) launch_step_attn<TKV, D, 2, SMALL>(cfg, a, scale);
+    else launch_step_attn<TKV, D, 0, SMALL>(cfg, a, scale);
 }
 
 template <typename TKV, int D>
-static void launch_step_attn_rep(cudaLaunchConfig_t cfg, const AttnDecArgs &a, float scale) {
-    const int n_rep = a.nq / a.nkv;
-    if (n_rep == 1) launch_step_attn<TKV, D, 1>(cfg, a, scale);
-    else if (n_rep == 2) launch_step_attn<TKV, D, 2>(cfg, a, scale);
-    else launch_step_attn<TKV, D, 0>(cfg, a, scale);
+static void launch_step_attn_size(cudaLaunchConfig_t cfg, const AttnDecArgs &a, float scale) {
+    if (a.B > kGroupB) launch_step_attn_rep<TKV, D, true>(cfg, a, scale);
+    else launch_step_attn_rep<TKV, D, false>(cfg, a, scale);
 }
 
 template <typename TKV, int D, int NREP>
 static void init_step_attn() {
-    cudaFuncSetAttribute(k_attn_step<TKV, D, NREP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)attn_step_smem<TKV, D, NREP>());
+    cudaFuncSetAttribute(k_attn_step<TKV, D, NREP, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)attn_step_smem<TKV, D, NREP, false>());
+    cudaFuncSetAttribute(k_attn_step<TKV, D, NREP, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)attn_step_smem<TKV, D, NREP, true>());
 }
 
 template <bool STEP>
@@ -593,10 +612,10 @@ static void attn_launch(bool kv_f16, const AttnDecArgs &a, int splits, cudaStrea
     cfg.numAttrs = 1;
     const float scale = (float)(1.0 / sqrt((double)a.d));
     if (STEP) {
-        if (kv_f16 && a.d == 128) launch_step_attn_rep<__half, 128>(cfg, a, scale);
-        else if (kv_f16) launch_step_attn_rep<__half, 64>(cfg, a, scale);
-        else if (a.d == 128) launch_step_attn_rep<float, 128>(cfg, a, scale);
-        else launch_step_attn_rep<float, 64>(cfg, a, scale);
+        if (kv_f16 && a.d == 128) launch_step_attn_size<__half, 128>(cfg, a, scale);
+        else if (kv_f16) launch_step_attn_size<__half, 64>(cfg, a, scale);
+        else if (a.d == 128) launch_step_attn_size<float, 128>(cfg, a, scale);
+        else launch_step_attn_size<float, 64>(cfg, a, scale);
         return;
     }
     if (kv_f16) {
@@ -691,8 +710,8 @@ __global__ void k_embed_rows(const TW *embed, SeqState *st, float *x, int H) {
 }
 
 void launch_embed_rows(const void *embed, bool w_bf16, SeqState *st, float *x, int B, int H, cudaStream_t s) {
-    if (w_bf16) k_embed_rows<__nv_bfloat16><<<B, 256, 0, s>>>((const __nv_bfloat16 *)embed, st, x, H);
-    else k_embed_rows<float><<<B, 256, 0, s>>>((const float *)embed, st, x, H);
+    if (w_bf16) launch_pdl(k_embed_rows<__nv_bfloat16>, dim3(B), dim3(256), 0, s, (const __nv_bfloat16 *)embed, st, x, H);
+    else launch_pdl(k_embed_rows<float>, dim3(B), dim3(256), 0, s, (const float *)embed, st, x, H);
 }
 
 // One CTA per row: strict '>' scan per thread over ascending indices, then a
@@ -739,7 +758,7 @@ __global__ void __launch_bounds__(512) k_argmax_rows(const float *logits, int V,
 
 void launch_argmax_rows(const float *logits, int B, int V, SeqState *st, int32_t *out_ids, int out_ids_cap,
                         cudaStream_t s) {
-    k_argmax_rows<<<B, 512, 0, s>>>(logits, V, st, out_ids, out_ids_cap);
+    launch_pdl(k_argmax_rows, dim3(B), dim3(512), 0, s, logits, V, st, out_ids, out_ids_cap);
 }
 
 }  // namespace dec

@@ -15,6 +15,8 @@ template <typename TO>
 __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float *x, const float *w, float eps, TO *out,
                                                       TO *out_lo, int H) {
     __shared__ float red[32];
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const size_t t = blockIdx.x;
     const float *xr = x + t * H;
     float ss = 0.f;
@@ -32,8 +34,9 @@ void launch_rmsnorm_rows(const float *x, const float *w, float eps, void *out, v
                          int H, cudaStream_t s) {
     if (T <= 0) return;
     if (act_bf16)
-        k_rmsnorm_rows<__nv_bfloat16><<<T, 256, 0, s>>>(x, w, eps, (__nv_bfloat16 *)out, (__nv_bfloat16 *)out_lo, H);
-    else k_rmsnorm_rows<float><<<T, 256, 0, s>>>(x, w, eps, (float *)out, nullptr, H);
+        launch_pdl(k_rmsnorm_rows<__nv_bfloat16>, dim3(T), dim3(256), 0, s, x, w, eps, (__nv_bfloat16 *)out,
+                   (__nv_bfloat16 *)out_lo, H);
+    else launch_pdl(k_rmsnorm_rows<float>, dim3(T), dim3(256), 0, s, x, w, eps, (float *)out, (float *)nullptr, H);
 }
 
 // ------------------------------------------------------------------ two bf16 planes
