@@ -80,9 +80,14 @@ __device__ __forceinline__ float cons_sum(float v, float *red) {
 // Activation rows of this CTA's sequences into shared memory (consumer
 // threads).  The rows' loads are issued together with the liveness reads (rows
 // that turn out finished are computed and not stored); the RMSNorm weights were
-// staged in nw before the kernel waited on its predecessor.
+// loaded into registers (nwr: this thread's first kNwRegs elements) before the
+// kernel waited on its predecessor, so that load and the activation loads are
+// in flight together.
+constexpr int kNwRegs = 8;                            // K = 2048 over 256 consumer threads
+
 template <int NB, int IN>
-__device__ void prologue(const GemvArgs &a, float *xs, const float *nw, int b0, int *live, int CPR, float *sred) {
+__device__ void prologue(const GemvArgs &a, float *xs, const float (&nwr)[kNwRegs], int b0, int *live, int CPR,
+                         float *sred) {
     const int K = a.K, tid = threadIdx.x;
     if (tid < kGroupB) live[tid] = tid < NB && b0 + tid < a.B && row_live(a.st, b0 + tid);
     if (IN == IN_EMBED_NORM) cons_sync();                 // the token ids come from the state
@@ -149,9 +154,17 @@ __device__ void prologue(const GemvArgs &a, float *xs, const float *nw, int b0, 
         if (!live[bi]) continue;                          // uniform
         const float r = rsqrtf(cons_sum(ss[bi], sred) / (float)K + a.eps);
         float *xr = xs + (size_t)bi * K;
-        for (int k = tid; k < K; k += kCT) {
+#pragma unroll
+        for (int i = 0; i < kNwRegs; ++i) {
+            const int k = tid + i * kCT;
+            if (k < K) {
+                const int o = xs_off(k, CPR);
+                xr[o] = xr[o] * r * nwr[i];
+            }
+        }
+        for (int k = tid + kNwRegs * kCT; k < K; k += kCT) {
             const int o = xs_off(k, CPR);
-            xr[o] = xr[o] * r * nw[k];
+            xr[o] = xr[o] * r * a.norm_w[k];
         }
     }
 }
@@ -317,7 +330,6 @@ __global__ void __launch_bounds__(kTT, 2) k_gemv_stream(GemvArgs a) {
     const int b0 = blockIdx.y * kGroupB;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     float *xs = reinterpret_cast<float *>(smem + (size_t)NS * kStage);
-    float *nw = xs + (size_t)NB * K;                      // RMSNorm weight (norm prologues)
     const unsigned char *W = reinterpret_cast<const unsigned char *>(a.W);
     constexpr bool kNorm = IN == IN_NORM || IN == IN_EMBED_NORM;
 
@@ -380,10 +392,14 @@ __global__ void __launch_bounds__(kTT, 2) k_gemv_stream(GemvArgs a) {
     }
 
     if (warp < kCW) {
-        if (kNorm)                                        // weights: no dependency either
-            for (int k = tid; k < K; k += kCT) nw[k] = a.norm_w[k];
+        float nwr[kNwRegs];                               // weights: no dependency either
+#pragma unroll
+        for (int i = 0; i < kNwRegs; ++i) {
+            const int k = tid + i * kCT;
+            nwr[i] = kNorm && k < K ? a.norm_w[k] : 0.f;
+        }
         ptx::pdl_wait();
-        prologue<NB, IN>(a, xs, nw, b0, live_s, CPR, sred);
+        prologue<NB, IN>(a, xs, nwr, b0, live_s, CPR, sred);
         if (tid == 0) {
             int any = 0;
             for (int b = 0; b < NB; ++b) any |= live_s[b];
@@ -567,8 +583,8 @@ void gemv_stream_set_slots(int slots) {
 
 GemvPlan gemv_stream_plan(int in_mode, int K, int nb, int N, int grid_x) {
     GemvPlan p{};
-    const bool norm = in_mode == IN_NORM || in_mode == IN_EMBED_NORM;
-    const size_t xs = ((size_t)(nb + (norm ? 1 : 0)) * K * 4 + 15) / 16 * 16;
+    (void)in_mode;
+    const size_t xs = ((size_t)nb * K * 4 + 15) / 16 * 16;
     int ns = g_stream_slots ? g_stream_slots : kAutoStages;
     while (ns > 2 && (size_t)ns * kStage + xs > (size_t)kGemvMaxSmem) --ns;
     p.n_ring = ns;
