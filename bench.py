@@ -144,7 +144,7 @@ def workload_for(args):
 
 def kernel_sha() -> str:
     h = hashlib.sha256()
-    for f in ("gemv.cu", "gemv_stream.cu", "decode.cuh", "common.cuh", "ptx.cuh"):
+    for f in ("gemv.cu", "gemv_stream.cu", "attn_step.cuh", "decode.cuh", "common.cuh", "ptx.cuh"):
         with open(os.path.join(ROOT, "speech_decoder_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

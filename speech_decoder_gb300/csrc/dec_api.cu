@@ -111,6 +111,7 @@ struct dec_handle {
     StepLayer *step_layers = nullptr;
     unsigned long long *step_bar = nullptr;
     bool use_step = false;
+    bool attn_fuse = false;         // single-sequence q|k|v GEMV runs the step attention (short contexts)
 };
 
 // ------------------------------------------------------------------ helpers
@@ -340,11 +341,45 @@ static void set_prefetch(const dec_handle *h, GemvArgs &g, const void *W, int N,
     g.pf_bytes = h->pf_bytes;
 }
 
-// One decoder block for the step rows in xd (one row per sequence).
+// Step attention of layer l over the q|k|v rows in qkvd (K/V appended at n_past).
+static AttnDecArgs step_attn_args(const dec_handle *h, int l, int B) {
+    const dec_hparams &hp = h->hp;
+    const DevLayer &L = h->L[l];
+    AttnDecArgs a{};
+    a.qkv = h->qkvd;
+    a.qn_w = L.qn;
+    a.kn_w = L.kn;
+    a.eps = hp.rms_eps;
+    a.rope = h->rope;
+    a.Kc = L.K;
+    a.Vc = L.V;
+    a.slots = (int)h->slots;
+    a.o = h->od;
+    a.part = h->attn_part;
+    a.counter = h->attn_counter;
+    a.st = h->st;
+    a.nq = hp.n_heads;
+    a.nkv = hp.n_kv_heads;
+    a.d = hp.head_dim;
+    a.B = B;
+    a.append = 1;
+    return a;
+}
+
+// Option (SPEECH_DECODER_STEP_ATTN=fused): a single sequence with a context
+// capacity of at most kFusedAttnMaxCtx keys has the q|k|v GEMV finish each KV
+// head's attention (one CTA per head, all keys) and no separate attention launch.
+static bool qkv_attn_fused(const dec_handle *h, int B) {
+    const dec_hparams &hp = h->hp;
+    return B == 1 && h->attn_fuse && h->w_bf16 && h->kv_f16 && gemv_impl() == 4 && hp.max_ctx <= kFusedAttnMaxCtx &&
+           gemv_stream_qkv_attn_ok(hp.hidden, gemv_grid(qkv_rows(hp), h->num_sms, h->gemv_ctas), hp.n_heads,
+                                   hp.n_kv_heads, hp.head_dim, h->kv_f16);
+}
+
 // The decode step's launches of one block (one row per sequence).  Each
 // projection helper returns the launch's algorithmic bytes (weights once, the
 // activation rows in and out) for the profiler.
-static double layer_qkv(dec_handle *h, int l, int B, bool from_embed) {
+static double layer_qkv(dec_handle *h, int l, int B, bool from_embed, bool with_attn) {
     const dec_hparams &hp = h->hp;
     const DevLayer &L = h->L[l];
     const int H = hp.hidden, nqd = hp.n_heads * hp.head_dim;
@@ -369,34 +404,18 @@ static double layer_qkv(dec_handle *h, int l, int B, bool from_embed) {
         g.kvp_row_bytes = (int)(hp.head_dim * kvsize(hp));
     }
     const bool emb = from_embed && l == 0;
-    launch_gemv(emb ? IN_EMBED_NORM : IN_NORM, OUT_STORE, h->w_bf16, g, gemv_grid(g.N, h->num_sms, h->gemv_ctas),
-                h->stream);
+    if (with_attn) {
+        g.at = step_attn_args(h, l, B);
+        g.at_scale = (float)(1.0 / std::sqrt((double)hp.head_dim));
+    }
+    launch_gemv(emb ? IN_EMBED_NORM : IN_NORM, with_attn ? OUT_QKV_ATTN : OUT_STORE, h->w_bf16, g,
+                gemv_grid(g.N, h->num_sms, h->gemv_ctas), h->stream);
     h->enq++;
     return (double)g.N * H * wsize(hp) + (double)B * (H + g.N) * 4.0;
 }
 
 static void layer_attn(dec_handle *h, int l, int B) {
-    const dec_hparams &hp = h->hp;
-    const DevLayer &L = h->L[l];
-    AttnDecArgs a{};
-    a.qkv = h->qkvd;
-    a.qn_w = L.qn;
-    a.kn_w = L.kn;
-    a.eps = hp.rms_eps;
-    a.rope = h->rope;
-    a.Kc = L.K;
-    a.Vc = L.V;
-    a.slots = (int)h->slots;
-    a.o = h->od;
-    a.part = h->attn_part;
-    a.counter = h->attn_counter;
-    a.st = h->st;
-    a.nq = hp.n_heads;
-    a.nkv = hp.n_kv_heads;
-    a.d = hp.head_dim;
-    a.B = B;
-    a.append = 1;
-    launch_attn_decode(h->kv_f16, a, splits_for(h, B), h->stream);
+    launch_attn_decode(h->kv_f16, step_attn_args(h, l, B), splits_for(h, B), h->stream);
     h->enq++;
 }
 
@@ -477,8 +496,9 @@ static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
         enqueue_decode_layer_tc(h, l, B, from_embed);
         return;
     }
-    layer_qkv(h, l, B, from_embed);
-    layer_attn(h, l, B);
+    const bool fused = qkv_attn_fused(h, B);
+    layer_qkv(h, l, B, from_embed, fused);
+    if (!fused) layer_attn(h, l, B);
     layer_o(h, l, B);
     layer_gu(h, l, B);
     layer_down(h, l, B);
@@ -1012,6 +1032,13 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
     }
     CKC(cudaMemsetAsync(h->attn_counter, 0, (size_t)hp->max_batch * nkv * sizeof(unsigned), s));
     {
+        // SPEECH_DECODER_STEP_ATTN=fused lets the q|k|v GEMV of a single sequence
+        // run the step attention (measured slower than the split-KV kernel on
+        // the 0.6B and 1.7B shapes: one 9-warp CTA per KV head over every key)
+        const char *sa = std::getenv("SPEECH_DECODER_STEP_ATTN");
+        h->attn_fuse = sa && !std::strcmp(sa, "fused");
+    }
+    {
         // tensor-core prompt attention: V^T columns past a sequence's keys meet
         // zero probabilities and must hold finite values, so the scratch starts at 0
         const char *pa = std::getenv("SPEECH_DECODER_PREFILL_ATTN");
@@ -1339,7 +1366,7 @@ dec_status dec_profile_kernel(dec_handle *h, int32_t op, int32_t iters, float *a
                 launches += 2;
             } else if (op == 0) {
                 // the step's four projection GEMVs of the layer, as the step launches them
-                bytes += layer_qkv(h, l, B, false);
+                bytes += layer_qkv(h, l, B, false, false);
                 bytes += layer_o(h, l, B);
                 bytes += layer_gu(h, l, B);
                 bytes += layer_down(h, l, B);

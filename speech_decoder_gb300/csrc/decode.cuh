@@ -7,7 +7,33 @@ namespace dec {
 enum GemvIn { IN_NORM = 0, IN_EMBED_NORM = 1, IN_PLAIN = 2, IN_SWIGLU = 3 };
 // OUT_SWIGLU (producer-warp GEMV only): W is the packed gate|up matrix, N the
 // ffn features, out[b][f] = silu(gate_f) * up_f
-enum GemvOut { OUT_STORE = 0, OUT_RESID = 1, OUT_ARGMAX = 2, OUT_SWIGLU = 3 };
+// OUT_QKV_ATTN (producer-warp GEMV, one sequence): W is the packed q|k|v
+// matrix; OUT_STORE of the row, then the CTA that completes the last rows of
+// a KV head's q, k and v runs that head's step attention (args a.at)
+enum GemvOut { OUT_STORE = 0, OUT_RESID = 1, OUT_ARGMAX = 2, OUT_SWIGLU = 3, OUT_QKV_ATTN = 4 };
+
+struct AttnDecArgs {
+    const float *qkv;       // [B, (nq + 2 nkv) d] raw projections of the step's row
+    const float *qn_w, *kn_w;
+    float eps;
+    const float2 *rope;     // [max_pos, d/2] (cos, sin)
+    void *Kc, *Vc;          // this layer's pool [nkv][slots][d]
+    int slots;
+    float *o;               // [B, nq d]
+    float *part;            // scratch [B][nkv][S][n_rep][d + 2]
+    unsigned *counter;      // scratch [B][nkv], zero between launches
+    SeqState *st;
+    int nq, nkv, d;
+    int B;                  // sequences (grid z)
+    int append;             // 1: write the row's K/V at slot n_past first
+    // plain mode (no state, no norm/RoPE/append): q already normed and roped
+    const float *q_plain;   // [B, nq, d]
+    const int32_t *kv_off;  // [B] first slot of each sequence
+    const int32_t *kv_len;  // [B] visible keys (rows with len <= 0 or out of range are skipped)
+    __nv_bfloat16 *o_bf16;  // optional bf16 copy of o (input of the tensor-core O projection)
+    __nv_bfloat16 *o_bf16_lo;  // with o_bf16: the bf16 rounding residual (may be null)
+
+};
 
 struct GemvArgs {
     const void *W;          // [N, K] weights (bf16 or f32)
@@ -35,6 +61,10 @@ struct GemvArgs {
     // KV of this layer pulled into L2 for the attention that follows (may be null)
     const void *kvp_K, *kvp_V;
     int kvp_slots, kvp_nkv, kvp_row_bytes;
+    // OUT_QKV_ATTN: the step attention of the row (at.qkv = out; at.counter
+    // holds one completed-row count per KV head, zero between launches)
+    AttnDecArgs at;
+    float at_scale;
     // filled in by launch_gemv: shared-memory slots per warp, units per CTA
     int n_ring;
     int max_units;
@@ -56,28 +86,6 @@ void gemv_reload_env();
 int gemv_impl();
 void gemv_set_ring(int slots);
 
-struct AttnDecArgs {
-    const float *qkv;       // [B, (nq + 2 nkv) d] raw projections of the step's row
-    const float *qn_w, *kn_w;
-    float eps;
-    const float2 *rope;     // [max_pos, d/2] (cos, sin)
-    void *Kc, *Vc;          // this layer's pool [nkv][slots][d]
-    int slots;
-    float *o;               // [B, nq d]
-    float *part;            // scratch [B][nkv][S][n_rep][d + 2]
-    unsigned *counter;      // scratch [B][nkv], zero between launches
-    SeqState *st;
-    int nq, nkv, d;
-    int B;                  // sequences (grid z)
-    int append;             // 1: write the row's K/V at slot n_past first
-    // plain mode (no state, no norm/RoPE/append): q already normed and roped
-    const float *q_plain;   // [B, nq, d]
-    const int32_t *kv_off;  // [B] first slot of each sequence
-    const int32_t *kv_len;  // [B] visible keys (rows with len <= 0 or out of range are skipped)
-    __nv_bfloat16 *o_bf16;  // optional bf16 copy of o (input of the tensor-core O projection)
-    __nv_bfloat16 *o_bf16_lo;  // with o_bf16: the bf16 rounding residual (may be null)
-
-};
 
 // Batched-step helpers (rows of several sequences through the tensor-core GEMM):
 // x[b] = embed[cur_tok[b]] for live rows; row argmax of logits [B, V] that
@@ -114,6 +122,12 @@ bool launch_gemv_stream(int in_mode, int out_mode, const GemvArgs &a, int grid_x
 void gemv_stream_set_slots(int slots);
 // the fused gate|up + SwiGLU GEMV fits (hidden K, ffn features)
 bool gemv_stream_swiglu_ok(int K, int nb, int ffn, int grid_x);
+// the q|k|v GEMV of one sequence with the step attention fused (f16 KV,
+// head_dim 128, two query heads per KV head) fits this shape
+bool gemv_stream_qkv_attn_ok(int K, int grid_x, int nq, int nkv, int d, bool kv_f16);
+// longest context for which one CTA per KV head runs the step attention
+// (longer ones take the split-KV attention kernel)
+constexpr int kFusedAttnMaxCtx = 1024;
 void init_gemv_stream_kernels();
 // GEMV CTAs per SM that suit the selected implementation
 int gemv_default_ctas_per_sm();

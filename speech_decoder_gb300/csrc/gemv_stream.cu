@@ -18,10 +18,15 @@
 // output, or silu(gate)*up from the packed gate|up rows; the epilogue stores,
 // adds into the residual, or writes logits and takes the argmax with the lowest
 // index winning ties, the last CTA advancing the greedy state.
+//
+// The q|k|v GEMV of a single sequence can finish the step attention itself:
+// each CTA counts the rows it completed of every KV head's q, k and v rows on
+// an acquire-release ticket, and the CTA that completes a head's last rows
+// runs that head's attention in its (by then idle) ring memory.  No CTA waits
+// for another, and the step loses one kernel boundary per layer.
 #include <climits>
 
-#include "decode.cuh"
-#include "ptx.cuh"
+#include "attn_step.cuh"
 
 namespace dec {
 namespace {
@@ -66,28 +71,71 @@ __host__ __device__ __forceinline__ int pairs_per_stage(int K) {
     return K * 2 > kStage ? 0 : p;
 }
 
-// sum over the consumer threads
-__device__ __forceinline__ float cons_sum(float v, float *red) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    v = warp_sum(v);
-    cons_sync();
-    if (lane == 0) red[warp] = v;
-    cons_sync();
-    float t = lane < kCW ? red[lane] : 0.f;
-    return warp_sum(t);
+// Head dims, query heads per KV head and key tile of the fused step attention.
+constexpr int kFD = 128;
+constexpr int kFRep = 2;
+constexpr int kFT = attn_tile_keys<__half, kFD>();
+constexpr size_t kFusedAttnSmem = 2 * (size_t)kFT * kFD * sizeof(__half) + sizeof(AttnSmem<kFD, kTT / 32>);
+
+__host__ __device__ __forceinline__ int range_overlap(int a0, int a1, int b0, int b1) {
+    const int lo = a0 > b0 ? a0 : b0, hi = a1 < b1 ? a1 : b1;
+    return hi > lo ? hi - lo : 0;
+}
+
+// OUT_QKV_ATTN tail (all threads of the CTA, after its rows [r0, r1) of the
+// q|k|v row are stored).  Thread g adds the CTA's rows of KV head g (its q, k
+// and v rows) to the head's acquire-release ticket; the CTA whose addition
+// completes the head's (kFRep + 2) * kFD rows runs its attention.  Every count
+// is added before any attention runs, so no head's completion waits behind
+// another head's attention.  Shared memory from `smem` on holds the key/value
+// tiles; bar is the tail's own mbarrier; mask is a shared word.
+__device__ void qkv_attn_tail(const GemvArgs &a, int r0, int r1, unsigned char *smem, uint64_t *bar,
+                              unsigned *mask) {
+    constexpr int W = kTT / 32, PL = kFD / 32;
+    const AttnDecArgs &at = a.at;
+    const int lane = threadIdx.x & 31;
+    const unsigned need = (unsigned)((kFRep + 2) * kFD);
+    float qw[PL], kw[PL];
+    load_vec<PL>(at.qn_w + lane * PL, qw);
+    load_vec<PL>(at.kn_w + lane * PL, kw);
+    if (threadIdx.x == 0) *mask = 0u;
+    __syncthreads();                                     // every store of the rows precedes the releases
+    if (threadIdx.x < at.nkv) {
+        const int g = threadIdx.x, qd = at.nq * kFD, kd = at.nkv * kFD;
+        const int cnt = range_overlap(r0, r1, g * kFRep * kFD, (g + 1) * kFRep * kFD) +
+                        range_overlap(r0, r1, qd + g * kFD, qd + (g + 1) * kFD) +
+                        range_overlap(r0, r1, qd + kd + g * kFD, qd + kd + (g + 1) * kFD);
+        if (cnt > 0 && atomic_add_acq_rel(&at.counter[g], (unsigned)cnt) + (unsigned)cnt == need) {
+            at.counter[g] = 0u;                          // every CTA of the head has added: reset for the next launch
+            atomicOr(mask, 1u << g);
+        }
+    }
+    __syncthreads();
+    const unsigned m = *mask;
+    uint32_t phase = 0;
+    for (int g = 0; g < at.nkv; ++g) {
+        if (!((m >> g) & 1u)) continue;                  // uniform
+        // the ring, the activation rows and an earlier head's tiles were
+        // accessed by the generic proxy; the tiles arrive there by bulk copy
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+        attn_step_core<__half, kFD, kFRep, W, kFT>(at, a.at_scale, g, 0, 1, 0, smem, bar, phase, qw, kw);
+    }
 }
 
 // Activation rows of this CTA's sequences into shared memory (consumer
 // threads).  The rows' loads are issued together with the liveness reads (rows
-// that turn out finished are computed and not stored); the RMSNorm weights were
-// loaded into registers (nwr: this thread's first kNwRegs elements) before the
-// kernel waited on its predecessor, so that load and the activation loads are
-// in flight together.
+// that turn out finished are computed and not stored).  RMSNorm inputs are
+// stored as x * w; each row's scale r = 1 / sqrt(mean(x^2) + eps) is returned
+// in rs (every thread sums the warps' partial sums itself, after the one
+// barrier that publishes the rows) and multiplies the finished dot products.
+// The norm weights were loaded into registers (nwr: this thread's first
+// kNwRegs elements) before the kernel waited on its predecessor.
 constexpr int kNwRegs = 8;                            // K = 2048 over 256 consumer threads
 
 template <int NB, int IN>
 __device__ void prologue(const GemvArgs &a, float *xs, const float (&nwr)[kNwRegs], int b0, int *live, int CPR,
-                         float *sred) {
+                         float *sred, float (&rs)[NB]) {
     const int K = a.K, tid = threadIdx.x;
     if (tid < kGroupB) live[tid] = tid < NB && b0 + tid < a.B && row_live(a.st, b0 + tid);
     if (IN == IN_EMBED_NORM) cons_sync();                 // the token ids come from the state
@@ -132,6 +180,8 @@ __device__ void prologue(const GemvArgs &a, float *xs, const float (&nwr)[kNwReg
                 }
             }
         }
+        constexpr bool kNorm = IN == IN_NORM || IN == IN_EMBED_NORM;
+        static_assert(!kNorm || P <= kNwRegs, "the first pass's norm weights are the registers");
 #pragma unroll
         for (int bi = 0; bi < NB; ++bi) {
             float *xr = xs + (size_t)bi * K;
@@ -139,7 +189,9 @@ __device__ void prologue(const GemvArgs &a, float *xs, const float (&nwr)[kNwReg
             for (int i = 0; i < P; ++i) {
                 const int k = k0 + i * kCT;
                 if (k < K) {
-                    xr[xs_off(k, CPR)] = v[bi][i];
+                    float w = 1.f;
+                    if (kNorm) w = k0 == tid ? nwr[i < kNwRegs ? i : 0] : a.norm_w[k];
+                    xr[xs_off(k, CPR)] = v[bi][i] * w;
                     ss[bi] += v[bi][i] * v[bi][i];
                     if (IN == IN_EMBED_NORM && blockIdx.x == 0 && b0 + bi < a.B && live[bi])
                         a.x_resid[(size_t)(b0 + bi) * K + k] = v[bi][i];
@@ -147,24 +199,21 @@ __device__ void prologue(const GemvArgs &a, float *xs, const float (&nwr)[kNwReg
             }
         }
     }
-    cons_sync();                                          // live[] and the rows are visible
-    if (IN == IN_PLAIN || IN == IN_SWIGLU) return;
+    if constexpr (IN == IN_NORM || IN == IN_EMBED_NORM) {
 #pragma unroll
-    for (int bi = 0; bi < NB; ++bi) {
-        if (!live[bi]) continue;                          // uniform
-        const float r = rsqrtf(cons_sum(ss[bi], sred) / (float)K + a.eps);
-        float *xr = xs + (size_t)bi * K;
-#pragma unroll
-        for (int i = 0; i < kNwRegs; ++i) {
-            const int k = tid + i * kCT;
-            if (k < K) {
-                const int o = xs_off(k, CPR);
-                xr[o] = xr[o] * r * nwr[i];
-            }
+        for (int bi = 0; bi < NB; ++bi) {
+            const float t = warp_sum(ss[bi]);
+            if ((tid & 31) == 0) sred[(tid >> 5) * NB + bi] = t;
         }
-        for (int k = tid + kNwRegs * kCT; k < K; k += kCT) {
-            const int o = xs_off(k, CPR);
-            xr[o] = xr[o] * r * a.norm_w[k];
+    }
+    cons_sync();                                          // live[], the rows and the partial sums are visible
+    if constexpr (IN == IN_NORM || IN == IN_EMBED_NORM) {
+#pragma unroll
+        for (int bi = 0; bi < NB; ++bi) {
+            float t = 0.f;
+#pragma unroll
+            for (int w = 0; w < kCW; ++w) t += sred[w * NB + bi];
+            rs[bi] = rsqrtf(t / (float)K + a.eps);
         }
     }
 }
@@ -188,7 +237,7 @@ __device__ __forceinline__ void row_out(const GemvArgs &a, int row, int b0, cons
     for (int bi = 0; bi < NB; ++bi) {
         if (!live[bi]) continue;
         const size_t o = (size_t)(b0 + bi) * a.N + row;
-        if (OUT == OUT_STORE) a.out[o] = acc[bi];
+        if (OUT == OUT_STORE || OUT == OUT_QKV_ATTN) a.out[o] = acc[bi];
         if (OUT == OUT_RESID) a.out[o] += acc[bi];
         if (OUT == OUT_ARGMAX) {
             if (a.out) a.out[o] = acc[bi];
@@ -203,7 +252,7 @@ __device__ __forceinline__ void row_out(const GemvArgs &a, int row, int b0, cons
 // Rows [row0, row0 + nr) of one stage; two rows share each activation read.
 template <int NB, int OUT>
 __device__ __forceinline__ void stage_rows(const GemvArgs &a, const uint4 *stage, int row0, int nr, int CPR, int b0,
-                                           const float *xs, const int *live, float (&best_v)[NB],
+                                           const float *xs, const float (&rs)[NB], const int *live, float (&best_v)[NB],
                                            int (&best_i)[NB]) {
     const int lane = threadIdx.x & 31, K = a.K;
     int rr = 0;
@@ -227,8 +276,8 @@ __device__ __forceinline__ void stage_rows(const GemvArgs &a, const uint4 *stage
         }
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            a0[b] = warp_sum(a0[b]);
-            a1[b] = warp_sum(a1[b]);
+            a0[b] = warp_sum(a0[b]) * rs[b];
+            a1[b] = warp_sum(a1[b]) * rs[b];
         }
         if (lane == 0) {
             row_out<NB, OUT>(a, row0 + rr, b0, live, a0, best_v, best_i);
@@ -251,7 +300,7 @@ __device__ __forceinline__ void stage_rows(const GemvArgs &a, const uint4 *stage
             }
         }
 #pragma unroll
-        for (int b = 0; b < NB; ++b) a0[b] = warp_sum(a0[b]);
+        for (int b = 0; b < NB; ++b) a0[b] = warp_sum(a0[b]) * rs[b];
         if (lane == 0) row_out<NB, OUT>(a, row0 + rr, b0, live, a0, best_v, best_i);
     }
 }
@@ -260,7 +309,7 @@ __device__ __forceinline__ void stage_rows(const GemvArgs &a, const uint4 *stage
 // warp writes silu(gate) * up per feature.
 template <int NB>
 __device__ __forceinline__ void stage_pairs(const GemvArgs &a, const uint4 *stage, int j0, int n, int CPR, int b0,
-                                            const float *xs, const int *live) {
+                                            const float *xs, const float (&rs)[NB], const int *live) {
     const int lane = threadIdx.x & 31, K = a.K;
     for (int i = 0; i < n; ++i) {
         const uint4 *wg = stage + (size_t)i * CPR, *wu = stage + (size_t)(n + i) * CPR;
@@ -282,8 +331,8 @@ __device__ __forceinline__ void stage_pairs(const GemvArgs &a, const uint4 *stag
         }
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            ag[b] = warp_sum(ag[b]);
-            au[b] = warp_sum(au[b]);
+            ag[b] = warp_sum(ag[b]) * rs[b];
+            au[b] = warp_sum(au[b]) * rs[b];
         }
         if (lane == 0) {
 #pragma unroll
@@ -296,10 +345,11 @@ __device__ __forceinline__ void stage_pairs(const GemvArgs &a, const uint4 *stag
 }  // namespace
 
 template <int NB, int IN, int OUT>
-__global__ void __launch_bounds__(kTT, 2) k_gemv_stream(GemvArgs a) {
+__global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_stream(GemvArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
     __shared__ __align__(8) uint64_t empty[kMaxStages];
+    __shared__ __align__(8) uint64_t attn_bar;
     __shared__ volatile int issued_s, abort_s;
     __shared__ int first_fail_s, any_s;
     __shared__ int live_s[kGroupB];
@@ -338,6 +388,7 @@ __global__ void __launch_bounds__(kTT, 2) k_gemv_stream(GemvArgs a) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
+        if (OUT == OUT_QKV_ATTN) ptx::mbar_init(&attn_bar, 1);
         issued_s = 0;
         abort_s = 0;
         first_fail_s = INT_MAX;
@@ -391,6 +442,9 @@ __global__ void __launch_bounds__(kTT, 2) k_gemv_stream(GemvArgs a) {
         }
     }
 
+    float rs[NB];                                         // RMSNorm scale of each row (1: no norm)
+#pragma unroll
+    for (int b = 0; b < NB; ++b) rs[b] = 1.f;
     if (warp < kCW) {
         float nwr[kNwRegs];                               // weights: no dependency either
 #pragma unroll
@@ -399,7 +453,7 @@ __global__ void __launch_bounds__(kTT, 2) k_gemv_stream(GemvArgs a) {
             nwr[i] = kNorm && k < K ? a.norm_w[k] : 0.f;
         }
         ptx::pdl_wait();
-        prologue<NB, IN>(a, xs, nwr, b0, live_s, CPR, sred);
+        prologue<NB, IN>(a, xs, nwr, b0, live_s, CPR, sred, rs);
         if (tid == 0) {
             int any = 0;
             for (int b = 0; b < NB; ++b) any |= live_s[b];
@@ -478,9 +532,9 @@ __global__ void __launch_bounds__(kTT, 2) k_gemv_stream(GemvArgs a) {
             const int row0 = r0 + j * R;
             const uint4 *stage = reinterpret_cast<const uint4 *>(smem + (size_t)slot * kStage);
             if (kPair)
-                stage_pairs<NB>(a, stage, row0, min(R, r1 - row0), CPR, b0, xs, live_s);
+                stage_pairs<NB>(a, stage, row0, min(R, r1 - row0), CPR, b0, xs, rs, live_s);
             else
-                stage_rows<NB, OUT>(a, stage, row0, min(R, r1 - row0), CPR, b0, xs, live_s, best_v, best_i);
+                stage_rows<NB, OUT>(a, stage, row0, min(R, r1 - row0), CPR, b0, xs, rs, live_s, best_v, best_i);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&empty[slot]);
         }
@@ -491,6 +545,11 @@ __global__ void __launch_bounds__(kTT, 2) k_gemv_stream(GemvArgs a) {
     if (tid == 0 && (!any || abort_s)) {
         const int first = any ? first_fail_s : 0;
         for (int g = first; g < issued_s; ++g) ptx::mbar_wait_ns(&full[g % NS], (g / NS) & 1, kWaitNs);
+    }
+    if constexpr (OUT == OUT_QKV_ATTN) {
+        // a live row whose every chunk was consumed (uniform: shared flags after the barrier)
+        if (any && !abort_s) qkv_attn_tail(a, r0, r1, smem, &attn_bar, &ticket_s);
+        return;
     }
     if (OUT != OUT_ARGMAX) return;
 
@@ -624,9 +683,28 @@ static void launch_io(GemvArgs a, int grid_x, cudaStream_t s) {
     }
 }
 
+bool gemv_stream_qkv_attn_ok(int K, int grid_x, int nq, int nkv, int d, bool kv_f16) {
+    if (d != kFD || !kv_f16 || nkv < 1 || nkv > 32 || nq != kFRep * nkv) return false;
+    const GemvPlan p = gemv_stream_plan(IN_NORM, K, 1, (nq + 2 * nkv) * d, grid_x);
+    return p.ok && p.smem >= kFusedAttnSmem;
+}
+
 bool launch_gemv_stream(int in_mode, int out_mode, const GemvArgs &a, int grid_x, cudaStream_t s) {
     const int nb = a.B < kGroupB ? a.B : kGroupB;
     if (!gemv_stream_plan(in_mode, a.K, nb, a.N, grid_x).ok) return false;
+    if (out_mode == OUT_QKV_ATTN) {
+        if (a.B != 1 || a.N != (a.at.nq + 2 * a.at.nkv) * a.at.d ||
+            !gemv_stream_qkv_attn_ok(a.K, grid_x, a.at.nq, a.at.nkv, a.at.d, true))
+            return false;
+        GemvArgs f = a;
+        const GemvPlan p = gemv_stream_plan(in_mode, a.K, 1, a.N, grid_x);
+        f.n_ring = p.n_ring;
+        f.max_units = p.max_units;
+        if (in_mode == IN_NORM) launch_nb<1, IN_NORM, OUT_QKV_ATTN>(f, dim3(grid_x, 1), p.smem, s);
+        else if (in_mode == IN_EMBED_NORM) launch_nb<1, IN_EMBED_NORM, OUT_QKV_ATTN>(f, dim3(grid_x, 1), p.smem, s);
+        else return false;
+        return true;
+    }
 #define DEC_STREAM_CASE(I, O)            \
     if (in_mode == I && out_mode == O) { \
         launch_io<I, O>(a, grid_x, s);   \
@@ -671,6 +749,8 @@ void init_gemv_stream_kernels() {
     init_io<IN_SWIGLU, OUT_RESID>();
     init_io<IN_NORM, OUT_ARGMAX>();
     init_io<IN_NORM, OUT_SWIGLU>();
+    init_nb<1, IN_NORM, OUT_QKV_ATTN>();
+    init_nb<1, IN_EMBED_NORM, OUT_QKV_ATTN>();
 }
 
 }  // namespace dec
