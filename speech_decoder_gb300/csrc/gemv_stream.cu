@@ -229,16 +229,25 @@ __device__ __forceinline__ void fma8(const float (&f)[8], const float4 &lo, cons
     acc = fmaf(f[7], hi.w, acc);
 }
 
+// OUT_RESID: the residual values of the CTA's rows [r0, r0 + n) of each
+// sequence, loaded with the activation rows (v[bi * n + row - r0]); v null
+// when the CTA holds more rows than the shared array (then read in place)
+struct Resid {
+    const float *v;
+    int r0, n;
+};
+constexpr int kResidRows = 32;
+
 // Epilogue of one finished row (lane 0 of the warp that computed it).
 template <int NB, int OUT>
-__device__ __forceinline__ void row_out(const GemvArgs &a, int row, int b0, const int *live, const float (&acc)[NB],
-                                        float (&best_v)[NB], int (&best_i)[NB]) {
+__device__ __forceinline__ void row_out(const GemvArgs &a, int row, int b0, const int *live, const Resid &rd,
+                                        const float (&acc)[NB], float (&best_v)[NB], int (&best_i)[NB]) {
 #pragma unroll
     for (int bi = 0; bi < NB; ++bi) {
         if (!live[bi]) continue;
         const size_t o = (size_t)(b0 + bi) * a.N + row;
         if (OUT == OUT_STORE || OUT == OUT_QKV_ATTN) a.out[o] = acc[bi];
-        if (OUT == OUT_RESID) a.out[o] += acc[bi];
+        if (OUT == OUT_RESID) a.out[o] = (rd.v ? rd.v[bi * rd.n + row - rd.r0] : a.out[o]) + acc[bi];
         if (OUT == OUT_ARGMAX) {
             if (a.out) a.out[o] = acc[bi];
             if (acc[bi] > best_v[bi]) {                    // rows ascend per warp: lowest index on ties
@@ -252,7 +261,8 @@ __device__ __forceinline__ void row_out(const GemvArgs &a, int row, int b0, cons
 // Rows [row0, row0 + nr) of one stage; two rows share each activation read.
 template <int NB, int OUT>
 __device__ __forceinline__ void stage_rows(const GemvArgs &a, const uint4 *stage, int row0, int nr, int CPR, int b0,
-                                           const float *xs, const float (&rs)[NB], const int *live, float (&best_v)[NB],
+                                           const float *xs, const float (&rs)[NB], const int *live, const Resid &rd,
+                                           float (&best_v)[NB],
                                            int (&best_i)[NB]) {
     const int lane = threadIdx.x & 31, K = a.K;
     int rr = 0;
@@ -280,8 +290,8 @@ __device__ __forceinline__ void stage_rows(const GemvArgs &a, const uint4 *stage
             a1[b] = warp_sum(a1[b]) * rs[b];
         }
         if (lane == 0) {
-            row_out<NB, OUT>(a, row0 + rr, b0, live, a0, best_v, best_i);
-            row_out<NB, OUT>(a, row0 + rr + 1, b0, live, a1, best_v, best_i);
+            row_out<NB, OUT>(a, row0 + rr, b0, live, rd, a0, best_v, best_i);
+            row_out<NB, OUT>(a, row0 + rr + 1, b0, live, rd, a1, best_v, best_i);
         }
     }
     if (rr < nr) {
@@ -301,7 +311,7 @@ __device__ __forceinline__ void stage_rows(const GemvArgs &a, const uint4 *stage
         }
 #pragma unroll
         for (int b = 0; b < NB; ++b) a0[b] = warp_sum(a0[b]) * rs[b];
-        if (lane == 0) row_out<NB, OUT>(a, row0 + rr, b0, live, a0, best_v, best_i);
+        if (lane == 0) row_out<NB, OUT>(a, row0 + rr, b0, live, rd, a0, best_v, best_i);
     }
 }
 
@@ -359,6 +369,7 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
     __shared__ float rv[kTT / 32];
     __shared__ int ri[kTT / 32];
     __shared__ unsigned ticket_s;
+    __shared__ float resid_s[OUT == OUT_RESID ? kGroupB * kResidRows : 1];
 
     const int NS = a.n_ring;
     const int K = a.K, CPR = K / 8;
@@ -453,7 +464,13 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
             nwr[i] = kNorm && k < K ? a.norm_w[k] : 0.f;
         }
         ptx::pdl_wait();
+        // OUT_RESID: this CTA's residual values, in flight with the activation rows
+        float rv0 = 0.f;
+        const int nres = r1 - r0;
+        const bool rpre = OUT == OUT_RESID && nres <= kResidRows && tid < NB * nres;
+        if (rpre && b0 + tid / nres < a.B) rv0 = a.out[(size_t)(b0 + tid / nres) * a.N + r0 + tid % nres];
         prologue<NB, IN>(a, xs, nwr, b0, live_s, CPR, sred, rs);
+        if (rpre) resid_s[tid] = rv0;
         if (tid == 0) {
             int any = 0;
             for (int b = 0; b < NB; ++b) any |= live_s[b];
@@ -504,6 +521,7 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
                 ptx::bulk_prefetch_l2(src + o, (uint32_t)(bytes - o < 32768 ? bytes - o : 32768));
         }
     } else if (any) {
+        const Resid rd{OUT == OUT_RESID && r1 - r0 <= kResidRows ? resid_s : nullptr, r0, r1 - r0};
         // Chunk j goes to warp j % 8.  A warp may run more than one ring lap
         // ahead of the slowest one, so before the parity wait it waits until
         // the producer has ISSUED chunk j: that happens only after chunk j - NS
@@ -534,7 +552,7 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
             if (kPair)
                 stage_pairs<NB>(a, stage, row0, min(R, r1 - row0), CPR, b0, xs, rs, live_s);
             else
-                stage_rows<NB, OUT>(a, stage, row0, min(R, r1 - row0), CPR, b0, xs, rs, live_s, best_v, best_i);
+                stage_rows<NB, OUT>(a, stage, row0, min(R, r1 - row0), CPR, b0, xs, rs, live_s, rd, best_v, best_i);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&empty[slot]);
         }
