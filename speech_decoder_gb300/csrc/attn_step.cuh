@@ -331,8 +331,9 @@ __device__ void attn_step_core(const AttnDecArgs &a, float scale, int g, int s, 
     float qv[PL], nv[PL];
     load_vec_cg<PL>(row + (size_t)(g * n_rep + (warp < n_rep ? warp : 0)) * D + lane * PL, qv);
     load_vec_cg<PL>(row + (size_t)(a.nq + (warp == 1 ? a.nkv : 0) + g) * D + lane * PL, nv);
-    if (!row_live(a.st, b)) return;
+    // the row's position and KV range load together with its liveness flags
     const int pos = a.st->n_past[b], len = pos + 1, off = a.st->kv_off[b];
+    if (!row_live(a.st, b)) return;
     int chunk, n_used;
     attn_split(len, S, chunk, n_used);
     if (s >= n_used) return;

@@ -149,8 +149,10 @@ struct SeqState {
     int32_t error;                // first device-side error code (0 = none)
 };
 
+// both flags are loaded before either is tested (one memory round trip)
 __device__ __forceinline__ bool row_live(const SeqState *st, int b) {
-    return st->active[b] && !st->done[b];
+    const int act = st->active[b], dn = st->done[b];
+    return act && !dn;
 }
 
 }  // namespace dec

@@ -126,16 +126,16 @@ __device__ void qkv_attn_tail(const GemvArgs &a, int r0, int r1, unsigned char *
 // Activation rows of this CTA's sequences into shared memory (consumer
 // threads).  The rows' loads are issued together with the liveness reads (rows
 // that turn out finished are computed and not stored).  RMSNorm inputs are
-// stored as x * w; each row's scale r = 1 / sqrt(mean(x^2) + eps) is returned
-// in rs (every thread sums the warps' partial sums itself, after the one
-// barrier that publishes the rows) and multiplies the finished dot products.
+// stored as x * w and each warp parks its partial sums of x^2 in sred; the
+// row's scale r = 1 / sqrt(mean(x^2) + eps) (row_scales, after the kernel's
+// barrier that publishes the rows) multiplies the finished dot products.
 // The norm weights were loaded into registers (nwr: this thread's first
 // kNwRegs elements) before the kernel waited on its predecessor.
 constexpr int kNwRegs = 8;                            // K = 2048 over 256 consumer threads
 
 template <int NB, int IN>
 __device__ void prologue(const GemvArgs &a, float *xs, const float (&nwr)[kNwRegs], int b0, int *live, int CPR,
-                         float *sred, float (&rs)[NB]) {
+                         float *sred) {
     const int K = a.K, tid = threadIdx.x;
     if (tid < kGroupB) live[tid] = tid < NB && b0 + tid < a.B && row_live(a.st, b0 + tid);
     if (IN == IN_EMBED_NORM) cons_sync();                 // the token ids come from the state
@@ -206,14 +206,19 @@ __device__ void prologue(const GemvArgs &a, float *xs, const float (&nwr)[kNwReg
             if ((tid & 31) == 0) sred[(tid >> 5) * NB + bi] = t;
         }
     }
-    cons_sync();                                          // live[], the rows and the partial sums are visible
+}
+
+// RMSNorm scale of each row from the consumer warps' partial sums (after the
+// barrier that publishes them)
+template <int NB, int IN>
+__device__ __forceinline__ void row_scales(const GemvArgs &a, const float *sred, float (&rs)[NB]) {
     if constexpr (IN == IN_NORM || IN == IN_EMBED_NORM) {
 #pragma unroll
         for (int bi = 0; bi < NB; ++bi) {
             float t = 0.f;
 #pragma unroll
             for (int w = 0; w < kCW; ++w) t += sred[w * NB + bi];
-            rs[bi] = rsqrtf(t / (float)K + a.eps);
+            rs[bi] = rsqrtf(t / (float)a.K + a.eps);
         }
     }
 }
@@ -361,7 +366,7 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
     __shared__ __align__(8) uint64_t empty[kMaxStages];
     __shared__ __align__(8) uint64_t attn_bar;
     __shared__ volatile int issued_s, abort_s;
-    __shared__ int first_fail_s, any_s;
+    __shared__ int first_fail_s;
     __shared__ int live_s[kGroupB];
     __shared__ float sred[32];
     __shared__ float wv[kCW * kGroupB];
@@ -469,16 +474,14 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
         const int nres = r1 - r0;
         const bool rpre = OUT == OUT_RESID && nres <= kResidRows && tid < NB * nres;
         if (rpre && b0 + tid / nres < a.B) rv0 = a.out[(size_t)(b0 + tid / nres) * a.N + r0 + tid % nres];
-        prologue<NB, IN>(a, xs, nwr, b0, live_s, CPR, sred, rs);
+        prologue<NB, IN>(a, xs, nwr, b0, live_s, CPR, sred);
         if (rpre) resid_s[tid] = rv0;
-        if (tid == 0) {
-            int any = 0;
-            for (int b = 0; b < NB; ++b) any |= live_s[b];
-            any_s = any;
-        }
     }
-    __syncthreads();
-    const bool any = any_s != 0;
+    __syncthreads();                                      // rows, partial sums, live_s, resid_s
+    bool any = false;
+#pragma unroll
+    for (int b = 0; b < NB; ++b) any |= live_s[b] != 0;
+    row_scales<NB, IN>(a, sred, rs);
 
     float best_v[NB];
     int best_i[NB];
