@@ -307,20 +307,23 @@ constexpr int attn_tile_keys() {
 
 
 // One (sequence b, kv head g, split s of S) of the step attention, run by all
-// W warps of the CTA once the step's q/k/v row is complete.  dsm holds the key
-// and value tiles (T keys each) followed by AttnSmem<D, W>; bar is an
-// initialised mbarrier whose next phase has parity (phase & 1) (phase advances
-// with every tile copied); qw, kw are this lane's Q/K norm weights.  The q/k/v
-// row is read through L2: other CTAs of the same kernel may have written it.
-// Rows that are not live and splits without keys return at once (uniformly).
-template <typename TKV, int D, int NREP, int W, int T>
+// W warps of the CTA once the step's q/k/v row is complete.  dsm holds NBUF
+// buffers of key and value tiles (T keys each) followed by AttnSmem<D, W>:
+// tile k of the split goes to buffer k % NBUF, the first NBUF tiles are
+// requested at once and each later one as soon as its buffer is consumed.
+// bar[i] is buffer i's initialised mbarrier, bit i of phase the parity of its
+// next phase; qw, kw are this lane's Q/K norm weights; splits hold at least
+// min_chunk keys.  The q/k/v row is read through L2: other CTAs of the same
+// kernel may have written it.  Rows that are not live and splits without keys
+// return at once (uniformly).
+template <typename TKV, int D, int NREP, int W, int T, int NBUF>
 __device__ void attn_step_core(const AttnDecArgs &a, float scale, int g, int s, int S, int b, unsigned char *dsm,
-                               uint64_t *bar, uint32_t &phase, const float (&qw)[D / 32], const float (&kw)[D / 32]) {
+                               uint64_t *bar, uint32_t &phase, const float (&qw)[D / 32], const float (&kw)[D / 32],
+                               int min_chunk) {
     constexpr int PL = D / 32;
     constexpr int DL = D / kLG;
-    TKV *Ks = reinterpret_cast<TKV *>(dsm);
-    TKV *Vs = Ks + (size_t)T * D;
-    AttnSmem<D, W> &sm = *reinterpret_cast<AttnSmem<D, W> *>(dsm + 2 * (size_t)T * D * sizeof(TKV));
+    TKV *Kb = reinterpret_cast<TKV *>(dsm);          // buffer i: keys at Kb + 2 i T D, values T D further
+    AttnSmem<D, W> &sm = *reinterpret_cast<AttnSmem<D, W> *>(dsm + (size_t)NBUF * 2 * T * D * sizeof(TKV));
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n_rep = NREP ? NREP : a.nq / a.nkv;
     // the step's raw q/k/v rows do not depend on the sequence state: issue
@@ -335,7 +338,7 @@ __device__ void attn_step_core(const AttnDecArgs &a, float scale, int g, int s, 
     const int pos = a.st->n_past[b], len = pos + 1, off = a.st->kv_off[b];
     if (!row_live(a.st, b)) return;
     int chunk, n_used;
-    attn_split(len, S, chunk, n_used);
+    attn_split(len, S, chunk, n_used, min_chunk);
     if (s >= n_used) return;
     const int j0 = s * chunk, j1 = min(len, j0 + chunk);
     TKV *Kc = reinterpret_cast<TKV *>(a.Kc);
@@ -352,7 +355,20 @@ __device__ void attn_step_core(const AttnDecArgs &a, float scale, int g, int s, 
             cs[e + 1] = make_float2(c.z, c.w);
         }
     }
-    __syncthreads();                                  // the barrier's previous use is over for every thread
+    __syncthreads();                                  // the buffers' previous use is over for every thread
+    // keys [t0, min(t1, pos)) of tile t0 from the pool (the new key is written from registers)
+    auto issue = [&](int t0) {
+        const int t1 = min(j1, t0 + T), ncopy = max(0, min(t1, pos) - t0);
+        if (ncopy <= 0) return;
+        const int i = ((t0 - j0) / T) % NBUF;
+        TKV *Ks = Kb + (size_t)i * 2 * T * D;
+        const uint32_t bytes = (uint32_t)(ncopy * D * sizeof(TKV));
+        ptx::mbar_expect_tx(&bar[i], 2 * bytes);
+        ptx::bulk_g2s(Ks, Kc + head_base + (size_t)t0 * D, bytes, &bar[i]);
+        ptx::bulk_g2s(Ks + (size_t)T * D, Vc + head_base + (size_t)t0 * D, bytes, &bar[i]);
+    };
+    if (tid == 0)
+        for (int k = 0; k < NBUF && j0 + k * T < j1; ++k) issue(j0 + k * T);
 
     constexpr int NR = NREP ? NREP : kMaxRep;         // running softmax state per head
     constexpr int AL = NREP ? DL : PL;                // accumulator dims per lane
@@ -370,12 +386,9 @@ __device__ void attn_step_core(const AttnDecArgs &a, float scale, int g, int s, 
     for (int t0 = j0; t0 < j1; t0 += T) {
         const int t1 = min(j1, t0 + T);
         const int ncopy = max(0, min(t1, pos) - t0);  // rows from the pool (the new key excluded)
-        if (tid == 0 && ncopy > 0) {
-            const uint32_t bytes = (uint32_t)(ncopy * D * sizeof(TKV));
-            ptx::mbar_expect_tx(bar, 2 * bytes);
-            ptx::bulk_g2s(Ks, Kc + head_base + (size_t)t0 * D, bytes, bar);
-            ptx::bulk_g2s(Vs, Vc + head_base + (size_t)t0 * D, bytes, bar);
-        }
+        const int bi = ((t0 - j0) / T) % NBUF;
+        TKV *Ks = Kb + (size_t)bi * 2 * T * D;
+        TKV *Vs = Ks + (size_t)T * D;
         if (t0 == j0) {
             for (int r = warp; r < n_rep; r += W) {          // n_rep <= W: one head per warp
                 float v[PL];
@@ -410,8 +423,8 @@ __device__ void attn_step_core(const AttnDecArgs &a, float scale, int g, int s, 
             }
         }
         if (ncopy > 0) {
-            const bool ok = ptx::mbar_wait_ns(bar, phase & 1, 200000000ull);
-            ++phase;
+            const bool ok = ptx::mbar_wait_ns(&bar[bi], (phase >> bi) & 1u, 200000000ull);
+            phase ^= 1u << bi;
             if (!ok && !failed) {
                 failed = true;
                 if (tid == 0) atomicCAS(&a.st->error, 0, 10);
@@ -476,7 +489,8 @@ __device__ void attn_step_core(const AttnDecArgs &a, float scale, int g, int s, 
                 attn_batch<PL>(sm.qs, kf, vf, jb, t1, n_rep, scale, lane, m, l, acc);
             }
         }
-        __syncthreads();                              // tile consumed before it is refilled
+        __syncthreads();                              // tile consumed before its buffer is refilled
+        if (tid == 0 && t0 + NBUF * T < j1) issue(t0 + NBUF * T);
     }
     if constexpr (NREP > 0) {
         // merge the warp's key groups (lanes with equal dims), then park the

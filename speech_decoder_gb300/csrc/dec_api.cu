@@ -168,7 +168,8 @@ static std::string validate(const dec_hparams *hp) {
 // only launch CTAs that exit at once (the step graph is captured once, so the
 // bound is the context capacity, not the current length).
 static int splits_for(const dec_handle *h, int B) {
-    const int by_ctx = (h->hp.max_ctx + kAttnMinChunk - 1) / kAttnMinChunk;
+    const int mc = attn_step_min_chunk(B);
+    const int by_ctx = (h->hp.max_ctx + mc - 1) / mc;
     return std::max(1, std::min(attn_decode_splits(B, h->hp.n_kv_heads, h->num_sms), by_ctx));
 }
 

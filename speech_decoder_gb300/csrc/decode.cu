@@ -79,28 +79,28 @@ __global__ void __launch_bounds__(attn_step_warps<SMALL, NREP>() * 32, SMALL ? 2
     k_attn_step(AttnDecArgs a, float scale) {
     constexpr int W = attn_step_warps<SMALL, NREP>();
     constexpr int PL = D / 32;
-    constexpr int T = SMALL ? attn_tile_keys<TKV, D>() / 2 : attn_tile_keys<TKV, D>();
+    constexpr int T = attn_tile_keys<TKV, D>() / 2, NBUF = SMALL ? 1 : 2;
     extern __shared__ __align__(128) unsigned char dsm[];
-    __shared__ __align__(8) uint64_t bar;
+    __shared__ __align__(8) uint64_t bar[NBUF];
     const int lane = threadIdx.x & 31;
     // Q/K norm weights: no dependency on earlier kernels
     float qw[PL], kw[PL];
     load_vec<PL>(a.qn_w + lane * PL, qw);
     load_vec<PL>(a.kn_w + lane * PL, kw);
     if (threadIdx.x == 0) {
-        ptx::mbar_init(&bar, 1);
+        for (int i = 0; i < NBUF; ++i) ptx::mbar_init(&bar[i], 1);
         ptx::fence_mbar_init();
     }
     ptx::pdl_launch();
     ptx::pdl_wait();
     uint32_t phase = 0;
-    attn_step_core<TKV, D, NREP, W, T>(a, scale, blockIdx.x, blockIdx.y, gridDim.y, blockIdx.z, dsm, &bar, phase, qw,
-                                       kw);
+    attn_step_core<TKV, D, NREP, W, T, NBUF>(a, scale, blockIdx.x, blockIdx.y, gridDim.y, blockIdx.z, dsm, bar, phase,
+                                             qw, kw, attn_step_min_chunk(SMALL ? kGroupB + 1 : 1));
 }
 
 template <typename TKV, int D, int NREP, bool SMALL>
 constexpr size_t attn_step_smem() {
-    return 2 * (size_t)(SMALL ? attn_tile_keys<TKV, D>() / 2 : attn_tile_keys<TKV, D>()) * D * sizeof(TKV) +
+    return (SMALL ? 1 : 2) * 2 * (size_t)(attn_tile_keys<TKV, D>() / 2) * D * sizeof(TKV) +
            sizeof(AttnSmem<D, attn_step_warps<SMALL, NREP>()>);
 }
 

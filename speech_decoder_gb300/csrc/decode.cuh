@@ -136,14 +136,20 @@ int gemv_default_ctas_per_sm();
 constexpr int kGemvMaxSmem = 216 * 1024;
 // split-KV partitions per (sequence, kv head)
 constexpr int kAttnMaxSplits = 32;
-// keys per split at least (short sequences run few splits)
+// keys per split at least (short sequences run few splits); the step attention
+// of at most kGroupB sequences (one CTA per SM, two key tiles in flight) takes
+// twice as many, so that contexts up to 512 keys need no split combine
 constexpr int kAttnMinChunk = 256;
+__host__ __device__ constexpr int attn_step_min_chunk(int B) {
+    return B > kGroupB ? kAttnMinChunk : 2 * kAttnMinChunk;
+}
 
-// Keys [0, len) of one (sequence, kv head) are cut into splits of `chunk` keys;
-// splits [0, n_used) hold keys.
-__host__ __device__ __forceinline__ void attn_split(int len, int S, int &chunk, int &n_used) {
+// Keys [0, len) of one (sequence, kv head) are cut into splits of `chunk` keys
+// (at least min_chunk); splits [0, n_used) hold keys.
+__host__ __device__ __forceinline__ void attn_split(int len, int S, int &chunk, int &n_used,
+                                                    int min_chunk = kAttnMinChunk) {
     chunk = (len + S - 1) / S;
-    chunk = chunk < kAttnMinChunk ? kAttnMinChunk : chunk;
+    chunk = chunk < min_chunk ? min_chunk : chunk;
     n_used = (len + chunk - 1) / chunk;
 }
 

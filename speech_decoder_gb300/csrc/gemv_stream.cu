@@ -74,8 +74,8 @@ __host__ __device__ __forceinline__ int pairs_per_stage(int K) {
 // Head dims, query heads per KV head and key tile of the fused step attention.
 constexpr int kFD = 128;
 constexpr int kFRep = 2;
-constexpr int kFT = attn_tile_keys<__half, kFD>();
-constexpr size_t kFusedAttnSmem = 2 * (size_t)kFT * kFD * sizeof(__half) + sizeof(AttnSmem<kFD, kTT / 32>);
+constexpr int kFT = attn_tile_keys<__half, kFD>() / 2, kFBuf = 2;
+constexpr size_t kFusedAttnSmem = kFBuf * 2 * (size_t)kFT * kFD * sizeof(__half) + sizeof(AttnSmem<kFD, kTT / 32>);
 
 __host__ __device__ __forceinline__ int range_overlap(int a0, int a1, int b0, int b1) {
     const int lo = a0 > b0 ? a0 : b0, hi = a1 < b1 ? a1 : b1;
@@ -88,7 +88,8 @@ __host__ __device__ __forceinline__ int range_overlap(int a0, int a1, int b0, in
 // completes the head's (kFRep + 2) * kFD rows runs its attention.  Every count
 // is added before any attention runs, so no head's completion waits behind
 // another head's attention.  Shared memory from `smem` on holds the key/value
-// tiles; bar is the tail's own mbarrier; mask is a shared word.
+// tiles; bar points to the tail's two mbarriers (one per tile buffer); mask is
+// a shared word.
 __device__ void qkv_attn_tail(const GemvArgs &a, int r0, int r1, unsigned char *smem, uint64_t *bar,
                               unsigned *mask) {
     constexpr int W = kTT / 32, PL = kFD / 32;
@@ -119,7 +120,8 @@ __device__ void qkv_attn_tail(const GemvArgs &a, int r0, int r1, unsigned char *
         // accessed by the generic proxy; the tiles arrive there by bulk copy
         ptx::fence_proxy_async_smem();
         __syncthreads();
-        attn_step_core<__half, kFD, kFRep, W, kFT>(at, a.at_scale, g, 0, 1, 0, smem, bar, phase, qw, kw);
+        attn_step_core<__half, kFD, kFRep, W, kFT, kFBuf>(at, a.at_scale, g, 0, 1, 0, smem, bar, phase, qw, kw,
+                                                         kAttnMinChunk);
     }
 }
 
@@ -364,7 +366,7 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
     __shared__ __align__(8) uint64_t empty[kMaxStages];
-    __shared__ __align__(8) uint64_t attn_bar;
+    __shared__ __align__(8) uint64_t attn_bar[2];
     __shared__ volatile int issued_s, abort_s;
     __shared__ int first_fail_s;
     __shared__ int live_s[kGroupB];
@@ -404,7 +406,10 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
-        if (OUT == OUT_QKV_ATTN) ptx::mbar_init(&attn_bar, 1);
+        if (OUT == OUT_QKV_ATTN) {
+            ptx::mbar_init(&attn_bar[0], 1);
+            ptx::mbar_init(&attn_bar[1], 1);
+        }
         issued_s = 0;
         abort_s = 0;
         first_fail_s = INT_MAX;
@@ -569,7 +574,7 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
     }
     if constexpr (OUT == OUT_QKV_ATTN) {
         // a live row whose every chunk was consumed (uniform: shared flags after the barrier)
-        if (any && !abort_s) qkv_attn_tail(a, r0, r1, smem, &attn_bar, &ticket_s);
+        if (any && !abort_s) qkv_attn_tail(a, r0, r1, smem, attn_bar, &ticket_s);
         return;
     }
     if (OUT != OUT_ARGMAX) return;
