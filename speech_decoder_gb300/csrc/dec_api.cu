@@ -112,6 +112,7 @@ struct dec_handle {
     unsigned long long *step_bar = nullptr;
     bool use_step = false;
     bool attn_fuse = false;         // single-sequence q|k|v GEMV runs the step attention (short contexts)
+    int attn_chunk = 0;             // keys per step-attention split at least (0: attn_step_min_chunk)
 };
 
 // ------------------------------------------------------------------ helpers
@@ -163,12 +164,18 @@ static std::string validate(const dec_hparams *hp) {
     return "";
 }
 
+// Keys per split of the step attention at least: attn_step_min_chunk(B), or
+// SPEECH_DECODER_ATTN_CHUNK.
+static int attn_min_chunk(const dec_handle *h, int B) {
+    return h->attn_chunk > 0 ? h->attn_chunk : attn_step_min_chunk(B);
+}
+
 // Split-KV partitions of the step attention: a split holds at least
-// kAttnMinChunk keys, so more splits than the longest context can fill would
+// attn_min_chunk keys, so more splits than the longest context can fill would
 // only launch CTAs that exit at once (the step graph is captured once, so the
 // bound is the context capacity, not the current length).
 static int splits_for(const dec_handle *h, int B) {
-    const int mc = attn_step_min_chunk(B);
+    const int mc = attn_min_chunk(h, B);
     const int by_ctx = (h->hp.max_ctx + mc - 1) / mc;
     return std::max(1, std::min(attn_decode_splits(B, h->hp.n_kv_heads, h->num_sms), by_ctx));
 }
@@ -324,6 +331,7 @@ static void enqueue_decode_layer_tc(dec_handle *h, int l, int B, bool from_embed
     a.d = hp.head_dim;
     a.B = B;
     a.append = 1;
+    a.min_chunk = attn_min_chunk(h, B);
     launch_attn_decode(h->kv_f16, a, splits_for(h, B), s);
     h->enq++;
     gemm(h, h->attn_o, h->attn_o_lo, L.wo, h->xd, H, B, H, nqd, EPI_RESID_F32);
@@ -364,6 +372,7 @@ static AttnDecArgs step_attn_args(const dec_handle *h, int l, int B) {
     a.d = hp.head_dim;
     a.B = B;
     a.append = 1;
+    a.min_chunk = attn_min_chunk(h, B);
     return a;
 }
 
@@ -1038,6 +1047,8 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
         // the 0.6B and 1.7B shapes: one 9-warp CTA per KV head over every key)
         const char *sa = std::getenv("SPEECH_DECODER_STEP_ATTN");
         h->attn_fuse = sa && !std::strcmp(sa, "fused");
+        const char *ac = std::getenv("SPEECH_DECODER_ATTN_CHUNK");
+        h->attn_chunk = ac ? std::max(0, std::min(1 << 20, std::atoi(ac))) : 0;
     }
     {
         // tensor-core prompt attention: V^T columns past a sequence's keys meet
@@ -1391,6 +1402,7 @@ dec_status dec_profile_kernel(dec_handle *h, int32_t op, int32_t iters, float *a
                 a.d = d;
                 a.B = B;
                 a.append = 0;
+                a.min_chunk = attn_min_chunk(h, B);
                 launch_attn_decode(h->kv_f16, a, splits_for(h, B), s);
                 for (int b = 0; b < B; ++b)
                     bytes += 2.0 * nkv * (double)(saved.n_past[b] + 1) * d * kvs;

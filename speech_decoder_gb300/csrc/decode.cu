@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(attn_step_warps<SMALL, NREP>() * 32, SMALL ? 2
     ptx::pdl_wait();
     uint32_t phase = 0;
     attn_step_core<TKV, D, NREP, W, T, NBUF>(a, scale, blockIdx.x, blockIdx.y, gridDim.y, blockIdx.z, dsm, bar, phase,
-                                             qw, kw, attn_step_min_chunk(SMALL ? kGroupB + 1 : 1));
+                                             qw, kw, a.min_chunk > 0 ? a.min_chunk : attn_step_min_chunk(SMALL ? kGroupB + 1 : 1));
 }
 
 template <typename TKV, int D, int NREP, bool SMALL>

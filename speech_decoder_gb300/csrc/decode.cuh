@@ -26,6 +26,7 @@ struct AttnDecArgs {
     int nq, nkv, d;
     int B;                  // sequences (grid z)
     int append;             // 1: write the row's K/V at slot n_past first
+    int min_chunk;          // step mode: keys per split at least (0: attn_step_min_chunk(B))
     // plain mode (no state, no norm/RoPE/append): q already normed and roped
     const float *q_plain;   // [B, nq, d]
     const int32_t *kv_off;  // [B] first slot of each sequence
