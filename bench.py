@@ -47,6 +47,9 @@ def parse():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--weights", choices=["bf16", "e4m3"], default="bf16",
+                   help="e4m3: the library rounds the weights row by row to 2^e * e4m3 and the single-sequence "
+                        "step GEMVs stream 1-byte codes (not the benchmark's bf16 configuration)")
     p.add_argument("--layers", type=int, default=0,
                    help="profiling only: keep the workload's shapes but run this many blocks "
                         "(the JSON line then names the reduced model and is not a benchmark value)")
@@ -136,6 +139,9 @@ class Clocks:
 
 def workload_for(args):
     wl = synth.workload(args.workload)
+    if getattr(args, "weights", "bf16") == "e4m3":
+        m = dataclasses.replace(wl.model, weight_dtype="e4m3", name=f"{wl.model.name}-e4m3")
+        wl = dataclasses.replace(wl, model=m, name=f"{wl.name}-e4m3")
     if args.layers > 0:
         m = dataclasses.replace(wl.model, n_layers=args.layers, name=f"{wl.model.name}-{args.layers}blocks")
         wl = dataclasses.replace(wl, model=m, name=f"{wl.name}-{args.layers}blocks")
@@ -172,11 +178,13 @@ def workload_inputs(wl, w):
 
 
 def decode_bytes_per_step(spec, kv_len_mean: float, batch: int = 1) -> float:
-    """Algorithmic HBM bytes of one decode step: every weight once (bf16)
-    plus the K and V rows each sequence's attention reads (fp16)."""
+    """Algorithmic HBM bytes of one decode step: every weight once (bf16; one
+    byte for the e4m3 format's single-sequence steps) plus the K and V rows
+    each sequence's attention reads (fp16)."""
     H, F, d, nq, nkv, L = spec.hidden, spec.ffn, spec.head_dim, spec.n_heads, spec.n_kv_heads, spec.n_layers
-    per_layer = ((nq + 2 * nkv) * d * H + H * nq * d + 2 * F * H + H * F) * 2
-    return L * per_layer + spec.vocab * H * 2 + batch * L * 2 * nkv * d * 2 * kv_len_mean
+    wb = 1 if spec.weight_dtype == "e4m3" and batch == 1 else 2
+    per_layer = ((nq + 2 * nkv) * d * H + H * nq * d + 2 * F * H + H * F) * wb
+    return L * per_layer + spec.vocab * H * wb + batch * L * 2 * nkv * d * 2 * kv_len_mean
 
 
 # ---------------------------------------------------------------- our arm
@@ -271,7 +279,7 @@ def run_ours(args):
     roof = {"kernel": kname, "bound": "hbm",
             "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
             "peak_source": peak_kind, "bytes_per_launch": int(kbytes), "avg_launch_us": round(kms * 1e3, 2),
-            "traffic": ncu_traffic() if B == 1 else None}
+            "traffic": ncu_traffic() if B == 1 and spec.weight_dtype == "bf16" else None}
     kv_mean = float(np.mean([t + wl.steps / 2 for t in Ts]))
     step_bytes = decode_bytes_per_step(spec, kv_mean, B)
     steps_done = n_tok / B
@@ -315,7 +323,8 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": round(decode_tok_s, 1), "unit": "tok/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 3),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if spec.weight_dtype == "bf16" else "e4m3 weights (per-row power-of-two scale), fp32 accumulate",
             "data": "synthetic (seeded random-init weights N(0,0.02), encoder rows N(0,1))",
             "config": {"workload": wl.name, "prompt_rows": T_all,
                        "layout": [[p.prefix_len, p.n_audio, p.suffix_len] for p in wl.prompts][:4],
@@ -352,7 +361,9 @@ def cpu_baseline(wl, sample_steps=3, rows=8):
     return {"value": round(sample_steps / (t2 - t1), 4), "unit": "tok/s", "cores": os.cpu_count(),
             "kind": "oracle", "prefill_tok_s": round(rows / (t1 - t0), 3),
             "sample": f"{wl.name}: prefill of the first {rows} prompt rows, then {sample_steps} greedy steps of "
-                      f"all {spec.n_layers} layers (numpy fp64, BLAS on all host cores)"}
+                      f"all {spec.n_layers} layers (numpy fp64, BLAS on all host cores"
+                      + ("; the oracle's time does not depend on the weights' rounding)"
+                         if spec.weight_dtype == "e4m3" else ")")}
 
 
 def run_reference(args):

@@ -50,7 +50,13 @@ typedef enum dec_status {
     DEC_ERR_DEVICE = 7             /* a kernel reported an error status                */
 } dec_status;
 
-typedef enum dec_dtype { DEC_BF16 = 0, DEC_F32 = 1, DEC_F16 = 2 } dec_dtype;
+/* DEC_E4M3 (weights only): the weights are passed as bf16; dec_create rounds
+ * every row of the projection matrices and of the tied embedding to
+ * 2^e * e4m3 as dec_quantize_e4m3_rows does, keeps the rounded values in bf16
+ * for the prompt path (and the embedding lookup), and the single-sequence
+ * step GEMVs stream the 1-byte codes with per-row scales.  Both paths compute
+ * with the same (rounded) weights; norm weights are not rounded. */
+typedef enum dec_dtype { DEC_BF16 = 0, DEC_F32 = 1, DEC_F16 = 2, DEC_E4M3 = 3 } dec_dtype;
 
 /* Model shape and run limits (qwen3_asr/decoder.cpp, to_block_params:
  * n_heads, n_kv_heads, head_dim, max_position, rms_eps, rope_theta). */
@@ -70,12 +76,13 @@ typedef struct dec_hparams {
     int32_t max_new;       /* generation budget; the length gate rejects a
                               prompt with T + max_new > max_ctx                 */
     int32_t eos_id;        /* end-of-stream token, -1 for none                 */
-    int32_t weight_dtype;  /* DEC_BF16 (production) or DEC_F32 (debug build)   */
-    int32_t kv_dtype;      /* DEC_F16 with BF16 weights; DEC_F32 with F32      */
+    int32_t weight_dtype;  /* DEC_BF16 (production), DEC_E4M3 (bf16 in, e4m3
+                              step weights) or DEC_F32 (debug build)           */
+    int32_t kv_dtype;      /* DEC_F16 with BF16 or E4M3 weights; DEC_F32 with F32 */
 } dec_hparams;
 
 /* Host pointers to one block's weights, each in hparams.weight_dtype (bf16
- * as raw 16-bit patterns).  Shapes: attn_norm, ffn_norm [H]; q [n_heads*d, H];
+ * as raw 16-bit patterns; bf16 for DEC_E4M3 too).  Shapes: attn_norm, ffn_norm [H]; q [n_heads*d, H];
  * k, v [n_kv_heads*d, H]; o [H, n_heads*d]; q_norm, k_norm [d] (one vector
  * shared by all heads); gate, up [F, H]; down [H, F]. */
 typedef struct dec_layer_weights {
@@ -299,6 +306,20 @@ dec_status dec_attn_decode_noalloc(const float *q, const void *K, const void *V,
  * returns after the launch. */
 dec_status dec_perception_project(const float *enc, int32_t T, int32_t d_in, const void *W, const float *bias,
                                   int32_t d_out, float *out, void *scratch, size_t scratch_bytes, void *stream);
+
+/* Per-row e4m3 rounding of bf16 weights, the DEC_E4M3 weight format (an
+ * extension of the pages' weight-streaming decode; their decoder streams
+ * bf16 or f32 weights).  Row r gets the scale 2^e_r, e_r the smallest integer
+ * with max_k |w[r][k]| <= 448 * 2^e_r (scale 1 for an all-zero row); codes[r][k]
+ * is the e4m3 value nearest w[r][k] / 2^e_r, ties to even (OCP 8-bit floating
+ * point, E4M3: exponent bias 7, 3 mantissa bits, subnormals, largest finite
+ * 448, byte = sign | exponent | mantissa); w_rounded[r][k] = value(codes[r][k])
+ * * 2^e_r, exact in bf16.  Device pointers: w bf16 [rows, cols] (raw 16-bit
+ * patterns); codes uint8 [rows, cols]; scales float32 [rows]; w_rounded bf16
+ * [rows, cols], may equal w (rounded in place).  rows >= 1, cols >= 1.  Runs
+ * on `stream` (NULL = legacy default stream); returns after the launch. */
+dec_status dec_quantize_e4m3_rows(const void *w, int64_t rows, int32_t cols, uint8_t *codes, float *scales,
+                                  void *w_rounded, void *stream);
 
 /* Standalone kernel (test hook): one prompt-row projection of the prefill,
  * C = X W^T (epi 0: store, epi 1: add into C) or, with gate|up packed in

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libdec.so")
 
 DEC_OK, DEC_ERR_INVALID_ARG, DEC_ERR_OOM, DEC_ERR_INPUT_TOO_LONG = 0, 1, 2, 3
 DEC_ERR_OUTPUT_TRUNCATED, DEC_ERR_CUDA, DEC_ERR_STATE, DEC_ERR_DEVICE = 4, 5, 6, 7
-DEC_BF16, DEC_F32, DEC_F16 = 0, 1, 2
+DEC_BF16, DEC_F32, DEC_F16, DEC_E4M3 = 0, 1, 2, 3
 
 EXPORTS = [
     "dec_workspace_size", "dec_create", "dec_destroy", "dec_reset", "dec_prefill", "dec_prefill_chunk", "dec_prefill_ids",
@@ -27,6 +27,7 @@ EXPORTS = [
     "dec_debug_logits", "dec_set_dumps", "dec_debug_dump", "dec_launch_count", "dec_last_timings",
     "dec_last_error", "dec_status_string", "dec_profile_kernel", "dec_attn_decode_scratch_size",
     "dec_attn_decode", "dec_attn_decode_noalloc", "dec_debug_gemm", "dec_perception_project",
+    "dec_quantize_e4m3_rows",
 ]
 
 
@@ -99,6 +100,7 @@ def load_library():
                             c_int32, c_int32, c_int32, c_void_p, c_size_t, c_void_p], c_int32),
         "dec_perception_project": ([c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
                                     c_size_t, c_void_p], c_int32),
+        "dec_quantize_e4m3_rows": ([c_void_p, c_int64, c_int32, c_void_p, c_void_p, c_void_p, c_void_p], c_int32),
         "dec_last_error": ([H], c_char_p),
         "dec_status_string": ([c_int32], c_char_p),
     }
@@ -117,7 +119,7 @@ def hparams_for(spec: "synth.ModelSpec", *, max_ctx: int, max_batch: int = 1, ma
         head_dim=spec.head_dim, ffn=spec.ffn, vocab=spec.vocab, rms_eps=spec.rms_eps,
         rope_theta=spec.rope_theta, max_ctx=max_ctx, max_batch=max_batch,
         max_tokens=max_tokens if max_tokens is not None else max_ctx, max_new=max_new, eos_id=eos_id,
-        weight_dtype=DEC_BF16 if spec.weight_dtype == "bf16" else DEC_F32,
+        weight_dtype={"bf16": DEC_BF16, "e4m3": DEC_E4M3, "f32": DEC_F32}[spec.weight_dtype],
         kv_dtype=DEC_F16 if spec.kv_dtype == "f16" else DEC_F32)
 
 
@@ -151,7 +153,7 @@ class Decoder:
         # a dedicated stream: the library captures CUDA graphs on it, which the
         # legacy default stream does not allow
         self.stream = torch.cuda.Stream(device=self.device)
-        bf16 = spec.weight_dtype == "bf16"
+        bf16 = spec.weight_dtype in ("bf16", "e4m3")
         keep = []
 
         def host(a):

@@ -24,6 +24,9 @@ namespace {
 
 struct DevLayer {
     void *wqkv = nullptr, *wo = nullptr, *wgu = nullptr, *wd = nullptr;
+    // DEC_E4M3: the same matrices as e4m3 codes with per-row scales
+    uint8_t *wqkv8 = nullptr, *wo8 = nullptr, *wgu8 = nullptr, *wd8 = nullptr;
+    float *wqkv_s = nullptr, *wo_s = nullptr, *wgu_s = nullptr, *wd_s = nullptr;
     float *attn_norm = nullptr, *ffn_norm = nullptr, *qn = nullptr, *kn = nullptr;
     void *K = nullptr, *V = nullptr;
 };
@@ -49,9 +52,12 @@ struct dec_handle {
     cudaStream_t stream = nullptr;
     int num_sms = 0;
     bool w_bf16 = true, kv_f16 = true, use_tc = true;
+    bool w_e4m3 = false;            // DEC_E4M3: bf16 weights rounded per row to e4m3; codes for the step GEMVs
     size_t slots = 0;
     // weights
     void *embed = nullptr;
+    uint8_t *embed8 = nullptr;      // DEC_E4M3: the lm_head as e4m3 codes
+    float *embed_s = nullptr;
     float *final_norm = nullptr;
     std::vector<DevLayer> L;
     float2 *rope = nullptr;
@@ -128,7 +134,8 @@ static dec_status fail(dec_handle *h, dec_status s, const std::string &msg) {
             return fail(h, DEC_ERR_CUDA, std::string(#call " failed: ") + cudaGetErrorString(e_)); \
     } while (0)
 
-static size_t wsize(const dec_hparams &hp) { return hp.weight_dtype == DEC_BF16 ? 2 : 4; }
+// bytes per weight as passed in and kept for the prompt path (DEC_E4M3: bf16)
+static size_t wsize(const dec_hparams &hp) { return hp.weight_dtype == DEC_F32 ? 4 : 2; }
 static size_t kvsize(const dec_hparams &hp) { return hp.kv_dtype == DEC_F16 ? 2 : 4; }
 static int qkv_rows(const dec_hparams &hp) { return (hp.n_heads + 2 * hp.n_kv_heads) * hp.head_dim; }
 
@@ -149,7 +156,7 @@ static std::string validate(const dec_hparams *hp) {
         const int qkv = (p.n_heads + 2 * p.n_kv_heads) * p.head_dim;
         const int shapes[5][2] = {{qkv, H}, {H, nqd}, {2 * F, H}, {H, F}, {p.vocab, H}};
         for (auto &nk : shapes)
-            if (!gemv_plan(nk[1], p.weight_dtype == DEC_BF16, std::min(p.max_batch, kGroupB), nk[0], 152).ok)
+            if (!gemv_plan(nk[1], p.weight_dtype != DEC_F32, std::min(p.max_batch, kGroupB), nk[0], 152).ok)
                 return "projection too large for the decode GEMV (hidden, ffn, n_heads*head_dim <= 6144)";
     }
     if (!(p.rms_eps >= 0.f) || !(p.rope_theta > 0.f)) return "rms_eps must be >= 0 and rope_theta > 0";
@@ -158,9 +165,9 @@ static std::string validate(const dec_hparams *hp) {
     if (p.max_ctx < 2 || p.max_ctx <= p.max_new) return "max_ctx must exceed max_new";
     if (p.max_tokens < 1) return "max_tokens must be >= 1";
     if (p.eos_id < -1 || p.eos_id >= p.vocab) return "eos_id must be -1 or a vocabulary id";
-    const bool ok = (p.weight_dtype == DEC_BF16 && p.kv_dtype == DEC_F16) ||
+    const bool ok = ((p.weight_dtype == DEC_BF16 || p.weight_dtype == DEC_E4M3) && p.kv_dtype == DEC_F16) ||
                     (p.weight_dtype == DEC_F32 && p.kv_dtype == DEC_F32);
-    if (!ok) return "supported formats: bf16 weights with f16 KV, or f32 weights with f32 KV";
+    if (!ok) return "supported formats: bf16 or e4m3 weights with f16 KV, or f32 weights with f32 KV";
     return "";
 }
 
@@ -199,7 +206,12 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     const size_t V = hp.vocab, Tm = hp.max_tokens, Bm = hp.max_batch;
     const size_t slots = (size_t)hp.max_batch * hp.max_ctx;
     h->slots = slots;
+    const bool e4m3 = hp.weight_dtype == DEC_E4M3;
     h->embed = b.take<char>(V * H * ws);
+    if (e4m3) {
+        h->embed8 = b.take<uint8_t>(V * H);
+        h->embed_s = b.take<float>(V);
+    }
     h->final_norm = b.take<float>(H);
     h->L.assign(hp.n_layers, DevLayer{});
     for (auto &l : h->L) {
@@ -207,6 +219,16 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
         l.wo = b.take<char>(H * nq * d * ws);
         l.wgu = b.take<char>(2 * F * H * ws);
         l.wd = b.take<char>(H * F * ws);
+        if (e4m3) {
+            l.wqkv8 = b.take<uint8_t>((size_t)qkv_rows(hp) * H);
+            l.wo8 = b.take<uint8_t>(H * nq * d);
+            l.wgu8 = b.take<uint8_t>(2 * F * H);
+            l.wd8 = b.take<uint8_t>(H * F);
+            l.wqkv_s = b.take<float>(qkv_rows(hp));
+            l.wo_s = b.take<float>(H);
+            l.wgu_s = b.take<float>(2 * F);
+            l.wd_s = b.take<float>(H);
+        }
         l.attn_norm = b.take<float>(H);
         l.ffn_norm = b.take<float>(H);
         l.qn = b.take<float>(d);
@@ -341,13 +363,27 @@ static void enqueue_decode_layer_tc(dec_handle *h, int l, int B, bool from_embed
     gemm(h, h->hbuf, h->hbuf_lo, L.wd, h->xd, H, B, H, F, EPI_RESID_F32);
 }
 
+// The matrix one step GEMV streams: e4m3 codes and row scales when the handle
+// holds them and the step has one sequence (the GEMV's e4m3 form), else the
+// bf16 (or f32) values.
+struct WSrc {
+    const void *W;
+    const float *scale;
+};
+static bool e4m3_step(const dec_handle *h, int B) { return h->w_e4m3 && B == 1 && gemv_impl() == 4; }
+static WSrc wsrc(const dec_handle *h, int B, const void *w, const uint8_t *codes, const float *scales) {
+    return e4m3_step(h, B) ? WSrc{codes, scales} : WSrc{w, nullptr};
+}
+static double wbytes(const dec_handle *h, int B) { return e4m3_step(h, B) ? 1.0 : (double)wsize(h->hp); }
+
 // The GEMV that runs next streams W [N, K]: let this one pull its first rows into L2.
-static void set_prefetch(const dec_handle *h, GemvArgs &g, const void *W, int N, int K) {
+static void set_prefetch(const dec_handle *h, GemvArgs &g, WSrc W, int N, int K) {
     if (!h->w_bf16 || h->pf_bytes <= 0) return;
-    g.pf = W;
+    g.pf = W.W;
     g.pf_N = N;
     g.pf_K = K;
     g.pf_bytes = h->pf_bytes;
+    g.pf_wb = W.scale ? 1 : 2;
 }
 
 // Step attention of layer l over the q|k|v rows in qkvd (K/V appended at n_past).
@@ -381,7 +417,8 @@ static AttnDecArgs step_attn_args(const dec_handle *h, int l, int B) {
 // head's attention (one CTA per head, all keys) and no separate attention launch.
 static bool qkv_attn_fused(const dec_handle *h, int B) {
     const dec_hparams &hp = h->hp;
-    return B == 1 && h->attn_fuse && h->w_bf16 && h->kv_f16 && gemv_impl() == 4 && hp.max_ctx <= kFusedAttnMaxCtx &&
+    return B == 1 && h->attn_fuse && h->w_bf16 && !h->w_e4m3 && h->kv_f16 && gemv_impl() == 4 &&
+           hp.max_ctx <= kFusedAttnMaxCtx &&
            gemv_stream_qkv_attn_ok(hp.hidden, gemv_grid(qkv_rows(hp), h->num_sms, h->gemv_ctas), hp.n_heads,
                                    hp.n_kv_heads, hp.head_dim, h->kv_f16);
 }
@@ -397,7 +434,9 @@ static double layer_qkv(dec_handle *h, int l, int B, bool from_embed, bool with_
     g.st = h->st;
     g.B = B;
     g.eps = hp.rms_eps;
-    g.W = L.wqkv;
+    const WSrc w = wsrc(h, B, L.wqkv, L.wqkv8, L.wqkv_s);
+    g.W = w.W;
+    g.wscale = w.scale;
     g.N = qkv_rows(hp);
     g.K = H;
     g.in = h->xd;
@@ -405,7 +444,7 @@ static double layer_qkv(dec_handle *h, int l, int B, bool from_embed, bool with_
     g.embed = h->embed;
     g.x_resid = h->xd;
     g.out = h->qkvd;
-    set_prefetch(h, g, L.wo, H, nqd);
+    set_prefetch(h, g, wsrc(h, B, L.wo, L.wo8, L.wo_s), H, nqd);
     if (h->w_bf16 && h->pf_bytes > 0) {
         g.kvp_K = L.K;
         g.kvp_V = L.V;
@@ -421,7 +460,7 @@ static double layer_qkv(dec_handle *h, int l, int B, bool from_embed, bool with_
     launch_gemv(emb ? IN_EMBED_NORM : IN_NORM, with_attn ? OUT_QKV_ATTN : OUT_STORE, h->w_bf16, g,
                 gemv_grid(g.N, h->num_sms, h->gemv_ctas), h->stream);
     h->enq++;
-    return (double)g.N * H * wsize(hp) + (double)B * (H + g.N) * 4.0;
+    return (double)g.N * H * wbytes(h, B) + (double)B * (H + g.N) * 4.0;
 }
 
 static void layer_attn(dec_handle *h, int l, int B) {
@@ -437,15 +476,17 @@ static double layer_o(dec_handle *h, int l, int B) {
     o.st = h->st;
     o.B = B;
     o.eps = hp.rms_eps;
-    o.W = L.wo;
+    const WSrc w = wsrc(h, B, L.wo, L.wo8, L.wo_s);
+    o.W = w.W;
+    o.wscale = w.scale;
     o.N = H;
     o.K = nqd;
     o.in = h->od;
     o.out = h->xd;
-    set_prefetch(h, o, L.wgu, 2 * F, H);
+    set_prefetch(h, o, wsrc(h, B, L.wgu, L.wgu8, L.wgu_s), 2 * F, H);
     launch_gemv(IN_PLAIN, OUT_RESID, h->w_bf16, o, gemv_grid(H, h->num_sms, h->gemv_ctas), h->stream);
     h->enq++;
-    return (double)H * nqd * wsize(hp) + (double)B * (nqd + 2 * H) * 4.0;
+    return (double)H * nqd * wbytes(h, B) + (double)B * (nqd + 2 * H) * 4.0;
 }
 
 // gate|up: with the producer-warp GEMV each gate row meets its up row in one
@@ -468,15 +509,17 @@ static double layer_gu(dec_handle *h, int l, int B) {
     f1.eps = hp.rms_eps;
     f1.K = H;
     f1.in = h->xd;
-    f1.W = L.wgu;
+    const WSrc w = wsrc(h, B, L.wgu, L.wgu8, L.wgu_s);
+    f1.W = w.W;
+    f1.wscale = w.scale;
     f1.N = fused ? F : 2 * F;
     f1.norm_w = L.ffn_norm;
     f1.out = h->gud;
-    set_prefetch(h, f1, L.wd, H, F);
+    set_prefetch(h, f1, wsrc(h, B, L.wd, L.wd8, L.wd_s), H, F);
     launch_gemv(IN_NORM, fused ? OUT_SWIGLU : OUT_STORE, h->w_bf16, f1, gemv_grid(2 * F, h->num_sms, h->gemv_ctas),
                 h->stream);
     h->enq++;
-    return (double)2 * F * H * wsize(hp) + (double)B * (H + f1.N) * 4.0;
+    return (double)2 * F * H * wbytes(h, B) + (double)B * (H + f1.N) * 4.0;
 }
 
 static double layer_down(dec_handle *h, int l, int B) {
@@ -487,18 +530,24 @@ static double layer_down(dec_handle *h, int l, int B) {
     GemvArgs f2{};
     f2.st = h->st;
     f2.B = B;
-    f2.W = L.wd;
+    const WSrc w = wsrc(h, B, L.wd, L.wd8, L.wd_s);
+    f2.W = w.W;
+    f2.wscale = w.scale;
     f2.N = H;
     f2.K = F;
     f2.in = h->gud;
     f2.ffn = F;
     f2.out = h->xd;
-    if (l + 1 < hp.n_layers) set_prefetch(h, f2, h->L[l + 1].wqkv, qkv_rows(hp), H);
-    else set_prefetch(h, f2, h->embed, hp.vocab, H);
+    if (l + 1 < hp.n_layers) {
+        const DevLayer &N = h->L[l + 1];
+        set_prefetch(h, f2, wsrc(h, B, N.wqkv, N.wqkv8, N.wqkv_s), qkv_rows(hp), H);
+    } else {
+        set_prefetch(h, f2, wsrc(h, B, h->embed, h->embed8, h->embed_s), hp.vocab, H);
+    }
     launch_gemv(fused ? IN_PLAIN : IN_SWIGLU, OUT_RESID, h->w_bf16, f2, gemv_grid(H, h->num_sms, h->gemv_ctas),
                 h->stream);
     h->enq++;
-    return (double)H * F * wsize(hp) + (double)B * ((fused ? 1 : 2) * F + 2 * H) * 4.0;
+    return (double)H * F * wbytes(h, B) + (double)B * ((fused ? 1 : 2) * F + 2 * H) * 4.0;
 }
 
 static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
@@ -527,7 +576,9 @@ static void enqueue_head(dec_handle *h, int B) {
     g.st = h->st;
     g.B = B;
     g.eps = h->hp.rms_eps;
-    g.W = h->embed;
+    const WSrc w = wsrc(h, B, h->embed, h->embed8, h->embed_s);
+    g.W = w.W;
+    g.wscale = w.scale;
     g.N = h->hp.vocab;
     g.K = h->hp.hidden;
     g.in = h->xd;
@@ -538,7 +589,7 @@ static void enqueue_head(dec_handle *h, int B) {
     g.counter = h->am_counter;
     g.out_ids = h->out_ids;
     g.out_ids_cap = h->hp.max_new;
-    set_prefetch(h, g, h->L[0].wqkv, qkv_rows(h->hp), h->hp.hidden);
+    set_prefetch(h, g, wsrc(h, B, h->L[0].wqkv, h->L[0].wqkv8, h->L[0].wqkv_s), qkv_rows(h->hp), h->hp.hidden);
     launch_gemv(IN_NORM, OUT_ARGMAX, h->w_bf16, g, h->lm_grid, h->stream);
     h->enq++;
 }
@@ -940,7 +991,8 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
         }
         h->own_stream = true;
     }
-    h->w_bf16 = hp->weight_dtype == DEC_BF16;
+    h->w_bf16 = hp->weight_dtype != DEC_F32;
+    h->w_e4m3 = hp->weight_dtype == DEC_E4M3;
     h->kv_f16 = hp->kv_dtype == DEC_F16;
     const char *g = std::getenv("SPEECH_DECODER_GEMM");
     h->use_tc = !(g && std::strcmp(g, "simt") == 0);
@@ -975,6 +1027,10 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
     const size_t ws = wsize(*hp), H = hp->hidden, F = hp->ffn, d = hp->head_dim;
     const size_t nq = hp->n_heads, nkv = hp->n_kv_heads;
     CKC(cudaMemcpyAsync(h->embed, w->embed, (size_t)hp->vocab * H * ws, cudaMemcpyHostToDevice, s));
+    if (h->w_e4m3) {
+        launch_quantize_e4m3_rows(h->embed, (size_t)hp->vocab, (int)H, h->embed8, h->embed_s, h->embed, s);
+        CKC(cudaGetLastError());
+    }
     std::vector<float> nbuf(std::max(H, d));
     std::vector<char> gu_host(2 * F * H * ws);
     auto put_norm = [&](float *dst, const void *src, size_t n) -> cudaError_t {
@@ -1001,6 +1057,14 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
             std::memcpy(gu_host.data() + (2 * j + 1) * blk, static_cast<const char *>(W.up) + j * blk, blk);
         }
         CKC(cudaMemcpyAsync(D.wgu, gu_host.data(), 2 * F * H * ws, cudaMemcpyHostToDevice, s));
+        if (h->w_e4m3) {
+            // rounded in place: the prompt path then computes with the same weights as the codes
+            launch_quantize_e4m3_rows(D.wqkv, qkv_rows(*hp), (int)H, D.wqkv8, D.wqkv_s, D.wqkv, s);
+            launch_quantize_e4m3_rows(D.wo, H, (int)(nq * d), D.wo8, D.wo_s, D.wo, s);
+            launch_quantize_e4m3_rows(D.wgu, 2 * F, (int)H, D.wgu8, D.wgu_s, D.wgu, s);
+            launch_quantize_e4m3_rows(D.wd, H, (int)F, D.wd8, D.wd_s, D.wd, s);
+            CKC(cudaGetLastError());
+        }
         CKC(cudaStreamSynchronize(s));
         CKC(put_norm(D.attn_norm, W.attn_norm, H));
         CKC(put_norm(D.ffn_norm, W.ffn_norm, H));
@@ -1479,6 +1543,13 @@ dec_status dec_perception_project(const float *enc, int32_t T, int32_t d_in, con
         cudaGetLastError();
         return DEC_ERR_CUDA;
     }
+    return cudaGetLastError() == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
+}
+
+dec_status dec_quantize_e4m3_rows(const void *w, int64_t rows, int32_t cols, uint8_t *codes, float *scales,
+                                  void *w_rounded, void *stream) {
+    if (!w || !codes || !scales || !w_rounded || rows < 1 || rows > INT32_MAX || cols < 1) return DEC_ERR_INVALID_ARG;
+    launch_quantize_e4m3_rows(w, (size_t)rows, cols, codes, scales, w_rounded, static_cast<cudaStream_t>(stream));
     return cudaGetLastError() == cudaSuccess ? DEC_OK : DEC_ERR_CUDA;
 }
 

@@ -37,7 +37,8 @@ struct AttnDecArgs {
 };
 
 struct GemvArgs {
-    const void *W;          // [N, K] weights (bf16 or f32)
+    const void *W;          // [N, K] weights (bf16 or f32; e4m3 codes when wscale is set)
+    const float *wscale;    // [N] scale of each e4m3 row (null: W holds bf16 or f32 values)
     int N, K;
     const float *in;        // [B, K] activations (IN_NORM, IN_PLAIN); [B, 2*ffn] gate|up (IN_SWIGLU)
     const float *norm_w;    // [K] RMSNorm weight (IN_NORM, IN_EMBED_NORM)
@@ -59,6 +60,7 @@ struct GemvArgs {
     // own rows are in flight, so HBM keeps streaming across the launch boundary
     const void *pf;
     int pf_N, pf_K, pf_bytes;
+    int pf_wb;              // bytes per weight of the next kernel's rows (0: 2, bf16)
     // KV of this layer pulled into L2 for the attention that follows (may be null)
     const void *kvp_K, *kvp_V;
     int kvp_slots, kvp_nkv, kvp_row_bytes;
@@ -130,6 +132,10 @@ bool gemv_stream_qkv_attn_ok(int K, int grid_x, int nq, int nkv, int d, bool kv_
 // (longer ones take the split-KV attention kernel)
 constexpr int kFusedAttnMaxCtx = 1024;
 void init_gemv_stream_kernels();
+// Per-row e4m3 rounding of bf16 weights [rows, cols]: codes, power-of-two row
+// scales and the rounded values in bf16 (`out` may equal `w`)
+void launch_quantize_e4m3_rows(const void *w, size_t rows, int cols, uint8_t *codes, float *scales, void *out,
+                               cudaStream_t s);
 // GEMV CTAs per SM that suit the selected implementation
 int gemv_default_ctas_per_sm();
 

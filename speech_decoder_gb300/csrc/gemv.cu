@@ -535,6 +535,7 @@ static void launch_one(const GemvArgs &a, dim3 grid, size_t smem, cudaStream_t s
 template <typename TW>
 static void launch_gemv_t(int in_mode, int out_mode, GemvArgs a, int grid_x, cudaStream_t s) {
     if (sizeof(TW) == 2 && gemv_impl() == 4 && launch_gemv_stream(in_mode, out_mode, a, grid_x, s)) return;
+    if (a.wscale) return;               // e4m3 codes: only the producer-warp GEMV reads them
     const int nb = a.B < kGroupB ? a.B : kGroupB;
     const GemvPlan p = gemv_plan(a.K, sizeof(TW) == 2, nb, a.N, grid_x);
     a.n_ring = p.n_ring;

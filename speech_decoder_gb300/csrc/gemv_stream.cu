@@ -26,6 +26,8 @@
 // for another, and the step loses one kernel boundary per layer.
 #include <climits>
 
+#include <cuda_fp8.h>
+
 #include "attn_step.cuh"
 
 namespace dec {
@@ -46,29 +48,72 @@ __device__ __forceinline__ void report(SeqState *st, int code) {
     if (st) atomicCAS(&st->error, 0, code);
 }
 
-// activation element k of a bf16 weight row lives at xs_off(k): the 8 values of
+// activation element k of a weight row with EPC weights per 16-byte chunk
+// (8 bf16 or 16 e4m3 codes) lives at xs_off<EPC>(k): the chunk's values are
+// split into float4 parts, part p of chunk c at float4 index p * CPR + c
+// (conflict-free reads).  For bf16 rows: the 8 values of
 // a 16-byte chunk are split into low/high float4 halves (conflict-free reads)
+template <int EPC>
 __device__ __forceinline__ int xs_off(int k, int CPR) {
-    const int c = k >> 3, half = (k >> 2) & 1;
-    return ((half * CPR + c) << 2) + (k & 3);
+    const int c = k / EPC, part = (k % EPC) >> 2;
+    return ((part * CPR + c) << 2) + (k & 3);
 }
 
-__host__ __device__ __forceinline__ int rows_per_stage(int K) {
-    const int rb = K * 2;
+// whole rows of rb bytes per stage
+__host__ __device__ __forceinline__ int rows_per_stage(int rb) {
     return rb >= kStage ? 1 : kStage / rb;
 }
 
 // OUT_SWIGLU: (gate, up) row pairs per stage, a power of two so that a chunk
 // that starts at a multiple of it never crosses a 128-feature block of the
 // packed gate|up layout; 0 = a pair does not fit one stage
-__host__ __device__ __forceinline__ int pairs_per_stage(int K) {
-    const int r = rows_per_stage(K) / 2;
+__host__ __device__ __forceinline__ int pairs_per_stage(int rb) {
+    const int r = rows_per_stage(rb) / 2;
     int p = 0;
     if (r >= 1) {
         p = 1;
         while (p * 2 <= r && p * 2 <= 128) p *= 2;
     }
-    return K * 2 > kStage ? 0 : p;
+    return rb > kStage ? 0 : p;
+}
+
+// The weights of one 16-byte chunk as floats: 8 bf16 values (WB = 2) or 16
+// e4m3 codes (WB = 1; byte i of the chunk is weight i).
+__device__ __forceinline__ void unpack_e4m3x16(const uint4 &u, float (&f)[16]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const __half2 h(__nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[i] >> (16 * j)), __NV_E4M3));
+            const float2 v = __half22float2(h);
+            f[4 * i + 2 * j] = v.x;
+            f[4 * i + 2 * j + 1] = v.y;
+        }
+}
+
+template <int WB>
+__device__ __forceinline__ void unpack_w(const uint4 &u, float (&f)[16 / WB]) {
+    if constexpr (WB == 2) unpack16(u, f, (const __nv_bfloat16 *)nullptr);
+    else unpack_e4m3x16(u, f);
+}
+
+// acc += the chunk's weights . its activations (Q float4 parts), in order
+template <int Q>
+__device__ __forceinline__ void fma_chunk(const float (&f)[4 * Q], const float4 (&x)[Q], float &acc) {
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
+        acc = fmaf(f[4 * q], x[q].x, acc);
+        acc = fmaf(f[4 * q + 1], x[q].y, acc);
+        acc = fmaf(f[4 * q + 2], x[q].z, acc);
+        acc = fmaf(f[4 * q + 3], x[q].w, acc);
+    }
+}
+
+template <int Q>
+__device__ __forceinline__ void load_parts(const float4 *x4, int c, int CPR, float4 (&x)[Q]) {
+#pragma unroll
+    for (int q = 0; q < Q; ++q) x[q] = x4[q * CPR + c];
 }
 
 // Head dims, query heads per KV head and key tile of the fused step attention.
@@ -135,7 +180,7 @@ __device__ void qkv_attn_tail(const GemvArgs &a, int r0, int r1, unsigned char *
 // kNwRegs elements) before the kernel waited on its predecessor.
 constexpr int kNwRegs = 8;                            // K = 2048 over 256 consumer threads
 
-template <int NB, int IN>
+template <int NB, int IN, int EPC>
 __device__ void prologue(const GemvArgs &a, float *xs, const float (&nwr)[kNwRegs], int b0, int *live, int CPR,
                          float *sred) {
     const int K = a.K, tid = threadIdx.x;
@@ -193,7 +238,7 @@ __device__ void prologue(const GemvArgs &a, float *xs, const float (&nwr)[kNwReg
                 if (k < K) {
                     float w = 1.f;
                     if (kNorm) w = k0 == tid ? nwr[i < kNwRegs ? i : 0] : a.norm_w[k];
-                    xr[xs_off(k, CPR)] = v[bi][i] * w;
+                    xr[xs_off<EPC>(k, CPR)] = v[bi][i] * w;
                     ss[bi] += v[bi][i] * v[bi][i];
                     if (IN == IN_EMBED_NORM && blockIdx.x == 0 && b0 + bi < a.B && live[bi])
                         a.x_resid[(size_t)(b0 + bi) * K + k] = v[bi][i];
@@ -223,17 +268,6 @@ __device__ __forceinline__ void row_scales(const GemvArgs &a, const float *sred,
             rs[bi] = rsqrtf(t / (float)a.K + a.eps);
         }
     }
-}
-
-__device__ __forceinline__ void fma8(const float (&f)[8], const float4 &lo, const float4 &hi, float &acc) {
-    acc = fmaf(f[0], lo.x, acc);
-    acc = fmaf(f[1], lo.y, acc);
-    acc = fmaf(f[2], lo.z, acc);
-    acc = fmaf(f[3], lo.w, acc);
-    acc = fmaf(f[4], hi.x, acc);
-    acc = fmaf(f[5], hi.y, acc);
-    acc = fmaf(f[6], hi.z, acc);
-    acc = fmaf(f[7], hi.w, acc);
 }
 
 // OUT_RESID: the residual values of the CTA's rows [r0, r0 + n) of each
@@ -266,35 +300,39 @@ __device__ __forceinline__ void row_out(const GemvArgs &a, int row, int b0, cons
 }
 
 // Rows [row0, row0 + nr) of one stage; two rows share each activation read.
-template <int NB, int OUT>
+// WB: bytes per weight (2: bf16; 1: e4m3 codes, the row's scale a.wscale[row]
+// multiplies its dot product).
+template <int NB, int OUT, int WB>
 __device__ __forceinline__ void stage_rows(const GemvArgs &a, const uint4 *stage, int row0, int nr, int CPR, int b0,
                                            const float *xs, const float (&rs)[NB], const int *live, const Resid &rd,
-                                           float (&best_v)[NB],
-                                           int (&best_i)[NB]) {
+                                           float (&best_v)[NB], int (&best_i)[NB]) {
+    constexpr int Q = 4 / WB;                      // float4 activation parts per chunk
     const int lane = threadIdx.x & 31, K = a.K;
     int rr = 0;
     for (; rr + 1 < nr; rr += 2) {
         const uint4 *w0 = stage + (size_t)rr * CPR, *w1 = w0 + CPR;
+        const float ws0 = WB == 1 ? __ldg(a.wscale + row0 + rr) : 1.f;
+        const float ws1 = WB == 1 ? __ldg(a.wscale + row0 + rr + 1) : 1.f;
         float a0[NB], a1[NB];
 #pragma unroll
         for (int b = 0; b < NB; ++b) a0[b] = a1[b] = 0.f;
 #pragma unroll 2
         for (int c = lane; c < CPR; c += 32) {
-            float f0[8], f1[8];
-            unpack16(w0[c], f0, (const __nv_bfloat16 *)nullptr);
-            unpack16(w1[c], f1, (const __nv_bfloat16 *)nullptr);
+            float f0[16 / WB], f1[16 / WB];
+            unpack_w<WB>(w0[c], f0);
+            unpack_w<WB>(w1[c], f1);
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
-                const float4 *x4 = reinterpret_cast<const float4 *>(xs + (size_t)b * K);
-                const float4 lo = x4[c], hi = x4[CPR + c];
-                fma8(f0, lo, hi, a0[b]);
-                fma8(f1, lo, hi, a1[b]);
+                float4 x[Q];
+                load_parts<Q>(reinterpret_cast<const float4 *>(xs + (size_t)b * K), c, CPR, x);
+                fma_chunk<Q>(f0, x, a0[b]);
+                fma_chunk<Q>(f1, x, a1[b]);
             }
         }
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            a0[b] = warp_sum(a0[b]) * rs[b];
-            a1[b] = warp_sum(a1[b]) * rs[b];
+            a0[b] = warp_sum(a0[b]) * rs[b] * ws0;
+            a1[b] = warp_sum(a1[b]) * rs[b] * ws1;
         }
         if (lane == 0) {
             row_out<NB, OUT>(a, row0 + rr, b0, live, rd, a0, best_v, best_i);
@@ -303,53 +341,61 @@ __device__ __forceinline__ void stage_rows(const GemvArgs &a, const uint4 *stage
     }
     if (rr < nr) {
         const uint4 *w0 = stage + (size_t)rr * CPR;
+        const float ws0 = WB == 1 ? __ldg(a.wscale + row0 + rr) : 1.f;
         float a0[NB];
 #pragma unroll
         for (int b = 0; b < NB; ++b) a0[b] = 0.f;
 #pragma unroll 4
         for (int c = lane; c < CPR; c += 32) {
-            float f0[8];
-            unpack16(w0[c], f0, (const __nv_bfloat16 *)nullptr);
+            float f0[16 / WB];
+            unpack_w<WB>(w0[c], f0);
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
-                const float4 *x4 = reinterpret_cast<const float4 *>(xs + (size_t)b * K);
-                fma8(f0, x4[c], x4[CPR + c], a0[b]);
+                float4 x[Q];
+                load_parts<Q>(reinterpret_cast<const float4 *>(xs + (size_t)b * K), c, CPR, x);
+                fma_chunk<Q>(f0, x, a0[b]);
             }
         }
 #pragma unroll
-        for (int b = 0; b < NB; ++b) a0[b] = warp_sum(a0[b]) * rs[b];
+        for (int b = 0; b < NB; ++b) a0[b] = warp_sum(a0[b]) * rs[b] * ws0;
         if (lane == 0) row_out<NB, OUT>(a, row0 + rr, b0, live, rd, a0, best_v, best_i);
     }
 }
 
 // OUT_SWIGLU: pairs [j0, j0 + n): gate rows first, then the n up rows; each
-// warp writes silu(gate) * up per feature.
-template <int NB>
+// warp writes silu(gate) * up per feature.  WB as for stage_rows (feature f's
+// gate row is (f / 128) * 256 + f % 128 of the packed matrix, its up row 128
+// further).
+template <int NB, int WB>
 __device__ __forceinline__ void stage_pairs(const GemvArgs &a, const uint4 *stage, int j0, int n, int CPR, int b0,
                                             const float *xs, const float (&rs)[NB], const int *live) {
+    constexpr int Q = 4 / WB;
     const int lane = threadIdx.x & 31, K = a.K;
     for (int i = 0; i < n; ++i) {
         const uint4 *wg = stage + (size_t)i * CPR, *wu = stage + (size_t)(n + i) * CPR;
+        const int f = j0 + i, grow = (f >> 7) * 256 + (f & 127);
+        const float wsg = WB == 1 ? __ldg(a.wscale + grow) : 1.f;
+        const float wsu = WB == 1 ? __ldg(a.wscale + grow + 128) : 1.f;
         float ag[NB], au[NB];
 #pragma unroll
         for (int b = 0; b < NB; ++b) ag[b] = au[b] = 0.f;
 #pragma unroll 2
         for (int c = lane; c < CPR; c += 32) {
-            float f0[8], f1[8];
-            unpack16(wg[c], f0, (const __nv_bfloat16 *)nullptr);
-            unpack16(wu[c], f1, (const __nv_bfloat16 *)nullptr);
+            float f0[16 / WB], f1[16 / WB];
+            unpack_w<WB>(wg[c], f0);
+            unpack_w<WB>(wu[c], f1);
 #pragma unroll
             for (int b = 0; b < NB; ++b) {
-                const float4 *x4 = reinterpret_cast<const float4 *>(xs + (size_t)b * K);
-                const float4 lo = x4[c], hi = x4[CPR + c];
-                fma8(f0, lo, hi, ag[b]);
-                fma8(f1, lo, hi, au[b]);
+                float4 x[Q];
+                load_parts<Q>(reinterpret_cast<const float4 *>(xs + (size_t)b * K), c, CPR, x);
+                fma_chunk<Q>(f0, x, ag[b]);
+                fma_chunk<Q>(f1, x, au[b]);
             }
         }
 #pragma unroll
         for (int b = 0; b < NB; ++b) {
-            ag[b] = warp_sum(ag[b]) * rs[b];
-            au[b] = warp_sum(au[b]) * rs[b];
+            ag[b] = warp_sum(ag[b]) * rs[b] * wsg;
+            au[b] = warp_sum(au[b]) * rs[b] * wsu;
         }
         if (lane == 0) {
 #pragma unroll
@@ -361,7 +407,8 @@ __device__ __forceinline__ void stage_pairs(const GemvArgs &a, const uint4 *stag
 
 }  // namespace
 
-template <int NB, int IN, int OUT>
+// WB: bytes per weight, 2 (bf16) or 1 (e4m3 codes with per-row scales a.wscale)
+template <int NB, int IN, int OUT, int WB>
 __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_stream(GemvArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ __align__(8) uint64_t full[kMaxStages];
@@ -379,12 +426,12 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
     __shared__ float resid_s[OUT == OUT_RESID ? kGroupB * kResidRows : 1];
 
     const int NS = a.n_ring;
-    const int K = a.K, CPR = K / 8;
-    const size_t rb = (size_t)K * 2;
+    const int K = a.K, CPR = K * WB / 16;             // 16-byte chunks per weight row
+    const size_t rb = (size_t)K * WB;
     // units: weight rows, or (gate, up) pairs for OUT_SWIGLU (a.N = ffn
     // features; each CTA's range starts at a multiple of R)
     constexpr bool kPair = OUT == OUT_SWIGLU;
-    const int R = kPair ? pairs_per_stage(K) : rows_per_stage(K);
+    const int R = kPair ? pairs_per_stage((int)rb) : rows_per_stage((int)rb);
     int r0, r1;
     if (kPair) {
         const long long U = (a.N + R - 1) / R;
@@ -479,7 +526,7 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
         const int nres = r1 - r0;
         const bool rpre = OUT == OUT_RESID && nres <= kResidRows && tid < NB * nres;
         if (rpre && b0 + tid / nres < a.B) rv0 = a.out[(size_t)(b0 + tid / nres) * a.N + r0 + tid % nres];
-        prologue<NB, IN>(a, xs, nwr, b0, live_s, CPR, sred);
+        prologue<NB, IN, 16 / WB>(a, xs, nwr, b0, live_s, CPR, sred);
         if (rpre) resid_s[tid] = rv0;
     }
     __syncthreads();                                      // rows, partial sums, live_s, resid_s
@@ -519,7 +566,7 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
         }
         // own rows all issued: pull this CTA's share of the next kernel's weights into L2
         if (lane == 0 && a.pf) {
-            const size_t prb = (size_t)a.pf_K * 2;
+            const size_t prb = (size_t)a.pf_K * (a.pf_wb ? a.pf_wb : 2);
             const long long p0 = (long long)a.pf_N * blockIdx.x / gridDim.x;
             const long long p1 = (long long)a.pf_N * (blockIdx.x + 1) / gridDim.x;
             size_t bytes = (size_t)(p1 - p0) * prb;
@@ -558,9 +605,10 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
             const int row0 = r0 + j * R;
             const uint4 *stage = reinterpret_cast<const uint4 *>(smem + (size_t)slot * kStage);
             if (kPair)
-                stage_pairs<NB>(a, stage, row0, min(R, r1 - row0), CPR, b0, xs, rs, live_s);
+                stage_pairs<NB, WB>(a, stage, row0, min(R, r1 - row0), CPR, b0, xs, rs, live_s);
             else
-                stage_rows<NB, OUT>(a, stage, row0, min(R, r1 - row0), CPR, b0, xs, rs, live_s, rd, best_v, best_i);
+                stage_rows<NB, OUT, WB>(a, stage, row0, min(R, r1 - row0), CPR, b0, xs, rs, live_s, rd, best_v,
+                                        best_i);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&empty[slot]);
         }
@@ -679,7 +727,7 @@ GemvPlan gemv_stream_plan(int in_mode, int K, int nb, int N, int grid_x) {
     return p;
 }
 
-template <int NB, int IN, int OUT>
+template <int NB, int IN, int OUT, int WB = 2>
 static void launch_nb(const GemvArgs &a, dim3 grid, size_t smem, cudaStream_t s) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
@@ -691,7 +739,33 @@ static void launch_nb(const GemvArgs &a, dim3 grid, size_t smem, cudaStream_t s)
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaLaunchKernelEx(&cfg, k_gemv_stream<NB, IN, OUT>, a);
+    cudaLaunchKernelEx(&cfg, k_gemv_stream<NB, IN, OUT, WB>, a);
+}
+
+// e4m3 weights (a.wscale set): one sequence, K a multiple of 16
+static bool launch_e4m3(int in_mode, int out_mode, GemvArgs a, int grid_x, cudaStream_t s) {
+    if (a.B != 1 || a.K % 16) return false;
+    const GemvPlan p = gemv_stream_plan(in_mode, a.K, 1, a.N, grid_x);
+    if (!p.ok) return false;
+    a.n_ring = p.n_ring;
+    a.max_units = p.max_units;
+    const dim3 grid(grid_x, 1);
+#define DEC_E4M3_CASE(I, O)                                 \
+    if (in_mode == I && out_mode == O) {                    \
+        launch_nb<1, I, O, 1>(a, grid, p.smem, s);           \
+        return true;                                         \
+    }
+    DEC_E4M3_CASE(IN_NORM, OUT_STORE)
+    DEC_E4M3_CASE(IN_EMBED_NORM, OUT_STORE)
+    DEC_E4M3_CASE(IN_PLAIN, OUT_RESID)
+    DEC_E4M3_CASE(IN_SWIGLU, OUT_RESID)
+    DEC_E4M3_CASE(IN_NORM, OUT_ARGMAX)
+    if (in_mode == IN_NORM && out_mode == OUT_SWIGLU && pairs_per_stage(a.K) > 0) {
+        launch_nb<1, IN_NORM, OUT_SWIGLU, 1>(a, grid, p.smem, s);
+        return true;
+    }
+#undef DEC_E4M3_CASE
+    return false;
 }
 
 template <int IN, int OUT>
@@ -716,6 +790,7 @@ bool gemv_stream_qkv_attn_ok(int K, int grid_x, int nq, int nkv, int d, bool kv_
 }
 
 bool launch_gemv_stream(int in_mode, int out_mode, const GemvArgs &a, int grid_x, cudaStream_t s) {
+    if (a.wscale) return launch_e4m3(in_mode, out_mode, a, grid_x, s);
     const int nb = a.B < kGroupB ? a.B : kGroupB;
     if (!gemv_stream_plan(in_mode, a.K, nb, a.N, grid_x).ok) return false;
     if (out_mode == OUT_QKV_ATTN) {
@@ -741,7 +816,7 @@ bool launch_gemv_stream(int in_mode, int out_mode, const GemvArgs &a, int grid_x
     DEC_STREAM_CASE(IN_PLAIN, OUT_RESID)
     DEC_STREAM_CASE(IN_SWIGLU, OUT_RESID)
     DEC_STREAM_CASE(IN_NORM, OUT_ARGMAX)
-    if (in_mode == IN_NORM && out_mode == OUT_SWIGLU && pairs_per_stage(a.K) > 0) {
+    if (in_mode == IN_NORM && out_mode == OUT_SWIGLU && pairs_per_stage(2 * a.K) > 0) {
         launch_io<IN_NORM, OUT_SWIGLU>(a, grid_x, s);
         return true;
     }
@@ -749,15 +824,15 @@ bool launch_gemv_stream(int in_mode, int out_mode, const GemvArgs &a, int grid_x
     return false;
 }
 
-template <int NB, int IN, int OUT>
+template <int NB, int IN, int OUT, int WB = 2>
 static void init_nb() {
-    auto fn = k_gemv_stream<NB, IN, OUT>;
+    auto fn = k_gemv_stream<NB, IN, OUT, WB>;
     cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvMaxSmem);
     cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
 }
 
 bool gemv_stream_swiglu_ok(int K, int nb, int ffn, int grid_x) {
-    return pairs_per_stage(K) > 0 && gemv_stream_plan(IN_NORM, K, nb, ffn, grid_x).ok;
+    return pairs_per_stage(2 * K) > 0 && gemv_stream_plan(IN_NORM, K, nb, ffn, grid_x).ok;
 }
 
 template <int IN, int OUT>
@@ -777,6 +852,12 @@ void init_gemv_stream_kernels() {
     init_io<IN_NORM, OUT_SWIGLU>();
     init_nb<1, IN_NORM, OUT_QKV_ATTN>();
     init_nb<1, IN_EMBED_NORM, OUT_QKV_ATTN>();
+    init_nb<1, IN_NORM, OUT_STORE, 1>();
+    init_nb<1, IN_EMBED_NORM, OUT_STORE, 1>();
+    init_nb<1, IN_PLAIN, OUT_RESID, 1>();
+    init_nb<1, IN_SWIGLU, OUT_RESID, 1>();
+    init_nb<1, IN_NORM, OUT_ARGMAX, 1>();
+    init_nb<1, IN_NORM, OUT_SWIGLU, 1>();
 }
 
 }  // namespace dec

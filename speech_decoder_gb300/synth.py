@@ -44,7 +44,7 @@ class ModelSpec:
     vocab: int
     rms_eps: float = 1e-6
     rope_theta: float = 1e6
-    weight_dtype: str = "bf16"      # "bf16" or "f32"
+    weight_dtype: str = "bf16"      # "bf16", "e4m3" (bf16 in; the library rounds rows to e4m3) or "f32"
     kv_dtype: str = "f16"           # "f16" or "f32"
     norm_init: str = "jitter"       # "ones" or "jitter"
     w_std: float = 0.02
@@ -153,7 +153,7 @@ def _gen(spec: ModelSpec, seed: int, layer: int, name: str) -> np.ndarray:
     else:
         a = rng.standard_normal(shape, dtype=np.float32)
         a *= np.float32(spec.w_std)
-    if spec.weight_dtype == "bf16":
+    if spec.weight_dtype in ("bf16", "e4m3"):
         round_bf16(a)
     return a
 
@@ -162,7 +162,7 @@ def model_weights(spec: ModelSpec, seed: int = 0, threads: int = 16) -> dict:
     """Random weights in the HF [out, in] layout, float32 arrays.
 
     Returns {"embed": [V,H], "final_norm": [H], "layers": [ {name: array} ]}.
-    Values are bf16-exact when spec.weight_dtype == "bf16".
+    Values are bf16-exact when spec.weight_dtype is "bf16" or "e4m3".
     """
     jobs = [(-1, "embed"), (-1, "final_norm")]
     jobs += [(l, n) for l in range(spec.n_layers) for n in _TENSORS]

@@ -20,7 +20,7 @@ def lib():
 def declared_functions():
     src = open(os.path.join(ROOT, "include", "dec.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(dec_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(dec_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_header_matches_binding_list():

@@ -42,3 +42,27 @@ def test_pins_catch_planted_mistake(tmp_path, name, old, new):
                         "tests/test_oracle_pins.py"], cwd=tmp_path, capture_output=True, text=True,
                        timeout=600)
     assert r.returncode != 0, f"planted mistake '{name}' passed every pin:\n{r.stdout[-2000:]}"
+
+
+E4M3_MUTATIONS = [
+    ("e4m3 ties away from zero", "np.round(a / step) * step", "np.floor(a / step + 0.5) * step"),
+    ("e4m3 subnormal spacing", "e = np.maximum(ex - 1, -6)", "e = np.maximum(ex - 1, -7)"),
+    ("e4m3 two mantissa bits", "step = np.ldexp(1.0, e - 3)", "step = np.ldexp(1.0, e - 2)"),
+    ("e4m3 no saturation", "q = np.minimum(np.round(a / step) * step, E4M3_MAX)", "q = np.round(a / step) * step"),
+    ("row scale not the smallest", "e = np.where(f == np.float32(0.5), x - 1, x)", "e = x"),
+    ("e4m3 exponent bias", "(1.0 + m / 8.0) * np.ldexp(1.0, e - 7)", "(1.0 + m / 8.0) * np.ldexp(1.0, e - 8)"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", E4M3_MUTATIONS, ids=[m[0] for m in E4M3_MUTATIONS])
+def test_e4m3_pins_catch_planted_mistake(tmp_path, name, old, new):
+    for d in ("oracle", "tests"):
+        shutil.copytree(os.path.join(ROOT, d), tmp_path / d,
+                        ignore=shutil.ignore_patterns("__pycache__", "golden"))
+    src = (tmp_path / "oracle" / "e4m3.py").read_text()
+    assert src.count(old) == 1, f"mutation anchor not found: {old}"
+    (tmp_path / "oracle" / "e4m3.py").write_text(src.replace(old, new))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
+                        "tests/test_e4m3_pins.py"], cwd=tmp_path, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"planted mistake '{name}' passed every pin:\n{r.stdout[-2000:]}"
+    assert " failed" in r.stdout, f"the pins did not run:\n{r.stdout[-2000:]}{r.stderr[-2000:]}"
