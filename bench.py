@@ -21,6 +21,7 @@ import csv
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -149,10 +150,15 @@ def workload_for(args):
 
 
 def kernel_sha() -> str:
+    """Hash of the sources the GEMV is compiled from, comments and whitespace
+    removed (the code, not its commentary, decides the kernel's traffic)."""
     h = hashlib.sha256()
     for f in ("gemv.cu", "gemv_stream.cu", "attn_step.cuh", "decode.cuh", "common.cuh", "ptx.cuh"):
-        with open(os.path.join(ROOT, "speech_decoder_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "speech_decoder_gb300", "csrc", f)) as fh:
+            src = fh.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 
