@@ -1,5 +1,6 @@
 // Weight-streaming GEMV of the decode step, fed by a producer warp (bf16
-// weights; one activation row per sequence, up to four sequences per CTA).
+// weights, or e4m3 codes with one power-of-two scale per row for a single
+// sequence; one activation row per sequence, up to four sequences per CTA).
 //
 // One CTA per SM owns a contiguous block of weight rows.  Its producer warp
 // copies whole rows, as many as fit a 16 KB stage, into a ring of shared-memory
@@ -19,11 +20,13 @@
 // adds into the residual, or writes logits and takes the argmax with the lowest
 // index winning ties, the last CTA advancing the greedy state.
 //
-// The q|k|v GEMV of a single sequence can finish the step attention itself:
-// each CTA counts the rows it completed of every KV head's q, k and v rows on
-// an acquire-release ticket, and the CTA that completes a head's last rows
-// runs that head's attention in its (by then idle) ring memory.  No CTA waits
-// for another, and the step loses one kernel boundary per layer.
+// Option (off by default: slower than the separate attention kernel on the
+// benchmark shapes): the q|k|v GEMV of a single sequence finishes the step
+// attention itself.  Each CTA counts the rows it completed of every KV head's
+// q, k and v rows on an acquire-release ticket, and the CTA that completes a
+// head's last rows runs that head's attention in its (by then idle) ring
+// memory.  No CTA waits for another, and the step loses one kernel boundary
+// per layer.
 #include <climits>
 
 #include <cuda_fp8.h>
