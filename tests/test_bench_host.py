@@ -1,0 +1,83 @@
+"""Host-side logic of bench.py (no GPU): the algorithmic byte count of a
+decode step, the workload options, and the hash that keys the committed ncu
+traffic record to the GEMV sources."""
+import argparse
+import os
+import shutil
+
+import pytest
+
+import bench
+from speech_decoder_gb300 import synth
+
+
+def weight_count(spec):
+    H, F, d = spec.hidden, spec.ffn, spec.head_dim
+    per_layer = (spec.n_heads + 2 * spec.n_kv_heads) * d * H + H * spec.n_heads * d + 2 * F * H + H * F
+    return spec.n_layers * per_layer + spec.vocab * H
+
+
+def test_decode_bytes_per_step_counts_every_weight_once():
+    spec = synth.QWEN3_1_7B
+    # 1.7B shape: 3.441 GB of bf16 weights per token, 114,688 B of fp16 K and V per cached token
+    assert bench.decode_bytes_per_step(spec, 0.0) == 2 * weight_count(spec)
+    assert abs(2 * weight_count(spec) / 1e9 - 3.441) < 1e-3
+    per_tok = bench.decode_bytes_per_step(spec, 1.0) - bench.decode_bytes_per_step(spec, 0.0)
+    assert per_tok == 114688
+    assert bench.decode_bytes_per_step(spec, 10.0, batch=4) - bench.decode_bytes_per_step(spec, 0.0, batch=4) \
+        == 4 * 10 * 114688
+
+
+def test_decode_bytes_e4m3_single_sequence_only():
+    import dataclasses
+    spec = dataclasses.replace(synth.QWEN3_1_7B, weight_dtype="e4m3")
+    # one sequence streams one byte per weight; batched steps take the bf16 copy
+    assert bench.decode_bytes_per_step(spec, 0.0) == weight_count(spec)
+    assert bench.decode_bytes_per_step(spec, 0.0, batch=2) == 2 * weight_count(spec)
+
+
+def _args(**kw):
+    a = argparse.Namespace(workload="qwen3-1.7b-t152", layers=0, weights="bf16")
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_workload_options():
+    wl = bench.workload_for(_args())
+    assert wl.name == "qwen3-1.7b-t152" and wl.model.weight_dtype == "bf16" and wl.model.n_layers == 28
+    wl = bench.workload_for(_args(weights="e4m3"))
+    assert wl.name == "qwen3-1.7b-t152-e4m3" and wl.model.weight_dtype == "e4m3"
+    wl = bench.workload_for(_args(layers=2))
+    assert wl.model.n_layers == 2 and wl.name.endswith("-2blocks")
+
+
+def test_kernel_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
+    csrc = os.path.join(bench.ROOT, "speech_decoder_gb300", "csrc")
+    dst = tmp_path / "speech_decoder_gb300" / "csrc"
+    shutil.copytree(csrc, dst)
+    base = bench.kernel_sha()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.kernel_sha() == base
+    f = dst / "gemv_stream.cu"
+    src = f.read_text()
+    f.write_text("// a new comment line\n" + src.replace("namespace dec {", "namespace dec {  /* inline note */", 1))
+    assert bench.kernel_sha() == base
+    f.write_text(src.replace("constexpr int kAutoStages = 12;", "constexpr int kAutoStages = 11;", 1))
+    assert "kAutoStages = 11" in f.read_text()
+    assert bench.kernel_sha() != base
+    # a record keyed to other sources is not reported
+    assert bench.ncu_traffic() is None
+
+
+def test_traffic_record_is_well_formed():
+    import json
+    with open(os.path.join(bench.ROOT, "profiles", "gemv_traffic.json")) as fh:
+        d = json.load(fh)
+    assert set(d["per_launch_bytes"]) == {"qkv", "o", "gate_up_swiglu", "down"}
+    assert d["dram_bytes_per_launch"] == pytest.approx(sum(d["per_launch_bytes"].values()) / 4, abs=1)
+    # DRAM bytes are at least the algorithmic bytes (weights are read once)
+    assert d["dram_bytes_per_launch"] >= d["algorithmic_bytes_per_launch"]
+    assert "--clock-control none" in d["command"]
+    t = bench.ncu_traffic()
+    assert t is None or t == d["dram_bytes_per_launch"]
