@@ -17,8 +17,8 @@ appear on docs.rs):
   3-way concat (prefix | enc_out | suffix), block stack, final RMSNorm,
   tied lm_head on the last position.
 * same page, build_step_graph: one token at position cur_past, KV written at
-  index cur_past, final RMSNorm, tied lm_head, argmax ("monotone-invariant",
-  no softmax).
+  index cur_past, final RMSNorm, tied lm_head, argmax of the logits directly
+  (no softmax: it would not change which logit is largest).
 * qwen3_asr/model.cpp (transcribe-cpp-sys 0.2.0), run: causal prefill mask
   (key c visible to query r iff c <= r), host argmax with strict '>' (lowest
   index wins a tie), the greedy loop (stop at EOS, at max_new generated ids
@@ -62,7 +62,8 @@ def linear(x: np.ndarray, W: np.ndarray) -> np.ndarray:
 
 
 def rope_neox(z: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
-    """NeoX rotary embedding (decoder.cpp header: "NeoX RoPE @ theta=1e6").
+    """NeoX rotary embedding (decoder.cpp, file header: NeoX-style RoPE with
+    base theta = 1e6).
 
     z: [T, heads, d]; pos: [T] absolute token positions.  For i < d/2 the
     pair (z_i, z_{i+d/2}) is rotated by the angle pos * theta^(-2i/d).
@@ -109,8 +110,9 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, q_pos: np.ndarray) ->
 
 def perception_projection(enc: np.ndarray, W: np.ndarray, bias: np.ndarray) -> np.ndarray:
     """The step just before the decoder (canary_qwen/model.cpp, forward shape:
-    "perception projection (Linear(1024, 2048) + bias)"): encoder rows enc
-    [T, d_in] to prompt rows W enc + bias, W in the [out, in] layout."""
+    the perception projection is a linear layer from 1024 to 2048 features
+    with a bias): encoder rows enc [T, d_in] to prompt rows W enc + bias, W in
+    the [out, in] layout."""
     return linear(enc, W) + _f64(bias)[None, :]
 
 
