@@ -55,7 +55,9 @@ typedef enum dec_status {
  * 2^e * e4m3 as dec_quantize_e4m3_rows does, keeps the rounded values in bf16
  * for the prompt path (and the embedding lookup), and the single-sequence
  * step GEMVs stream the 1-byte codes with per-row scales.  Both paths compute
- * with the same (rounded) weights; norm weights are not rounded. */
+ * with the same (rounded) weights; norm weights are not rounded.  The
+ * workspace (dec_workspace_size) holds both forms: one more byte per
+ * projection and embedding weight and one float per row. */
 typedef enum dec_dtype { DEC_BF16 = 0, DEC_F32 = 1, DEC_F16 = 2, DEC_E4M3 = 3 } dec_dtype;
 
 /* Model shape and run limits (qwen3_asr/decoder.cpp, to_block_params:
