@@ -206,6 +206,27 @@ dec_status dec_generate(dec_handle *h, int32_t max_new, int32_t *out_ids, int32_
 dec_status dec_generate_batch(dec_handle *h, int32_t max_new, int32_t *out_ids, int32_t *n_out,
                               int32_t *truncated);
 
+/* Generation budget of a run (moss/model.cpp of transcribe-cpp-sys 0.4.1,
+ * run and run_batch: the budget handed to the greedy loop).  The page asks
+ * for twice the audio rows plus 128 tokens (room above the plain audio-token
+ * count for the transcript's markers), takes the fixed generation reserve as
+ * the floor and the context left after the prompt as the cap; it shows the
+ * call, not the helper's body.  Reading taken here:
+ *     *budget = min(max(2 * n_audio + 128, floor_new), ceiling - T_prompt)
+ * n_audio: encoder rows injected into the prompt (>= 0); T_prompt: prompt
+ * rows (>= 1); floor_new: the generation reserve (the pages' 256; >= 1);
+ * ceiling: the context ceiling in tokens (hparams.max_ctx for this library).
+ * For a batch the page passes the longest audio and the longest prompt of
+ * the batch.  DEC_ERR_INPUT_TOO_LONG when T_prompt + floor_new > ceiling
+ * (the page's gate, checked before the budget); DEC_ERR_INVALID_ARG for a
+ * null budget pointer or an argument out of range.  Host arithmetic only:
+ * no device work.  Pass the result as max_new to dec_generate or
+ * dec_generate_batch (a decoder whose hparams.max_new is at least the
+ * budget); the loop then stops at EOS, at the budget, or when the KV range
+ * is full. */
+dec_status dec_decode_budget(int32_t n_audio, int32_t T_prompt, int32_t floor_new, int32_t ceiling,
+                             int32_t *budget);
+
 /* Copy the logits rows of the last prefill/step (one row per sequence,
  * float32 [rows, vocab]) into host memory.  rows <= sequences of that call. */
 dec_status dec_debug_logits(dec_handle *h, float *out, int32_t rows);
@@ -287,9 +308,14 @@ dec_status dec_attn_decode(const float *q, const void *K, const void *V, int32_t
  * cudaFree or allocating library routine); it zeroes the counters with
  * cudaMemsetAsync on `stream`.  The first call on a device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current;
- * make that first call before any stream capture.  Every call shares the one
- * array, so calls that overlap on the GPU (other streams, other threads) race
- * and corrupt each other's results: serialise them. */
+ * make that first call before any stream capture.  That address is kept for
+ * the life of the process: after cudaDeviceReset, or once the device's
+ * primary context was destroyed and created again, the kept address is stale,
+ * so do not call this entry point on that device again.  Every call shares
+ * the one array, so calls that overlap on the GPU (other streams, other
+ * threads) race and corrupt each other's results: serialise them.  The
+ * scratch a shape needs is dec_attn_decode_scratch_size(); for 8 KV heads of
+ * 2 query heads each and head_dim 128 the array holds up to 502 sequences. */
 dec_status dec_attn_decode_noalloc(const float *q, const void *K, const void *V, int32_t kv_dtype,
                                    int32_t slots, const int32_t *kv_off, const int32_t *kv_len,
                                    int32_t B, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim,

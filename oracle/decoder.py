@@ -217,6 +217,29 @@ class Oracle:
         return self.head(x[0])
 
 
+def decode_budget(n_audio: int, T_prompt: int, ceiling: int, floor_new: int = 256) -> int:
+    """Generation budget of one run (moss/model.cpp of transcribe-cpp-sys
+    0.4.1, run: the budget passed to the greedy loop; run_batch takes the
+    same call with the batch's longest audio and longest prompt).
+
+    The page first rejects a prompt whose rows plus the fixed 256-token
+    generation reserve exceed the context ceiling, then asks for twice the
+    audio rows plus 128 tokens (room above the plain audio-token count for
+    the transcript's markers), with the 256-token reserve as the floor and the
+    context left after the prompt as the cap.  The helper's body is not on
+    the page; the reading taken is the plain clamp
+    min(max(2 n_audio + 128, floor_new), ceiling - T_prompt).
+    Raises ValueError where the page returns its input-too-long status.
+    """
+    n_audio, T_prompt, ceiling, floor_new = int(n_audio), int(T_prompt), int(ceiling), int(floor_new)
+    if n_audio < 0 or T_prompt < 1 or floor_new < 1 or ceiling < 1:
+        raise ValueError("invalid argument")
+    if T_prompt + floor_new > ceiling:
+        raise ValueError("input too long")
+    want = 2 * n_audio + 128
+    return min(max(want, floor_new), ceiling - T_prompt)
+
+
 def greedy(oracle: Oracle, embeds: np.ndarray, max_new: int, eos_id: int = -1,
            keep_logits: bool = False):
     """The greedy loop of qwen3_asr/model.cpp, run.

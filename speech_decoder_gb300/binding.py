@@ -27,7 +27,7 @@ EXPORTS = [
     "dec_debug_logits", "dec_set_dumps", "dec_debug_dump", "dec_launch_count", "dec_last_timings",
     "dec_last_error", "dec_status_string", "dec_profile_kernel", "dec_attn_decode_scratch_size",
     "dec_attn_decode", "dec_attn_decode_noalloc", "dec_debug_gemm", "dec_perception_project",
-    "dec_quantize_e4m3_rows",
+    "dec_quantize_e4m3_rows", "dec_decode_budget",
 ]
 
 
@@ -101,6 +101,7 @@ def load_library():
         "dec_perception_project": ([c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_int32, c_void_p, c_void_p,
                                     c_size_t, c_void_p], c_int32),
         "dec_quantize_e4m3_rows": ([c_void_p, c_int64, c_int32, c_void_p, c_void_p, c_void_p, c_void_p], c_int32),
+        "dec_decode_budget": ([c_int32, c_int32, c_int32, c_int32, POINTER(c_int32)], c_int32),
         "dec_last_error": ([H], c_char_p),
         "dec_status_string": ([c_int32], c_char_p),
     }
@@ -134,6 +135,16 @@ def workspace_size(hp: dec_hparams) -> int:
 
 def _host_f32(a) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def decode_budget(n_audio: int, T_prompt: int, ceiling: int, floor_new: int = 256) -> int:
+    """dec_decode_budget: the generation budget of a run (raises DecError)."""
+    lib = load_library()
+    out = c_int32()
+    st = lib.dec_decode_budget(int(n_audio), int(T_prompt), int(floor_new), int(ceiling), byref(out))
+    if st != DEC_OK:
+        raise DecError(st, lib.dec_status_string(st).decode())
+    return out.value
 
 
 class Decoder:

@@ -1353,6 +1353,16 @@ dec_status dec_generate_batch(dec_handle *h, int32_t max_new, int32_t *out_ids, 
     return DEC_OK;
 }
 
+dec_status dec_decode_budget(int32_t n_audio, int32_t T_prompt, int32_t floor_new, int32_t ceiling,
+                             int32_t *budget) {
+    if (!budget || n_audio < 0 || T_prompt < 1 || floor_new < 1 || ceiling < 1) return DEC_ERR_INVALID_ARG;
+    if ((int64_t)T_prompt + floor_new > (int64_t)ceiling) return DEC_ERR_INPUT_TOO_LONG;
+    const int64_t asked = 2 * (int64_t)n_audio + 128;
+    const int64_t room = (int64_t)ceiling - T_prompt;
+    *budget = (int32_t)std::min(std::max(asked, (int64_t)floor_new), room);
+    return DEC_OK;
+}
+
 dec_status dec_debug_logits(dec_handle *h, float *out, int32_t rows) {
     if (!h || !out || rows < 1) return fail(h, DEC_ERR_INVALID_ARG, "bad arguments");
     if (rows > h->logits_rows) return fail(h, DEC_ERR_STATE, "fewer logits rows available");

@@ -62,3 +62,25 @@ def test_null_arguments_rejected(lib):
     assert lib.dec_workspace_size(None, None) == binding.DEC_ERR_INVALID_ARG
     assert lib.dec_reset(None) == binding.DEC_ERR_INVALID_ARG
     assert lib.dec_step(None, 0, None) == binding.DEC_ERR_INVALID_ARG
+
+
+def test_decode_budget_matches_oracle_reading(lib):
+    """dec_decode_budget is host arithmetic: compare it with the oracle's
+    reading of the page's budget on a grid, and its status codes with the
+    oracle's rejections."""
+    import oracle as O
+    out = ctypes.c_int32()
+    for ceiling in (600, 4096, 8271, 40960):
+        for n_audio in range(0, 9000, 97):
+            for extra in (1, 15, 300):
+                T = n_audio + extra
+                st = lib.dec_decode_budget(n_audio, T, 256, ceiling, ctypes.byref(out))
+                try:
+                    want = O.decode_budget(n_audio, T, ceiling)
+                except ValueError:
+                    assert st == binding.DEC_ERR_INPUT_TOO_LONG, (n_audio, T, ceiling)
+                    continue
+                assert st == binding.DEC_OK and out.value == want, (n_audio, T, ceiling)
+    assert lib.dec_decode_budget(-1, 10, 256, 1000, ctypes.byref(out)) == binding.DEC_ERR_INVALID_ARG
+    assert lib.dec_decode_budget(10, 0, 256, 1000, ctypes.byref(out)) == binding.DEC_ERR_INVALID_ARG
+    assert lib.dec_decode_budget(10, 20, 256, 1000, None) == binding.DEC_ERR_INVALID_ARG

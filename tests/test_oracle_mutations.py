@@ -27,6 +27,9 @@ MUTATIONS = [
      'x = linear(o.reshape(T, nq * d), W["o"])'),
     ("argmax picks last tie", "np.flatnonzero(v == np.max(v))[0]", "np.flatnonzero(v == np.max(v))[-1]"),
     ("transposed weight", "return _f64(x) @ _f64(W).T", "return _f64(x) @ _f64(W).reshape(_f64(W).shape[::-1])"),
+    ("budget slack dropped", "want = 2 * n_audio + 128", "want = 2 * n_audio"),
+    ("budget floor ignored", "min(max(want, floor_new), ceiling - T_prompt)", "min(want, ceiling - T_prompt)"),
+    ("budget cap ignored", "min(max(want, floor_new), ceiling - T_prompt)", "max(want, floor_new)"),
 ]
 
 

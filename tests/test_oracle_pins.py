@@ -417,6 +417,36 @@ def test_greedy_eos_first_token():
     assert ids == [] and not trunc
 
 
+# ------------------------------------------------------------------ decode budget
+# moss/model.cpp (transcribe-cpp-sys 0.4.1), run: the budget asked for is twice
+# the audio rows plus 128, the 256-token generation reserve is the floor, the
+# context left after the prompt the cap; a prompt that cannot take the reserve
+# is rejected before.  Values worked by hand from that reading.
+@pytest.mark.parametrize("n_audio,T,ceiling,want", [
+    (138, 152, 8192, 404),        # the JFK prompt: 2 * 138 + 128 = 404 (above the floor, far below the cap)
+    (50, 65, 8192, 256),          # 2 * 50 + 128 = 228 < 256: the reserve is the floor
+    (64, 79, 8192, 256),          # 2 * 64 + 128 = 256 exactly
+    (65, 80, 8192, 258),          # one audio row above that: two more tokens
+    (4000, 4015, 8192, 4177),     # 8128 asked, 8192 - 4015 = 4177 left: the cap
+    (8000, 8015, 8271, 256),      # cap = 256 = the floor: the gate's boundary case
+])
+def test_decode_budget_worked_values(n_audio, T, ceiling, want):
+    assert O.decode_budget(n_audio, T, ceiling) == want
+
+
+def test_decode_budget_gate_and_invariants():
+    with pytest.raises(ValueError):
+        O.decode_budget(8000, 8015, 8270)        # 8015 + 256 > 8270: input too long
+    with pytest.raises(ValueError):
+        O.decode_budget(-1, 10, 1000)
+    for n in range(0, 3000, 7):
+        T = n + 15
+        b = O.decode_budget(n, T, 4096)
+        assert 256 <= b and T + b <= 4096
+        # more audio never lowers the budget for the same prompt length
+        assert O.decode_budget(n + 1, T, 4096) >= b
+
+
 # ------------------------------------------------------------------ synth
 def test_round_bf16_ties_to_even_and_exact():
     a = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5, 1.0 + 2 ** -9], np.float32)
