@@ -47,6 +47,9 @@ def parse():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-long-prefill", action="store_true",
+                   help="skip the timed 8015-row prompt of the same model")
+    p.add_argument("--cpu-sample", type=int, default=0, help=argparse.SUPPRESS)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--weights", choices=["bf16", "e4m3"], default="bf16",
                    help="e4m3: the library rounds the weights row by row to 2^e * e4m3 and the single-sequence "
@@ -193,6 +196,46 @@ def decode_bytes_per_step(spec, kv_len_mean: float, batch: int = 1) -> float:
     return L * per_layer + spec.vocab * H * wb + batch * L * 2 * nkv * d * 2 * kv_len_mean
 
 
+def prefill_work(spec, Ts) -> tuple:
+    """Algorithmic work of one prefill of the prompts Ts (one sequence each):
+    (FLOPs, HBM bytes).
+
+    FLOPs follow the method as this library runs it: every block but the
+    last takes all prompt rows (2 T N K per projection, 4 nq d T (T + 1) / 2
+    for the causal attention); the last block writes every row's keys and
+    values (its q|k|v projection on all rows) and runs the attention query,
+    o projection and FFN on the last row only (slice_last), and the tied
+    lm_head runs on that row.  Bytes: every weight once (the prompt is one
+    pass over the model) plus the fp16 K/V rows written and the fp32 prompt
+    rows read."""
+    H, F, d, nq, nkv, L, V = (spec.hidden, spec.ffn, spec.head_dim, spec.n_heads, spec.n_kv_heads,
+                              spec.n_layers, spec.vocab)
+    qkv_n = (nq + 2 * nkv) * d
+    rest = H * nq * d + 2 * F * H + H * F             # o, gate|up, down weights
+    flops = 0.0
+    for T in Ts:
+        flops += 2.0 * T * (qkv_n * H + rest) * (L - 1) + 4.0 * nq * d * T * (T + 1) / 2 * (L - 1)
+        flops += 2.0 * T * qkv_n * H + 2.0 * rest + 4.0 * nq * d * T
+        flops += 2.0 * V * H
+    wbytes = L * (qkv_n * H + rest) * 2 + V * H * 2
+    nbytes = wbytes + sum(Ts) * (L * 2 * nkv * d * 2 + H * 4)
+    return flops, float(nbytes)
+
+
+def prefill_roofline(spec, Ts, ms, hbm, tc_peak) -> dict:
+    """Achieved rates of one prefill against both ceilings; `bound` names
+    the one the arithmetic intensity selects (FLOPs per byte below the ridge
+    tc_peak / hbm: HBM)."""
+    flops, nbytes = prefill_work(spec, Ts)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    tfs = flops / (ms / 1e3) / 1e12
+    bound = "hbm" if flops / nbytes < tc_peak * 1e12 / (hbm * 1e9) else "tensor"
+    return {"bound": bound, "flops": flops, "bytes": int(nbytes),
+            "achieved_gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4),
+            "achieved_tflops": round(tfs, 2), "tc_frac": round(tfs / tc_peak, 4),
+            "frac": round(gbs / hbm if bound == "hbm" else tfs / tc_peak, 4)}
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args):
     import torch
@@ -321,9 +364,16 @@ def run_ours(args):
                "h2d_bytes_per_step": int(ids_h.numel() * 4 + audio_h.numel() * 4),
                "d2h_bytes_per_step": int(B * (4 + 4 * max_new))}
 
+    pre_roof = prefill_roofline(spec, Ts, pre_ms / args.steps, hbm, bf16_peak)
+    pre_roof["peak_gbs"], pre_roof["peak_tflops"], pre_roof["peak_source"] = hbm, bf16_peak, peak_kind
+
+    long = None
+    if B == 1 and not args.no_long_prefill and args.layers == 0:
+        long = long_prefill(args, hbm, bf16_peak, peak_kind, dev)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, sample_steps=3)
+        cpu = cpu_baseline(wl)
 
     if rank == 0:
         line = {
@@ -336,7 +386,9 @@ def run_ours(args):
                        "layout": [[p.prefix_len, p.n_audio, p.suffix_len] for p in wl.prompts][:4],
                        "decode_steps": wl.steps, "batch": wl.batch, "parallelism": f"replicas x{world}",
                        "l2": "inputs larger than L2: every step streams 3.4 GB of weights"},
-            "prefill": {"value": round(prefill_tok_s, 1), "unit": "tok/s", "ms": round(pre_ms / args.steps, 3)},
+            "prefill": {"value": round(prefill_tok_s, 1), "unit": "tok/s", "ms": round(pre_ms / args.steps, 3),
+                        "roofline": pre_roof},
+            "prefill_long": long,
             "decode_ms_per_step": round(step_ms, 4),
             "roofline": roof, "step_roofline": step_roof, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clk, "gpu_launches": int(launches),
@@ -346,30 +398,96 @@ def run_ours(args):
         torch.distributed.destroy_process_group()
 
 
+# ---------------------------------------------------------------- long prompt
+LONG_WORKLOAD = "qwen3-1.7b-t8015"
+
+
+def long_prefill(args, hbm, bf16_peak, peak_kind, dev, reps=3):
+    """The tensor-core-bound prefill: the 8015-row prompt (9 | 8000 encoder
+    rows | 6) of the same model, timed with CUDA events on the decoder's
+    stream (prefill only; one untimed warm-up)."""
+    import torch
+    from speech_decoder_gb300.binding import Decoder
+    lw = synth.workload(LONG_WORKLOAD)
+    spec = lw.model
+    if args.weights == "e4m3":
+        spec = dataclasses.replace(spec, weight_dtype="e4m3", name=f"{spec.name}-e4m3")
+    pr = lw.prompts[0]
+    w = synth.model_weights(spec, seed=lw.seed)
+    it = synth.prompt_inputs(spec, pr, seed=lw.seed, item=0)
+    dec = Decoder(spec, w, max_ctx=pr.T + lw.steps + 1, max_batch=1, max_tokens=pr.T, max_new=lw.steps + 1,
+                  device=dev)
+    del w
+    ids = torch.from_numpy(np.asarray(it["ids"], np.int32)).to(dev)
+    audio = torch.from_numpy(np.asarray(it["audio"], np.float32)).to(dev)
+    dec.prefill_ids(ids, audio, int(it["prefix_len"]))
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(dec.stream)
+    for _ in range(reps):
+        dec.prefill_ids(ids, audio, int(it["prefix_len"]))
+    e1.record(dec.stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    dec.close()
+    del dec
+    torch.cuda.empty_cache()
+    roof = prefill_roofline(spec, [pr.T], ms, hbm, bf16_peak)
+    roof["peak_gbs"], roof["peak_tflops"], roof["peak_source"] = hbm, bf16_peak, peak_kind
+    return {"workload": lw.name, "prompt_rows": pr.T, "reps": reps, "ms": round(ms, 3),
+            "value": round(pr.T / (ms / 1e3), 1), "unit": "tok/s", "roofline": roof}
+
+
 # ---------------------------------------------------------------- oracle timings
-def cpu_baseline(wl, sample_steps=3, rows=8):
-    """The fp64 oracle, as it stands, on a bounded sample of the workload:
-    a prefill of the first `rows` prompt rows, then `sample_steps` greedy
-    steps of the full model.  Decode tok/s = steps / their time."""
+def oracle_sample(wl, rows: int, steps: int) -> dict:
+    """The fp64 oracle, as it stands: a prefill of the first `rows` prompt
+    rows of item 0, then `steps` greedy steps of the full model."""
     import oracle as O
     spec = wl.model
     w = synth.model_weights(spec, seed=wl.seed)
     item = synth.prompt_inputs(spec, wl.prompts[0], seed=wl.seed, item=0)
     emb = O.assemble_prompt(w["embed"], item["ids"], item["audio"], item["prefix_len"])[:rows]
-    orc = O.Oracle(spec, w, rows + sample_steps + 1)
+    orc = O.Oracle(spec, w, rows + steps + 1)
     t0 = time.perf_counter()
     logits = orc.prefill(emb)
     t1 = time.perf_counter()
     tok = O.argmax_lowest(logits)
-    for _ in range(sample_steps):
+    for _ in range(steps):
         tok = O.argmax_lowest(orc.step(tok))
     t2 = time.perf_counter()
-    return {"value": round(sample_steps / (t2 - t1), 4), "unit": "tok/s", "cores": os.cpu_count(),
-            "kind": "oracle", "prefill_tok_s": round(rows / (t1 - t0), 3),
-            "sample": f"{wl.name}: prefill of the first {rows} prompt rows, then {sample_steps} greedy steps of "
-                      f"all {spec.n_layers} layers (numpy fp64, BLAS on all host cores"
-                      + ("; the oracle's time does not depend on the weights' rounding)"
-                         if spec.weight_dtype == "e4m3" else ")")}
+    return {"value": round(steps / (t2 - t1), 4), "prefill_tok_s": round(rows / (t1 - t0), 3),
+            "rows": rows, "steps": steps}
+
+
+def _sample_in_child(wl, threads: int, rows: int, steps: int) -> dict:
+    """oracle_sample in a child process whose BLAS runs on `threads` threads."""
+    env = dict(os.environ)
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[k] = str(threads)
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-sample", str(threads), "--workload", wl.name,
+           "--steps", str(steps), "--warmup", str(rows), "--weights", "bf16"]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle sample failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(wl) -> dict:
+    """The oracle timed on the host cores, as a reported baseline: on every
+    core, the whole prompt's prefill and 3 greedy steps; on one thread, an
+    8-row prefill and 1 step (bounded samples of the same workload)."""
+    cores = os.cpu_count() or 1
+    T0 = wl.prompts[0].T
+    allc = _sample_in_child(wl, cores, T0, 3)
+    one = _sample_in_child(wl, 1, 8, 1)
+    note = "; the oracle's time does not depend on the weights' rounding" if wl.model.weight_dtype == "e4m3" else ""
+    return {"value": allc["value"], "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "prefill_tok_s": allc["prefill_tok_s"],
+            "sample": f"{wl.name}: prefill of the whole {T0}-row prompt, then 3 greedy steps of all "
+                      f"{wl.model.n_layers} layers (numpy fp64, BLAS on {cores} threads{note})",
+            "one_thread": {"value": one["value"], "unit": "tok/s", "cores": 1, "prefill_tok_s": one["prefill_tok_s"],
+                           "sample": f"{wl.name}: prefill of the first 8 prompt rows, then 1 greedy step "
+                                     f"(numpy fp64, BLAS on 1 thread)"}}
 
 
 def run_reference(args):
@@ -407,7 +525,10 @@ def run_reference(args):
 
 if __name__ == "__main__":
     a = parse()
-    if a.impl == "reference":
+    if a.cpu_sample:
+        # child of cpu_baseline: --warmup carries the prefill rows, --steps the greedy steps
+        print(json.dumps(oracle_sample(workload_for(a), a.warmup, a.steps)), flush=True)
+    elif a.impl == "reference":
         run_reference(a)
     else:
         run_ours(a)

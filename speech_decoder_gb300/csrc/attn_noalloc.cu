@@ -15,9 +15,12 @@
 namespace {
 
 // 4 MiB of device memory, reserved on every GPU that loads the library and
-// held until the process exits.  Enough for B * n_kv_heads * splits partial
-// rows of up to 8 query heads of head_dim 128 (about 600 rows at full split
-// width, which covers up to 64 sequences of 8 KV heads).
+// held until the process exits.  A call needs B * n_kv_heads * splits *
+// n_rep * (head_dim + 2) floats of partials plus B * n_kv_heads counters,
+// each rounded up to 256 bytes (attn_op_scratch_bytes); the split count
+// falls to 1 once B * n_kv_heads reaches twice the SM count.  For the 1.7B
+// shape (8 KV heads, 2 query heads each, head_dim 128) that admits up to 502
+// sequences.
 constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;
 __device__ __align__(256) unsigned char g_attn_scratch[kNoAllocScratchBytes];
 

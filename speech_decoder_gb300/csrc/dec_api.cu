@@ -118,6 +118,7 @@ struct dec_handle {
     unsigned long long *step_bar = nullptr;
     bool use_step = false;
     bool attn_fuse = false;         // single-sequence q|k|v GEMV runs the step attention (short contexts)
+    bool attn_split_kernel = false; // step attention always on the split-KV kernel (no cluster kernel)
     int attn_chunk = 0;             // keys per step-attention split at least (0: attn_step_min_chunk)
 };
 
@@ -463,8 +464,21 @@ static double layer_qkv(dec_handle *h, int l, int B, bool from_embed, bool with_
     return (double)g.N * H * wbytes(h, B) + (double)B * (H + g.N) * 4.0;
 }
 
+// Cluster size of the step attention for B sequences (0: the split-KV kernel).
+static int cluster_splits(const dec_handle *h, int B) {
+    if (h->attn_split_kernel) return 0;
+    const dec_hparams &hp = h->hp;
+    return attn_cluster_splits(hp.max_ctx, hp.n_heads, hp.n_kv_heads, hp.head_dim, h->kv_f16, B);
+}
+
 static void layer_attn(dec_handle *h, int l, int B) {
-    launch_attn_decode(h->kv_f16, step_attn_args(h, l, B), splits_for(h, B), h->stream);
+    AttnDecArgs a = step_attn_args(h, l, B);
+    const int S = cluster_splits(h, B);
+    if (S > 0 && launch_attn_cluster(a, S, h->stream) == cudaSuccess) {
+        h->enq++;
+        return;
+    }
+    launch_attn_decode(h->kv_f16, a, splits_for(h, B), h->stream);
     h->enq++;
 }
 
@@ -1111,6 +1125,7 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
         // the 0.6B and 1.7B shapes: one 9-warp CTA per KV head over every key)
         const char *sa = std::getenv("SPEECH_DECODER_STEP_ATTN");
         h->attn_fuse = sa && !std::strcmp(sa, "fused");
+        h->attn_split_kernel = sa && !std::strcmp(sa, "split");
         const char *ac = std::getenv("SPEECH_DECODER_ATTN_CHUNK");
         h->attn_chunk = ac ? std::max(0, std::min(1 << 20, std::atoi(ac))) : 0;
     }

@@ -79,15 +79,13 @@ struct GemvPlan {
     bool ok;
 };
 GemvPlan gemv_plan(int K, bool w_bf16, int nb, int N, int grid_x);
-// tuning knobs (process-wide): pipeline implementation (1 registers, 2 cp.async
-// ring, 3 per-warp bulk ring, 4 producer-warp stream for bf16 weights; the
-// SPEECH_DECODER_GEMV variable ldg|cpasync|tma|stream picks the first default)
-// and bulk ring sizes
+// tuning knobs (process-wide): GEMV implementation for bf16 weights (1
+// registers, 4 producer-warp stream; SPEECH_DECODER_GEMV=ldg|stream) and the
+// stream GEMV's ring size
 void gemv_set_impl(int impl);
 // re-read SPEECH_DECODER_GEMV and SPEECH_DECODER_GEMV_SLOTS (each decoder creation)
 void gemv_reload_env();
 int gemv_impl();
-void gemv_set_ring(int slots);
 
 
 // Batched-step helpers (rows of several sequences through the tensor-core GEMM):
@@ -132,6 +130,14 @@ bool gemv_stream_qkv_attn_ok(int K, int grid_x, int nq, int nkv, int d, bool kv_
 // (longer ones take the split-KV attention kernel)
 constexpr int kFusedAttnMaxCtx = 1024;
 void init_gemv_stream_kernels();
+// Step attention of at most kGroupB sequences as one thread-block cluster per
+// (sequence, KV head) whose CTAs split the keys and combine through
+// distributed shared memory (f16 KV, head_dim 128, 1, 2 or 4 query heads per
+// KV head).  attn_cluster_splits: the cluster size for contexts of up to
+// `capacity` keys, 0 when this kernel does not apply.
+void init_attn_cluster();
+int attn_cluster_splits(int capacity, int nq, int nkv, int d, bool kv_f16, int B);
+cudaError_t launch_attn_cluster(const AttnDecArgs &a, int S, cudaStream_t s);
 // Per-row e4m3 rounding of bf16 weights [rows, cols]: codes, power-of-two row
 // scales and the rounded values in bf16 (`out` may equal `w`)
 void launch_quantize_e4m3_rows(const void *w, size_t rows, int cols, uint8_t *codes, float *scales, void *out,

@@ -7,12 +7,10 @@
 // preceding kernel (programmatic dependent launch): the next projection's
 // weights stream in while the previous kernel drains.
 //
-// Two ways to keep enough bytes in flight (selectable, see gemv_set_impl):
-//  * ring: every warp owns a ring of shared-memory slots fed by 1-D bulk
-//    copies (TMA) completing on per-slot mbarriers, or by cp.async; lanes read
-//    back only the chunks of their own slots, so warps never synchronise with
-//    each other;
-//  * ldg: 16-byte non-allocating loads double-buffered in registers.
+// Bytes in flight come from 16-byte non-allocating loads double-buffered in
+// registers.  This kernel serves fp32 weights (the debug build) and, when
+// selected, bf16 weights; the default bf16 path is the producer-warp GEMV of
+// gemv_stream.cu.
 //
 // Prologues: RMSNorm(x)*w (the pre-LN norms and the final norm), the embedding
 // row of the step's token (layer 0), the plain attention output, or
@@ -31,8 +29,6 @@ namespace dec {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kUnit = 8;                    // 16-byte chunks per lane per unit
-constexpr int kUnitBytes = 32 * kUnit * 16; // 4 KB
-constexpr uint32_t kWaitPolls = 1u << 22;   // bounded mbarrier waits
 
 __device__ __forceinline__ void report(SeqState *st, int code) {
     if (st) atomicCAS(&st->error, 0, code);
@@ -293,125 +289,6 @@ __device__ void rows_epilogue(const GemvArgs &a, const Share &sh, const float *p
     }
 }
 
-// ============================================================== ring variant
-__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(ptx::smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-// wait until at most n committed groups of this thread are pending
-__device__ __forceinline__ void cp_async_wait_pending(int n) {
-    switch (n) {
-    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
-    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
-    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
-    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
-    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
-    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
-    default: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
-    }
-}
-
-template <typename TW, int IN, int OUT, bool TMA>
-__global__ void __launch_bounds__(kThreads, 2) k_gemv_ring(GemvArgs a) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    constexpr int VEC = Vec16<TW>::N;
-    __shared__ float sred[32];
-    __shared__ int live_s[kGroupB];
-    const int NSW = a.n_ring;
-    const int K = a.K, CPR = K / VEC;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int b0 = blockIdx.y * kGroupB;
-    const int nb = min(kGroupB, a.B - b0);
-    const Share sh(a.N, CPR, warp);
-    unsigned char *ring = smem + (size_t)warp * NSW * kUnitBytes;
-    float *xs = reinterpret_cast<float *>(smem + (size_t)kWarps * NSW * kUnitBytes);
-    float *part = xs + (((size_t)nb * K + 3) & ~size_t(3));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(part + (size_t)a.max_units * kGroupB) + warp * NSW;
-    const unsigned char *W = reinterpret_cast<const unsigned char *>(a.W);
-
-    if (TMA && lane == 0) {
-        for (int s = 0; s < NSW; ++s) ptx::mbar_init(&bars[s], 1);
-        ptx::fence_mbar_init();
-    }
-    __syncwarp();
-
-    auto issue = [&](int k) {                            // k-th unit of this warp into slot k % NSW
-        const int u = sh.unit(k, warp), seg = u % sh.SEG;
-        const int nc = min(32 * kUnit, CPR - seg * 32 * kUnit);
-        const unsigned char *src = W + (size_t)sh.row(u) * K * sizeof(TW) + (size_t)seg * kUnitBytes;
-        unsigned char *dst = ring + (size_t)(k % NSW) * kUnitBytes;
-        if (TMA) {
-            if (lane == 0) {
-                ptx::mbar_expect_tx(&bars[k % NSW], (uint32_t)nc * 16);
-                ptx::bulk_g2s(dst, src, (uint32_t)nc * 16, &bars[k % NSW]);
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < kUnit; ++j) {
-                const int c = lane + 32 * j;
-                if (c < nc) cp_async16(dst + c * 16, src + c * 16);
-            }
-            cp_async_commit();
-        }
-    };
-    const int pre = min(NSW, sh.my_units);
-    for (int k = 0; k < pre; ++k) issue(k);                 // weights: no dependency on earlier kernels
-    if (!TMA)
-        for (int k = pre; k < NSW; ++k) cp_async_commit();  // one group per slot
-    ptx::pdl_launch();
-    ptx::pdl_wait();
-
-    const bool any_live = gemv_prologue<TW, IN>(a, xs, b0, nb, CPR, live_s, sred);
-    const int n_k = any_live ? sh.my_units : 0;
-
-    float acc[kGroupB], best_v[kGroupB];
-    int best_i[kGroupB];
-#pragma unroll
-    for (int bi = 0; bi < kGroupB; ++bi) {
-        acc[bi] = 0.f;
-        best_v[bi] = -INFINITY;
-        best_i[bi] = 0x7fffffff;
-    }
-    int k = 0;
-    bool ok = true;
-    for (; k < n_k; ++k) {
-        const int slot = k % NSW;
-        if (TMA) {
-            ok = ptx::mbar_wait_bounded(&bars[slot], (k / NSW) & 1, kWaitPolls);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
-        } else {
-            cp_async_wait_pending(NSW - 1);
-        }
-        const uint4 *wv = reinterpret_cast<const uint4 *>(ring + (size_t)slot * kUnitBytes);
-        const int u = sh.unit(k, warp), seg = u % sh.SEG;
-#pragma unroll
-        for (int j = 0; j < kUnit; ++j) {
-            const int cl = lane + 32 * j, c = seg * 32 * kUnit + cl;
-            if (c < CPR) unit_fma<TW>(wv[cl], c, CPR, K, nb, xs, acc);
-        }
-        __syncwarp();                                          // slot fully read before it is refilled
-        if (k + NSW < n_k) issue(k + NSW);
-        else if (!TMA) cp_async_commit();
-        unit_done(u, nb, part, acc);
-    }
-    // drain what is still in flight (dead rows, or a wait that gave up)
-    if (TMA) {
-        if (lane == 0) {
-            const int issued = any_live ? min(sh.my_units, k + NSW) : pre;
-            for (int v = k; v < issued; ++v) ptx::mbar_wait_bounded(&bars[v % NSW], (v / NSW) & 1, kWaitPolls);
-            if (!ok) report(a.st, 3);
-        }
-    } else {
-        cp_async_wait_all();
-    }
-    if (OUT == OUT_ARGMAX || any_live) rows_epilogue<OUT>(a, sh, part, b0, nb, live_s, best_v, best_i);
-    if (OUT == OUT_ARGMAX) argmax_finalize(a, best_v, best_i, b0, nb, live_s);
-}
-
 // ============================================================== register variant
 template <typename TW, int IN, int OUT>
 __global__ void __launch_bounds__(kThreads, 2) k_gemv_ldg(GemvArgs a) {
@@ -473,18 +350,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemv_ldg(GemvArgs a) {
 }
 
 // ------------------------------------------------------------------ host side
-// 1: registers, 2: ring fed by cp.async, 3: per-warp ring fed by 1-D TMA,
-// 4: producer-warp stream (bf16 weights; f32 weights use 1)
+// 1: registers (fp32 weights always, bf16 weights when selected),
+// 4: producer-warp stream (bf16 weights)
 static int g_impl = 0;
-static int g_ring_slots = 3;
 void gemv_set_impl(int impl) {
-    if (impl >= 1 && impl <= 4) g_impl = impl;
+    if (impl == 1 || impl == 4) g_impl = impl;
 }
 void gemv_reload_env() {
     const char *v = std::getenv("SPEECH_DECODER_GEMV");
-    g_impl = !v ? 4 : !std::strcmp(v, "ldg") ? 1 : !std::strcmp(v, "cpasync") ? 2 : !std::strcmp(v, "tma") ? 3 : 4;
+    g_impl = v && !std::strcmp(v, "ldg") ? 1 : 4;
     const char *n = std::getenv("SPEECH_DECODER_GEMV_SLOTS");
-    if (n) gemv_set_ring(std::atoi(n));
     gemv_stream_set_slots(n ? std::atoi(n) : 0);
 }
 int gemv_impl() {
@@ -492,9 +367,6 @@ int gemv_impl() {
     return g_impl;
 }
 int gemv_default_ctas_per_sm() { return gemv_impl() == 4 ? 1 : 2; }
-void gemv_set_ring(int slots) {
-    if (slots >= 2 && slots <= 7) g_ring_slots = slots;
-}
 
 int gemv_grid(int N, int num_sms, int ctas_per_sm) {
     const int g = num_sms * ctas_per_sm;
@@ -504,13 +376,12 @@ int gemv_grid(int N, int num_sms, int ctas_per_sm) {
 GemvPlan gemv_plan(int K, bool w_bf16, int nb, int N, int grid_x) {
     GemvPlan p{};
     const int row_bytes = K * (w_bf16 ? 2 : 4);
-    p.n_ring = g_ring_slots;
+    p.n_ring = 0;
     const int seg = (row_bytes / 16 + 32 * kUnit - 1) / (32 * kUnit);
     p.max_units = ((N + grid_x - 1) / grid_x) * seg;
     const size_t xs = ((size_t)nb * K + 3) / 4 * 16;
     const size_t part = (size_t)p.max_units * kGroupB * 4;
-    const size_t ring = (size_t)kWarps * p.n_ring * kUnitBytes + (size_t)kWarps * p.n_ring * 8;
-    p.smem = (gemv_impl() == 1 || gemv_impl() == 4 ? 0 : ring) + xs + part;
+    p.smem = xs + part;
     p.ok = (row_bytes % 16 == 0) && p.smem <= (size_t)kGemvMaxSmem;
     return p;
 }
@@ -527,9 +398,7 @@ static void launch_one(const GemvArgs &a, dim3 grid, size_t smem, cudaStream_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (g_impl == 1 || g_impl == 4) cudaLaunchKernelEx(&cfg, k_gemv_ldg<TW, IN, OUT>, a);
-    else if (g_impl == 2) cudaLaunchKernelEx(&cfg, k_gemv_ring<TW, IN, OUT, false>, a);
-    else cudaLaunchKernelEx(&cfg, k_gemv_ring<TW, IN, OUT, true>, a);
+    cudaLaunchKernelEx(&cfg, k_gemv_ldg<TW, IN, OUT>, a);
 }
 
 template <typename TW>
@@ -569,8 +438,6 @@ static void set_attrs(F *fn) {
 template <typename TW, int IN, int OUT>
 static void init_one() {
     set_attrs(k_gemv_ldg<TW, IN, OUT>);
-    set_attrs(k_gemv_ring<TW, IN, OUT, false>);
-    set_attrs(k_gemv_ring<TW, IN, OUT, true>);
 }
 
 template <typename TW>
@@ -587,6 +454,7 @@ void init_gemv_kernels() {
     init_t<float>();
     init_gemv_stream_kernels();
     init_attn_kernels();
+    init_attn_cluster();
 }
 
 }  // namespace dec

@@ -81,3 +81,33 @@ def test_traffic_record_is_well_formed():
     assert "--clock-control none" in d["command"]
     t = bench.ncu_traffic()
     assert t is None or t == d["dram_bytes_per_launch"]
+
+
+def test_prefill_work_counts_rows_pairs_and_slice_last():
+    """FLOPs of a prefill counted by brute force over rows and causal
+    (query, key) pairs, with the last block on the last row only."""
+    spec = synth.small_spec(n_layers=3, hidden=64, n_heads=4, n_kv_heads=2, head_dim=16, ffn=96, vocab=50)
+    H, F, d, nq, nkv, V = spec.hidden, spec.ffn, spec.head_dim, spec.n_heads, spec.n_kv_heads, spec.vocab
+    qkv = (nq + 2 * nkv) * d * H
+    rest = H * nq * d + 2 * F * H + H * F
+    for Ts in ([1], [7], [5, 9]):
+        want = 0
+        for T in Ts:
+            pairs = sum(t + 1 for t in range(T))          # causal (query, key) pairs
+            want += (spec.n_layers - 1) * (2 * T * (qkv + rest) + 4 * nq * d * pairs)
+            want += 2 * T * qkv + 2 * rest + 4 * nq * d * T  # last block: keys of every row, one query row
+            want += 2 * V * H                                 # tied lm_head on the last row
+        flops, nbytes = bench.prefill_work(spec, Ts)
+        assert flops == want
+        kv = sum(Ts) * spec.n_layers * 2 * nkv * d * 2
+        assert nbytes == 2 * weight_count(spec) + kv + sum(Ts) * H * 4
+
+
+def test_prefill_roofline_picks_the_bound():
+    spec = synth.QWEN3_1_7B
+    # 152 rows: about 125 FLOP per byte, below the ridge (HBM); 8015 rows: far above (tensor cores)
+    r = bench.prefill_roofline(spec, [152], 1.0, 6793.1, 1701.1)
+    assert r["bound"] == "hbm" and r["frac"] == r["hbm_frac"]
+    r = bench.prefill_roofline(spec, [8015], 30.0, 6793.1, 1701.1)
+    assert r["bound"] == "tensor" and r["frac"] == r["tc_frac"]
+    assert 28e12 < r["flops"] < 30.1e12

@@ -293,3 +293,102 @@ def test_batched_tc_path_prefill_steps_generate(small):
     for b in range(7):
         rids, rtrunc, _ = O.greedy(O.Oracle(spec, w, embs[b].shape[0] + 10), embs[b], 10, eos_id=eos)
         assert out[b][0] == rids and out[b][1] == rtrunc, (b, out[b], rids)
+
+
+# ------------------------------------------------------------------ argmax ties on the device
+def _tie_weights(spec, w, tops, used, near):
+    """A copy of the weights in which, for each top token t in `tops`, a lower
+    index j (t - 1 when `near`, else the lowest index not in `used`) gets the
+    embedding row of t: logit j then equals logit t exactly, at every
+    position (the lm_head is the tied embedding), so the lowest-index rule
+    must pick j.  Returns (weights, {t: j})."""
+    w2 = dict(w)
+    E = np.array(w["embed"], copy=True)
+    pairs, taken = {}, set(used) | set(tops)
+    for t in sorted(set(tops)):
+        if near:
+            j = t - 1
+            assert j >= 0 and j not in taken
+        else:
+            j = next(i for i in range(t) if i not in taken)
+        E[j] = E[t]
+        pairs[t] = j
+        taken.add(j)
+    w2["embed"] = E
+    return w2, pairs
+
+
+@pytest.mark.parametrize("near", [True, False], ids=["same-warp", "across-ctas"])
+def test_argmax_tie_single_sequence(small, near):
+    """The lm_head GEMV's argmax (one sequence) returns the lower index of two
+    equal logits, within a warp's rows and across CTAs (model.cpp, run: the
+    strict '>' scan keeps the first maximum)."""
+    spec, w = small
+    emb, item = prompt_rows(spec, w, synth.Prompt(3, 30, 2), seed=31)
+    t = O.argmax_lowest(O.Oracle(spec, w, emb.shape[0] + 2).prefill(emb))
+    used = set(int(v) for v in item["ids"])
+    if near and (t == 0 or t - 1 in used):
+        pytest.skip("no free neighbour below the top token for this seed")
+    w2, pairs = _tie_weights(spec, w, [t], used, near)
+    j = pairs[t]
+    if not near:
+        assert t - j > spec.vocab // 152, "the two rows must sit in different CTAs"
+    emb2, _ = prompt_rows(spec, w2, synth.Prompt(3, 30, 2), seed=31)
+    ref = O.Oracle(spec, w2, emb2.shape[0] + 2).prefill(emb2)
+    assert ref[j] == ref[t] and O.argmax_lowest(ref) == j
+    dec = make(spec, w2, max_ctx=64, max_new=2)
+    tok = dec.prefill(emb2)
+    got = dec.logits(1)[0]
+    dec.close()
+    assert got[j] == got[t], "the duplicated rows must give identical logits"
+    assert tok == j, f"tie of rows {j} and {t}: the device picked {tok}"
+
+
+def test_argmax_tie_batched_rows(small):
+    """Same rule for the batched head (more rows than one GEMV CTA holds: the
+    tensor-core lm_head and the row-wise argmax kernel)."""
+    spec, w = small
+    prompts = [synth.Prompt(2, 10 + 7 * i, 1) for i in range(6)]
+    rows = [prompt_rows(spec, w, p, seed=41, item=i) for i, p in enumerate(prompts)]
+    tops = [O.argmax_lowest(O.Oracle(spec, w, e.shape[0] + 2).prefill(e)) for e, _ in rows]
+    used = set(int(v) for _, it in rows for v in it["ids"])
+    w2, pairs = _tie_weights(spec, w, tops, used, near=False)
+    embs = [prompt_rows(spec, w2, p, seed=41, item=i)[0] for i, p in enumerate(prompts)]
+    dec = make(spec, w2, max_ctx=128, max_batch=8, max_tokens=1024, max_new=2)
+    first = dec.prefill_batch(embs)
+    got = dec.logits(6)
+    dec.close()
+    for b, e in enumerate(embs):
+        ref = O.Oracle(spec, w2, e.shape[0] + 2).prefill(e)
+        j = O.argmax_lowest(ref)
+        assert j in pairs.values() and ref[j] == ref[tops[b]], b
+        assert got[b][j] == got[b][tops[b]], f"item {b}: duplicated rows differ on the device"
+        assert int(first[b]) == j, f"item {b}: tie of rows {j} and {tops[b]}, device picked {first[b]}"
+
+
+# ------------------------------------------------------------------ decode budget (moss/model.cpp, run)
+def test_greedy_stops_at_decode_budget(small):
+    """A greedy run given the generation budget of dec_decode_budget stops
+    exactly there, with the oracle's tokens."""
+    from speech_decoder_gb300.binding import decode_budget
+    spec, w = small
+    prompt = synth.Prompt(9, 70, 6)
+    emb, _ = prompt_rows(spec, w, prompt, seed=51)
+    ceiling = prompt.T + 300
+    budget = decode_budget(prompt.n_audio, prompt.T, ceiling)
+    assert budget == O.decode_budget(prompt.n_audio, prompt.T, ceiling) == 268
+    dec = make(spec, w, max_ctx=ceiling, max_new=300)
+    dec.prefill(emb)
+    ids, trunc = dec.generate(budget)
+    ref, rtrunc, hist = O.greedy(O.Oracle(spec, w, ceiling), emb, budget, keep_logits=True)
+    assert len(ids) == budget and trunc and rtrunc
+    # tokens equal the oracle's up to the first tie inside the observed error:
+    # at a difference, replay the GPU's tokens up to it for its logits there
+    k = next((i for i, (a, b) in enumerate(zip(ids, ref)) if a != b), None)
+    if k is not None:
+        dec.prefill(emb)
+        for i in range(k):
+            dec.step(ids[i])
+        got = dec.logits(1)[0]
+        assert token_ok(ids[k], hist[k], got), f"token {k}: GPU {ids[k]}, oracle {ref[k]}"
+    dec.close()

@@ -39,6 +39,9 @@ def test_noalloc_matches_scratch_entry_point_twice(lib):
 
 def test_noalloc_rejects_oversized_shapes(lib):
     from speech_decoder_gb300.binding import DEC_ERR_OOM
-    # 4096 sequences x 8 KV heads x 2 query heads of d=128 need ~8.5 MB of partials
+    # 4096 sequences x 8 KV heads x 1 split x 2 query heads x (128 + 2) floats:
+    # about 34 MB of partials, far above the 4 MiB array
     st = lib.dec_attn_decode_noalloc(1, 1, 1, 2, 100, 1, 1, 4096, 16, 8, 128, 1, None)
     assert st == DEC_ERR_OOM
+    # the limit of that shape is 502 sequences: 503 no longer fits
+    assert lib.dec_attn_decode_noalloc(1, 1, 1, 2, 100, 1, 1, 503, 16, 8, 128, 1, None) == DEC_ERR_OOM
