@@ -115,10 +115,12 @@ struct dec_handle {
     int pf_bytes = 0;               // L2 look-ahead of the decode GEMVs, bytes per CTA
     // persistent step kernel
     StepLayer *step_layers = nullptr;
+    CUtensorMap *kv_maps = nullptr;  // [L][2] K and V pool maps of the step kernel's attention tiles
     unsigned long long *step_bar = nullptr;
     bool use_step = false;
     bool attn_fuse = false;         // single-sequence q|k|v GEMV runs the step attention (short contexts)
     bool attn_split_kernel = false; // step attention always on the split-KV kernel (no cluster kernel)
+    int lo_planes = 15;             // prompt projections whose activations enter as two bf16 planes
     int attn_chunk = 0;             // keys per step-attention split at least (0: attn_step_min_chunk)
 };
 
@@ -276,6 +278,7 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     h->st = b.take<SeqState>(1);
     h->tc_scratch = b.take<float>(kTcScratchFloats);
     h->step_layers = b.take<StepLayer>(hp.n_layers);
+    h->kv_maps = b.take<CUtensorMap>(2 * (size_t)hp.n_layers);
     h->step_bar = b.take<unsigned long long>(1);
     h->dump_inj = b.take<float>(Tm * H);
     h->dump_b0 = b.take<float>(Tm * H);
@@ -300,6 +303,13 @@ static void gemm(dec_handle *h, const void *A, const void *A_lo, const void *W, 
     else
         launch_gemm_simt(A, h->w_bf16, W, h->w_bf16, C, ldc, M, N, K, epi, h->stream);
     h->enq++;
+}
+
+// The second activation plane of a prompt projection, or null where the
+// projection takes one bf16 plane (bit of h->lo_planes: 1 q|k|v, 2 o,
+// 4 gate|up, 8 down).
+static const void *lo_plane(const dec_handle *h, int bit, const void *lo) {
+    return (h->lo_planes & bit) ? lo : nullptr;
 }
 
 // Gate|up projection and SwiGLU into h->hbuf (and its second plane).
@@ -608,7 +618,7 @@ static void enqueue_head(dec_handle *h, int B) {
     h->enq++;
 }
 
-static StepArgs step_args(dec_handle *h, int B) {
+static StepArgs step_args(dec_handle *h) {
     const dec_hparams &hp = h->hp;
     StepArgs a{};
     a.L = hp.n_layers;
@@ -618,22 +628,20 @@ static StepArgs step_args(dec_handle *h, int B) {
     a.nkv = hp.n_kv_heads;
     a.V = hp.vocab;
     a.qkv_n = qkv_rows(hp);
-    a.B = B;
     a.slots = (int)h->slots;
-    a.splits = splits_for(h, B);
+    a.S = step_splits(hp.max_ctx);
     a.eps = hp.rms_eps;
     a.scale = (float)(1.0 / std::sqrt((double)hp.head_dim));
     a.layers = h->step_layers;
+    a.kv_maps = h->kv_maps;
     a.embed = static_cast<const __nv_bfloat16 *>(h->embed);
     a.final_norm = h->final_norm;
     a.rope = h->rope;
     a.x = h->xd;
     a.qkv = h->qkvd;
-    a.o = h->od;
-    a.gu = h->gud;
+    a.h = h->gud;
+    a.part = h->attn_part;
     a.logits = h->logits;
-    a.attn_part = h->attn_part;
-    a.attn_counter = h->attn_counter;
     a.am_val = h->am_val;
     a.am_idx = h->am_idx;
     a.am_counter = h->am_counter;
@@ -644,11 +652,11 @@ static StepArgs step_args(dec_handle *h, int B) {
     return a;
 }
 
-static bool step_path(const dec_handle *h, int B) { return h->use_step && B <= kGroupB; }
+static bool step_path(const dec_handle *h, int B) { return h->use_step && B == 1; }
 
 static void enqueue_step(dec_handle *h, int B) {
     if (step_path(h, B)) {
-        launch_step(step_args(h, B), h->num_sms, h->stream);
+        launch_step(step_args(h), h->num_sms, h->stream);
         h->enq++;
         return;
     }
@@ -758,7 +766,7 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
     for (int l = 0; l < hp.n_layers; ++l) {
         const DevLayer &L = h->L[l];
         launch_rmsnorm_rows(h->x, L.attn_norm, hp.rms_eps, h->xn, h->xn_lo, h->w_bf16, total, H, s);
-        gemm(h, h->xn, h->xn_lo, L.wqkv, h->qkv, qkv_rows(hp), total, qkv_rows(hp), H, EPI_STORE_F32);
+        gemm(h, h->xn, lo_plane(h, 1, h->xn_lo), L.wqkv, h->qkv, qkv_rows(hp), total, qkv_rows(hp), H, EPI_STORE_F32);
         RopeKvArgs r{};
         r.qkv = h->qkv;
         r.qn_w = L.qn;
@@ -824,10 +832,10 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
             } else {
                 launch_attn_prefill_simt(h->kv_f16, h->w_bf16, a, s);
             }
-            gemm(h, h->attn_o, h->attn_o_lo, L.wo, h->x, H, total, H, nqd, EPI_RESID_F32);
+            gemm(h, h->attn_o, lo_plane(h, 2, h->attn_o_lo), L.wo, h->x, H, total, H, nqd, EPI_RESID_F32);
             launch_rmsnorm_rows(h->x, L.ffn_norm, hp.rms_eps, h->xn, h->xn_lo, h->w_bf16, total, H, s);
-            gemm_swiglu(h, h->xn, h->xn_lo, L.wgu, total, F, H);
-            gemm(h, h->hbuf, h->hbuf_lo, L.wd, h->x, H, total, H, F, EPI_RESID_F32);
+            gemm_swiglu(h, h->xn, lo_plane(h, 4, h->xn_lo), L.wgu, total, F, H);
+            gemm(h, h->hbuf, lo_plane(h, 8, h->hbuf_lo), L.wd, h->x, H, total, H, F, EPI_RESID_F32);
             h->enq += 2;
             if (h->dumps && l == 0) {
                 CK(cudaMemcpyAsync(h->dump_b0, h->x, (size_t)total * H * 4, cudaMemcpyDeviceToDevice, s));
@@ -1109,13 +1117,24 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
                               static_cast<__half *>(D.V)};
         }
         CKC(cudaMemcpyAsync(h->step_layers, sl.data(), sl.size() * sizeof(StepLayer), cudaMemcpyHostToDevice, s));
-        CKC(cudaStreamSynchronize(s));
         // the per-op kernel sequence is the default; SPEECH_DECODER_STEP=persistent
-        // selects the single cooperative launch per step where it is supported
+        // selects the single cooperative launch per step of one sequence where
+        // it is supported
         const char *env = std::getenv("SPEECH_DECODER_STEP");
-        h->use_step = h->w_bf16 && h->kv_f16 && env && !std::strcmp(env, "persistent") &&
-                      step_supported((int)d, (int)(nq / nkv), (int)H, (int)F, (int)(nq * d),
-                                     std::min(hp->max_batch, kGroupB));
+        bool maps_ok = true;
+        std::vector<CUtensorMap> maps(2 * (size_t)hp->n_layers);
+        if (h->w_bf16 && !h->w_e4m3 && h->kv_f16 && d == 128)
+            for (int l = 0; l < hp->n_layers && maps_ok; ++l)
+                maps_ok = step_kv_maps(&maps[2 * l], &maps[2 * l + 1], h->L[l].K, h->L[l].V, (int)(nkv * h->slots));
+        else
+            maps_ok = false;
+        if (maps_ok)
+            CKC(cudaMemcpyAsync(h->kv_maps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice,
+                                s));
+        CKC(cudaStreamSynchronize(s));
+        h->use_step = maps_ok && env && !std::strcmp(env, "persistent") &&
+                      step_supported((int)d, (int)(nq / nkv), (int)nkv, (int)H, (int)F, hp->max_ctx, h->num_sms) &&
+                      step_splits(hp->max_ctx) <= kAttnMaxSplits;
         cudaGetLastError();
     }
     CKC(cudaMemsetAsync(h->attn_counter, 0, (size_t)hp->max_batch * nkv * sizeof(unsigned), s));
@@ -1126,6 +1145,8 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
         const char *sa = std::getenv("SPEECH_DECODER_STEP_ATTN");
         h->attn_fuse = sa && !std::strcmp(sa, "fused");
         h->attn_split_kernel = sa && !std::strcmp(sa, "split");
+        const char *pl = std::getenv("SPEECH_DECODER_PLANES");
+        h->lo_planes = pl ? std::max(0, std::min(15, std::atoi(pl))) : 15;
         const char *ac = std::getenv("SPEECH_DECODER_ATTN_CHUNK");
         h->attn_chunk = ac ? std::max(0, std::min(1 << 20, std::atoi(ac))) : 0;
     }
