@@ -30,6 +30,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+
 #include "gemm_tc.cuh"
 #include "ptx.cuh"
 #include "tc.cuh"
@@ -280,8 +282,170 @@ __global__ void __launch_bounds__(256) k_splitk_reduce(TcArgs a, int mt) {
     }
 }
 
+// ------------------------------------------------------------------ persistent form (long prompts)
+// One CTA per SM walks output tiles of 256 weight rows (two 128-row MMA groups:
+// gate and up rows for SwiGLU) x 128 prompt rows, the tiles of one prompt-row
+// block consecutively (its activation panel stays in L2 while the weights
+// pass).  The accumulator is double-buffered in TMEM (columns 0-255 and
+// 256-511): the epilogue warps drain tile i while the MMA warp runs tile i + 1,
+// and the TMA producer runs ahead through a ring that spans tile boundaries.
+constexpr int kPtBN = 128;
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_gemm_tc_pt(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmB2, TcArgs a) {
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *smem =
+        reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int S = a.n_stages;
+    const uint32_t a_bytes = 2u * 16384u, b_bytes = (uint32_t)kPtBN * 128u;
+    const uint32_t stage_bytes = a_bytes + (uint32_t)a.planes * b_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * stage_bytes);
+    uint64_t *empty = full + S;
+    uint64_t *tfull = empty + S;                  // [2] accumulator buffer ready for the epilogue
+    uint64_t *tempty = tfull + 2;                 // [2] accumulator buffer drained
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(tempty + 2);
+    __shared__ int abort_s;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int MT = a.n_feat * (a.epi == EPI_SWIGLU_BF16 ? 2 : 1) / 256;   // 256-row weight tiles
+    const int NT = (a.T + kPtBN - 1) / kPtBN;
+    const int tiles = MT * NT;
+    const int KT = a.k_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&tfull[b], 1);
+            ptx::mbar_init(&tempty[b], 4);           // one arrival per epilogue warp
+        }
+        abort_s = 0;
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         ptx::smem_u32(tmem_slot)),
+                     "r"(512)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    ptx::pdl_launch();
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------------- TMA producer
+        int it = 0;
+        bool waited = false;
+        for (int t = blockIdx.x; t < tiles && !*(volatile int *)&abort_s; t += gridDim.x) {
+            const int m0 = (t % MT) * 256, n0 = (t / MT) * kPtBN;
+            for (int kt = 0; kt < KT; ++kt, ++it) {
+                const int s = it % S;
+                if (it >= S && !ptx::mbar_wait_bounded(&empty[s], ((it / S) - 1) & 1, kTcPolls)) {
+                    tc_report(a.err, 14);
+                    abort_s = 1;
+                    break;
+                }
+                unsigned char *st = smem + (size_t)s * stage_bytes;
+                ptx::mbar_expect_tx(&full[s], stage_bytes);
+                tma_load_2d(st, &tmA, kt * kBK, m0, &full[s]);           // weights: no dependency
+                if (!waited) {
+                    ptx::pdl_wait();                                    // activations come from the predecessor
+                    waited = true;
+                }
+                tma_load_2d(st + a_bytes, &tmB, kt * kBK, n0, &full[s]);
+                if (a.planes == 2) tma_load_2d(st + a_bytes + b_bytes, &tmB2, kt * kBK, n0, &full[s]);
+            }
+        }
+        // stages issued but not consumed (a wait that gave up) land before the CTA exits
+        if (*(volatile int *)&abort_s)
+            for (int i = it > S ? it - S : 0; i < it; ++i) ptx::mbar_wait_bounded(&full[i % S], (i / S) & 1, kTcPolls);
+    } else if (warp == 1 && lane == 0) {
+        // ---------------------------------------------------------- MMA issuer
+        int it = 0, tl = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++tl) {
+            const int buf = tl & 1;
+            if (tl >= 2 && !ptx::mbar_wait_bounded(&tempty[buf], ((tl >> 1) - 1) & 1, kTcPolls)) {
+                tc_report(a.err, 15);
+                abort_s = 1;
+            }
+            if (*(volatile int *)&abort_s) break;
+            tc_fence_after();
+            const uint32_t acc = tmem + (uint32_t)(buf * 2 * kPtBN);
+            for (int kt = 0; kt < KT; ++kt, ++it) {
+                const int s = it % S;
+                if (!ptx::mbar_wait_bounded(&full[s], (it / S) & 1, kTcPolls)) {
+                    tc_report(a.err, 16);
+                    abort_s = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t abase = ptx::smem_u32(smem + (size_t)s * stage_bytes), bbase = abase + a_bytes;
+#pragma unroll
+                for (int kk = 0; kk < kBK / 16; ++kk) {
+                    for (int pl = 0; pl < a.planes; ++pl) {
+                        const uint64_t bdesc = sw128_desc(bbase + pl * b_bytes + kk * 32);
+#pragma unroll
+                        for (int g = 0; g < 2; ++g)
+                            mma_f16(acc + (uint32_t)(g * kPtBN), sw128_desc(abase + g * 16384 + kk * 32), bdesc,
+                                    a.idesc, (kt | kk | pl) != 0);
+                    }
+                }
+                mma_commit(&empty[s]);                  // stage free once these MMAs have read it
+            }
+            if (*(volatile int *)&abort_s) break;
+            mma_commit(&tfull[buf]);                    // accumulator buffer final
+        }
+    } else if (warp >= 2) {
+        // ---------------------------------------------------------- epilogue
+        ptx::pdl_wait();
+        const int q = warp & 3;                         // TMEM lane quarter this warp may access
+        const int r = 32 * q + lane;                    // row within a 128-row group
+        int tl = 0;
+        for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++tl) {
+            const int buf = tl & 1;
+            const bool ok = ptx::mbar_wait_bounded(&tfull[buf], (tl >> 1) & 1, kTcPolls);
+            if (!ok && lane == 0) {
+                tc_report(a.err, 17);
+                abort_s = 1;
+            }
+            // warp-uniform: the TMEM loads below are warp-collective
+            if (__any_sync(0xffffffffu, !ok || *(volatile int *)&abort_s)) break;
+            tc_fence_after();
+            const int mt = t % MT, n0 = (t / MT) * kPtBN;
+            const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 2 * kPtBN);
+            const bool swiglu = a.epi == EPI_SWIGLU_BF16;
+            const int f = swiglu ? mt * 128 + r : mt * 256 + r;
+            for (int c = 0; c < kPtBN; c += 32) {
+                float v[32], u[32];
+                tmem_ld32(tq + c, v);
+                tmem_ld32(tq + kPtBN + c, u);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    epi_store(a, f, n0 + c + j, v[j], u[j]);
+                    if (!swiglu) epi_store(a, f + 128, n0 + c + j, u[j], 0.f);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&tempty[buf]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512) : "memory");
+}
+
 // ------------------------------------------------------------------ host side
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static int g_pt_max_smem = 0;
 static bool g_tc_ready = false;
 static int g_max_dyn_smem = 0;
 
@@ -303,12 +467,26 @@ void init_gemm_tc() {
             if (cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, g_max_dyn_smem) ==
                 cudaSuccess)
                 g_tc_ready = true;
+            cudaFuncAttributes fp{};
+            if (cudaFuncGetAttributes(&fp, k_gemm_tc_pt) == cudaSuccess) {
+                g_pt_max_smem = optin - (int)fp.sharedSizeBytes;
+                if (cudaFuncSetAttribute(k_gemm_tc_pt, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         g_pt_max_smem) != cudaSuccess)
+                    g_pt_max_smem = 0;
+            }
         }
     }
     cudaGetLastError();
 }
 
 bool gemm_tc_ready() { return g_tc_ready; }
+
+// persistent form: stages of 256 weight rows + planes x 128 prompt rows of 64 K each
+static int pt_stages(int planes) {
+    const int stage = 2 * 16384 + planes * kPtBN * 128;
+    const int n = (g_pt_max_smem - 1024 - 256) / stage;
+    return n > 6 ? 6 : n;
+}
 
 static bool make_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t K, uint32_t box_rows) {
     const cuuint64_t dims[2] = {K, rows};
@@ -358,12 +536,71 @@ TcPlan gemm_tc_plan(int T, int n_feat, int K, int groups, int num_sms, size_t sc
     return p;
 }
 
+// Long prompts with 256-row weight tiles: the persistent kernel (at least one
+// tile per SM, no split-K).
+static bool use_persistent(int T, int n_feat, int K, int groups, int planes, int num_sms, int force_splits) {
+    if (!g_tc_ready || g_pt_max_smem <= 0 || groups != 2 || force_splits > 0 || K % kBK || n_feat % 256) return false;
+    if (pt_stages(planes) < 3) return false;
+    const long long tiles = (long long)(n_feat / 256) * ((T + kPtBN - 1) / kPtBN);
+    return T >= 1024 && tiles >= num_sms;
+}
+
+static bool pt_disabled() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = std::getenv("SPEECH_DECODER_GEMM_PT");
+        v = e && e[0] == '0' ? 1 : 0;
+    }
+    return v == 1;
+}
+
 cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K, int groups,
                            int epi, float *C, int ldc, void *Hout, void *Hout_lo, int ldh, float *scratch,
                            size_t scratch_floats, int *err, int num_sms, cudaStream_t s, int force_splits,
                            const float *bias) {
     if (epi == EPI_BIAS_F32 && !bias) return cudaErrorInvalidValue;
     const int planes = X_lo ? 2 : 1;
+    if (!pt_disabled() && use_persistent(T, n_feat, K, groups, planes, num_sms, force_splits)) {
+        CUtensorMap mA, mB, mB2;
+        if (!make_map(&mA, W, (uint64_t)n_feat, (uint64_t)K, 256u) ||
+            !make_map(&mB, X, (uint64_t)T, (uint64_t)K, (uint32_t)kPtBN) ||
+            !make_map(&mB2, X_lo ? X_lo : X, (uint64_t)T, (uint64_t)K, (uint32_t)kPtBN))
+            return cudaErrorInvalidValue;
+        TcArgs a{};
+        a.n_feat = epi == EPI_SWIGLU_BF16 ? n_feat / 2 : n_feat;
+        a.T = T;
+        a.K = K;
+        a.groups = 2;
+        a.planes = planes;
+        a.BN = kPtBN;
+        a.n_stages = pt_stages(planes);
+        a.k_tiles = K / kBK;
+        a.splits = 1;
+        a.kt_per_split = a.k_tiles;
+        a.epi = epi;
+        a.C = C;
+        a.ldc = ldc;
+        a.Hout = static_cast<__nv_bfloat16 *>(Hout);
+        a.Hout_lo = static_cast<__nv_bfloat16 *>(Hout_lo);
+        a.ldh = ldh;
+        a.bias = bias;
+        a.err = err;
+        a.idesc = mma_idesc_f16(true, 128, kPtBN);
+        a.tmem_cols = 512;
+        const int tiles = (n_feat / 256) * ((T + kPtBN - 1) / kPtBN);
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(std::min(num_sms, tiles));
+        cfg.blockDim = dim3(kTcThreads);
+        cfg.dynamicSmemBytes = (size_t)a.n_stages * (2 * 16384 + planes * kPtBN * 128) + 1024 + 256;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc_pt, mA, mB, mB2, a);
+        return e != cudaSuccess ? e : cudaPeekAtLastError();
+    }
     const TcPlan p = gemm_tc_plan(T, n_feat, K, groups, num_sms, scratch_floats, force_splits, planes);
     if (!p.ok) return cudaErrorInvalidValue;
     CUtensorMap mA, mB, mB2;

@@ -124,6 +124,9 @@ def run_gemm(lib, X, W, epi, use_tc, splits=0, C0=None):
 GEMMS = [  # T, N, K, splits (0 = automatic)
     (16, 512, 256, 0), (152, 4096, 2048, 0), (152, 2048, 6144, 0), (1, 256, 512, 0), (700, 1024, 512, 0),
     (8015, 256, 256, 0), (37, 384, 1408, 3), (152, 128, 64, 1), (300, 768, 192, 2),
+    # long prompts: the persistent kernel (tiles of 256 weight rows x 128 prompt rows, several per CTA;
+    # ragged last prompt-row tile; K = 6144 as in the down projection)
+    (8015, 12288, 2048, 0), (2048, 4096, 2048, 0), (1500, 2048, 6144, 0),
 ]
 
 
@@ -141,8 +144,9 @@ def test_gemm_tc_matches_oracle_linear(lib, shape):
     assert rel_err(got, C0 + ref) <= 1e-5
 
 
-@pytest.mark.parametrize("shape", [(152, 1536, 512, 0), (16, 512, 256, 2), (500, 768, 256, 0)],
-                         ids=["T152F768", "T16F256s2", "T500F384"])
+@pytest.mark.parametrize("shape", [(152, 1536, 512, 0), (16, 512, 256, 2), (500, 768, 256, 0), (8015, 12288, 2048, 0),
+                                   (1100, 4096, 1024, 0)],
+                         ids=["T152F768", "T16F256s2", "T500F384", "T8015F6144", "T1100F2048"])
 def test_gemm_tc_swiglu_matches_oracle(lib, shape):
     T, N2, K, splits = shape
     F = N2 // 2
@@ -153,9 +157,13 @@ def test_gemm_tc_swiglu_matches_oracle(lib, shape):
     # pack as the library does: blocks of 128 gate rows then the same 128 features' up rows
     packed = np.concatenate([np.concatenate([Wg[j:j + 128], Wu[j:j + 128]]) for j in range(0, F, 128)])
     got = run_gemm(lib, X, packed, 2, 1, splits)
-    ref = O.silu(O.linear(X, Wg)) * O.linear(X, Wu)
-    # output is rounded to bf16: relative error up to 2^-8 of each value
-    assert np.all(np.abs(got - ref) <= 2 ** -8 * np.abs(ref) + 1e-6)
+    g, u = O.linear(X, Wg), O.linear(X, Wu)
+    ref = O.silu(g) * u
+    # output rounded to bf16 (relative error up to 2^-9 of each value, 2^-8
+    # allowed), plus the fp32 accumulation error of gate and up (well below
+    # 1e-5 absolute for K <= 2048 at these magnitudes), carried through the
+    # product: it dominates where one factor is near zero
+    assert np.all(np.abs(got - ref) <= 2 ** -8 * np.abs(ref) + 1e-5 * (np.abs(O.silu(g)) + np.abs(u)))
 
 
 def test_gemm_simt_matches_oracle_linear(lib):
