@@ -370,11 +370,12 @@ __device__ __forceinline__ void stage_rows(const GemvArgs &a, const uint4 *stage
 // gate row is (f / 128) * 256 + f % 128 of the packed matrix, its up row 128
 // further).
 template <int NB, int WB>
-__device__ __forceinline__ void stage_pairs(const GemvArgs &a, const uint4 *stage, int j0, int n, int CPR, int b0,
-                                            const float *xs, const float (&rs)[NB], const int *live) {
+__device__ __forceinline__ void stage_pairs(const GemvArgs &a, const uint4 *stage, int j0, int n, int i0, int i1,
+                                            int CPR, int b0, const float *xs, const float (&rs)[NB],
+                                            const int *live) {
     constexpr int Q = 4 / WB;
     const int lane = threadIdx.x & 31, K = a.K;
-    for (int i = 0; i < n; ++i) {
+    for (int i = i0; i < i1; ++i) {
         const uint4 *wg = stage + (size_t)i * CPR, *wu = stage + (size_t)(n + i) * CPR;
         const int f = j0 + i, grow = (f >> 7) * 256 + (f & 127);
         const float wsg = WB == 1 ? __ldg(a.wscale + grow) : 1.f;
@@ -451,10 +452,14 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
     const unsigned char *W = reinterpret_cast<const unsigned char *>(a.W);
     constexpr bool kNorm = IN == IN_NORM || IN == IN_EMBED_NORM;
 
+    // consumer work units: (gate, up) pairs, or at most two rows of a chunk
+    // (two rows share each activation read); every warp takes units round
+    // robin, so a CTA's rows spread over all consumer warps
+    const int UPC = kPair ? R : (R + 1) / 2;             // units per full chunk
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], 1);
+            ptx::mbar_init(&empty[s], UPC);             // one arrival per unit of the chunk
         }
         if (OUT == OUT_QKV_ATTN) {
             ptx::mbar_init(&attn_bar[0], 1);
@@ -580,11 +585,16 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
         }
     } else if (any) {
         const Resid rd{OUT == OUT_RESID && r1 - r0 <= kResidRows ? resid_s : nullptr, r0, r1 - r0};
-        // Chunk j goes to warp j % 8.  A warp may run more than one ring lap
-        // ahead of the slowest one, so before the parity wait it waits until
-        // the producer has ISSUED chunk j: that happens only after chunk j - NS
-        // was consumed, hence landed, so the slot is then in chunk j's phase.
-        for (int j = warp; j < n_chunks; j += kCW) {
+        // Unit v (chunk v / UPC) goes to warp v % 8.  A warp may run more than
+        // one ring lap ahead of the slowest one, so before the parity wait it
+        // waits until the producer has ISSUED chunk j: that happens only after
+        // chunk j - NS was consumed, hence landed, so the slot is then in chunk
+        // j's phase.  The last unit of a short chunk arrives for the units the
+        // chunk lacks.
+        const int last_n = (r1 - r0) - (n_chunks - 1) * R;
+        const int n_units = n_chunks > 0 ? (n_chunks - 1) * UPC + (kPair ? last_n : (last_n + 1) / 2) : 0;
+        for (int v = warp; v < n_units; v += kCW) {
+            const int j = v / UPC, k = v % UPC;
             const int slot = j % NS;
             bool ok = !abort_s;
             if (ok && issued_s <= j) {
@@ -605,15 +615,18 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
                 }
                 break;
             }
-            const int row0 = r0 + j * R;
+            const int row0 = r0 + j * R, n = min(R, r1 - row0);
+            const int units = kPair ? n : (n + 1) / 2;
             const uint4 *stage = reinterpret_cast<const uint4 *>(smem + (size_t)slot * kStage);
-            if (kPair)
-                stage_pairs<NB, WB>(a, stage, row0, min(R, r1 - row0), CPR, b0, xs, rs, live_s);
-            else
-                stage_rows<NB, OUT, WB>(a, stage, row0, min(R, r1 - row0), CPR, b0, xs, rs, live_s, rd, best_v,
-                                        best_i);
+            if (kPair) {
+                stage_pairs<NB, WB>(a, stage, row0, n, k, k + 1, CPR, b0, xs, rs, live_s);
+            } else {
+                const int rr = 2 * k, nr = min(2, n - rr);
+                stage_rows<NB, OUT, WB>(a, stage + (size_t)rr * CPR, row0 + rr, nr, CPR, b0, xs, rs, live_s, rd,
+                                        best_v, best_i);
+            }
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&empty[slot]);
+            if (lane == 0) ptx::mbar_arrive_cnt(&empty[slot], k == units - 1 ? (uint32_t)(UPC - units + 1) : 1u);
         }
     }
     __syncthreads();
