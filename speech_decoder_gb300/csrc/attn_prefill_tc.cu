@@ -36,19 +36,29 @@ constexpr uint32_t kTile = 2 * kAtom;    // a 128 x 128 fp16 tile
 constexpr uint64_t kWaitNs = 200000000ull;
 constexpr uint32_t kTmemCols = 512;      // S of even key tiles, O, S of odd key tiles (one CTA per SM)
 
+constexpr float kLazy = 8.f;             // log2 headroom before the running output is rescaled
+
 struct Smem {                            // offsets into the 1024-aligned dynamic shared memory
     static constexpr uint32_t q = 0;
     static constexpr uint32_t k = q + kTile;           // [2] stages
     static constexpr uint32_t vt = k + 2 * kTile;      // [2] stages
-    static constexpr uint32_t p = vt + 2 * kTile;
-    static constexpr uint32_t bytes = p + kTile;
+    static constexpr uint32_t p = vt + 2 * kTile;      // [2] buffers
+    static constexpr uint32_t bytes = p + 2 * kTile;
 };
 
 struct Sync {
-    uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], p_ready, pv_done;
+    uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], p_ready[2], pv_done[2];
     uint32_t tmem;
     int abort;
 };
+
+// 2^x on the special-function unit (max relative error about 2^-22; the
+// probabilities are rounded to fp16 right after)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __device__ __forceinline__ bool wait_bar(Sync &sy, uint64_t *bar, uint32_t parity, int *err, int code) {
     if (*(volatile int *)&sy.abort) return false;
@@ -80,10 +90,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&sy.kv_full[s], 1);
             ptx::mbar_init(&sy.kv_empty[s], 1);
         }
-        ptx::mbar_init(&sy.s_full[0], 1);
-        ptx::mbar_init(&sy.s_full[1], 1);
-        ptx::mbar_init(&sy.p_ready, 128);
-        ptx::mbar_init(&sy.pv_done, 1);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&sy.s_full[b], 1);
+            ptx::mbar_init(&sy.p_ready[b], 128);
+            ptx::mbar_init(&sy.pv_done[b], 1);
+        }
         sy.abort = 0;
         ptx::fence_mbar_init();
     }
@@ -135,16 +146,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < n_kt; ++j) {
                 const int s = j & 1;
                 if (j + 1 < n_kt && !issue_s(j + 1)) break;
-                if (!wait_bar(sy, &sy.p_ready, j & 1, a.err, 24)) break;
+                if (!wait_bar(sy, &sy.p_ready[j & 1], (j >> 1) & 1, a.err, 24)) break;
                 tc_fence_after();
-                const uint32_t pb = sbase + Smem::p, vb = sbase + Smem::vt + s * kTile;
+                const uint32_t pb = sbase + Smem::p + (j & 1) * kTile, vb = sbase + Smem::vt + s * kTile;
 #pragma unroll
                 for (int k = 0; k < kBK / 16; ++k) {
                     const uint32_t off = (k >> 2) * kAtom + (k & 3) * 32;
                     mma_f16(tO, sw128_desc(pb + off), sw128_desc(vb + off), idesc, (j | k) != 0);
                 }
                 mma_commit(&sy.kv_empty[s]);
-                mma_commit(&sy.pv_done);
+                mma_commit(&sy.pv_done[j & 1]);
             }
         }
     } else if (warp >= 2) {
@@ -156,7 +167,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = r < n_rows;
         const float c2 = a.scale * 1.4426950408889634f;     // scores to log2 units
         // tcgen05.ld / st are warp-collective (.sync.aligned): every decision
-        // that guards them is made uniform across the warp
+        // that guards them is made uniform across the warp.
+        // Lazy rescaling: probabilities are exp2(s - m) against a reference
+        // max m that moves only when a row's scores exceed it by more than
+        // kLazy (then the running output is rescaled once); otherwise P may
+        // reach 2^kLazy, exact enough in fp16 and summed in fp32.  P is
+        // double-buffered, so tile j + 1's softmax overlaps tile j's P . V.
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_kt && ok; ++j) {
@@ -172,23 +188,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sv[c] = vis ? sv[c] * c2 : -INFINITY;
                 mx = fmaxf(mx, sv[c]);
             }
-            const float m_new = fmaxf(m, mx);
-            const float corr = m_new == -INFINITY ? 1.f : exp2f(m - m_new);
+            const bool resc = __any_sync(0xffffffffu, mx > m + kLazy);
+            float corr = 1.f;
+            if (resc) {
+                const float m_new = fmaxf(m, mx);
+                corr = m == -INFINITY ? 0.f : ex2(m - m_new);
+                m = m_new;
+            }
             float ls = 0.f;
 #pragma unroll
             for (int c = 0; c < kBK; ++c) {
-                sv[c] = m_new == -INFINITY ? 0.f : exp2f(sv[c] - m_new);
+                sv[c] = m == -INFINITY ? 0.f : ex2(sv[c] - m);
                 ls += sv[c];
             }
             l = l * corr + ls;
-            m = m_new;
-            // the previous P . V has finished reading P and writing O
-            if (j > 0) {
-                ok = __all_sync(0xffffffffu, wait_bar(sy, &sy.pv_done, (j - 1) & 1, a.err, 26));
+            // P buffer j & 1 was last read by P . V of tile j - 2
+            if (j >= 2) {
+                ok = __all_sync(0xffffffffu,
+                                wait_bar(sy, &sy.pv_done[j & 1], ((j >> 1) - 1) & 1, a.err, 26));
                 if (!ok) break;
-                tc_fence_after();
             }
-            unsigned char *prow = sm + Smem::p;
+            unsigned char *prow = sm + Smem::p + (j & 1) * kTile;
 #pragma unroll
             for (int c8 = 0; c8 < kBK / 8; ++c8) {
                 uint32_t w[4];
@@ -200,7 +220,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int at = c8 >> 3, ch = c8 & 7;
                 *reinterpret_cast<uint4 *>(prow + at * kAtom + sw128_offset(r, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
             }
-            if (j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {   // rescale the running output (whole warp)
+            if (j > 0 && resc) {                            // rescale the running output (whole warp)
+                // every earlier P . V has written O
+                ok = __all_sync(0xffffffffu,
+                                wait_bar(sy, &sy.pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, a.err, 28));
+                if (!ok) break;
+                tc_fence_after();
                 float t[kD];
                 tmem_ld128(tO + lane_off, t);
 #pragma unroll
@@ -209,9 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_async_smem();
             tc_fence_before();
-            ptx::mbar_arrive(&sy.p_ready);
+            ptx::mbar_arrive(&sy.p_ready[j & 1]);
         }
-        if (ok) ok = __all_sync(0xffffffffu, wait_bar(sy, &sy.pv_done, (n_kt - 1) & 1, a.err, 27));
+        if (ok)
+            ok = __all_sync(0xffffffffu,
+                            wait_bar(sy, &sy.pv_done[(n_kt - 1) & 1], ((n_kt - 1) >> 1) & 1, a.err, 27));
         tc_fence_after();
         if (ok) {                                           // whole warp loads; rows past the tile do not store
             const float inv = row_ok ? 1.f / l : 0.f;
