@@ -165,15 +165,19 @@ def kernel_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic():
+def ncu_traffic(spec):
     """Per-launch DRAM bytes of the dominant kernel from the committed ncu
-    summary, or None when the kernel source changed since it was taken."""
+    summary, or None when the kernel source changed since it was taken or the
+    model's projection shapes differ from the captured ones."""
     path = os.path.join(ROOT, "profiles", "gemv_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     if d.get("kernel_sha") != kernel_sha():
+        return None
+    shape = d.get("shape", {})
+    if any(getattr(spec, k) != v for k, v in shape.items()) or not shape:
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -328,7 +332,7 @@ def run_ours(args):
     roof = {"kernel": kname, "bound": "hbm",
             "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4),
             "peak_source": peak_kind, "bytes_per_launch": int(kbytes), "avg_launch_us": round(kms * 1e3, 2),
-            "traffic": ncu_traffic() if B == 1 and spec.weight_dtype == "bf16" else None}
+            "traffic": ncu_traffic(spec) if B == 1 and spec.weight_dtype == "bf16" else None}
     kv_mean = float(np.mean([t + wl.steps / 2 for t in Ts]))
     step_bytes = decode_bytes_per_step(spec, kv_mean, B)
     steps_done = n_tok / B
@@ -385,7 +389,8 @@ def run_ours(args):
             "config": {"workload": wl.name, "prompt_rows": T_all,
                        "layout": [[p.prefix_len, p.n_audio, p.suffix_len] for p in wl.prompts][:4],
                        "decode_steps": wl.steps, "batch": wl.batch, "parallelism": f"replicas x{world}",
-                       "l2": "inputs larger than L2: every step streams 3.4 GB of weights"},
+                       "l2": "inputs larger than L2: every step streams %.1f GB of weights" % (
+                           decode_bytes_per_step(spec, 0.0, 1) / 1e9)},
             "prefill": {"value": round(prefill_tok_s, 1), "unit": "tok/s", "ms": round(pre_ms / args.steps, 3),
                         "roofline": pre_roof},
             "prefill_long": long,

@@ -67,7 +67,7 @@ def test_kernel_hash_ignores_comments_but_not_code(tmp_path, monkeypatch):
     assert "kAutoStages = 11" in f.read_text()
     assert bench.kernel_sha() != base
     # a record keyed to other sources is not reported
-    assert bench.ncu_traffic() is None
+    assert bench.ncu_traffic(synth.workload("qwen3-1.7b-t152").model) is None
 
 
 def test_traffic_record_is_well_formed():
@@ -79,8 +79,10 @@ def test_traffic_record_is_well_formed():
     # DRAM bytes are at least the algorithmic bytes (weights are read once)
     assert d["dram_bytes_per_launch"] >= d["algorithmic_bytes_per_launch"]
     assert "--clock-control none" in d["command"]
-    t = bench.ncu_traffic()
+    t = bench.ncu_traffic(synth.workload("qwen3-1.7b-t152").model)
     assert t is None or t == d["dram_bytes_per_launch"]
+    # only reported for the projection shapes it was captured on
+    assert bench.ncu_traffic(synth.workload("qwen3-0.6b-t153").model) is None
 
 
 def test_prefill_work_counts_rows_pairs_and_slice_last():
