@@ -50,25 +50,6 @@ __device__ __forceinline__ uint32_t sw_off(int row, int c) {
     return (uint32_t)(row * 128 + ((c ^ (row & 7)) << 4));
 }
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// a float of CTA `rank`'s shared memory at the address of `local` in this CTA
-__device__ __forceinline__ float ld_cluster(const float *local, uint32_t rank) {
-    uint32_t a = ptx::smem_u32(local), r;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r) : "memory");
-    return v;
-}
-
 template <int NREP>
 __global__ void __launch_bounds__(kCThreads, 1)
     k_attn_cluster(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnDecArgs a,
@@ -79,7 +60,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
     constexpr int PL = kCD / 32;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int S = gridDim.x, g = blockIdx.y, b = blockIdx.z;
-    const uint32_t rank = cluster_rank();
+    const uint32_t rank = ptx::cluster_rank();
     const int s = (int)rank;
     if (tid == 0) {
         ptx::mbar_init(&sm.bar, 1);
@@ -236,7 +217,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
         sm.acc[r][i] = sm.accp[0][r][i] + sm.accp[1][r][i];
     }
     // every CTA's (m, l, acc) complete and visible to the cluster
-    cluster_sync();
+    ptx::cluster_sync();
     // combine: CTA s normalises output elements [s E / S, (s + 1) E / S)
     {
         constexpr int E = NREP * kCD;
@@ -244,13 +225,13 @@ __global__ void __launch_bounds__(kCThreads, 1)
         for (int idx = e0 + tid; idx < e1; idx += kCThreads) {
             const int r = idx / kCD, i = idx % kCD;
             float M = -INFINITY;
-            for (int t = 0; t < S; ++t) M = fmaxf(M, ld_cluster(&sm.m[r], t));
+            for (int t = 0; t < S; ++t) M = fmaxf(M, ptx::ld_cluster(&sm.m[r], t));
             float L = 0.f, O = 0.f;
             for (int t = 0; t < S; ++t) {
-                const float mt = ld_cluster(&sm.m[r], t);
+                const float mt = ptx::ld_cluster(&sm.m[r], t);
                 const float w = mt == -INFINITY ? 0.f : expf(mt - M);
-                L = fmaf(w, ld_cluster(&sm.l[r], t), L);
-                O = fmaf(w, ld_cluster(&sm.acc[r][i], t), O);
+                L = fmaf(w, ptx::ld_cluster(&sm.l[r], t), L);
+                O = fmaf(w, ptx::ld_cluster(&sm.acc[r][i], t), O);
             }
             const size_t oi = (size_t)b * a.nq * kCD + (size_t)(g * NREP + r) * kCD + i;
             a.o[oi] = O / L;
@@ -258,7 +239,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
         }
     }
     // no CTA leaves while another may still read its shared memory
-    cluster_sync();
+    ptx::cluster_sync();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_cl_encode = nullptr;

@@ -89,6 +89,30 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
+// Thread-block clusters: this CTA's rank, a barrier of every thread of the
+// cluster (release / acquire: shared-memory writes before it are visible to
+// the cluster's reads after it), and a float of CTA `rank`'s shared memory at
+// the address of `local` in this CTA (distributed shared memory).
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ld_cluster(const float *local, uint32_t rank) {
+    uint32_t a = smem_u32(local), r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    float v;
+    // volatile: stays after the cluster barrier that precedes it; no memory
+    // clobber, so independent loads issue back to back
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r));
+    return v;
+}
+
 // Programmatic dependent launch: wait for the preceding grid's results /
 // allow the following grid to start launching.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

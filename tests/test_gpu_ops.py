@@ -124,6 +124,9 @@ def run_gemm(lib, X, W, epi, use_tc, splits=0, C0=None):
 GEMMS = [  # T, N, K, splits (0 = automatic)
     (16, 512, 256, 0), (152, 4096, 2048, 0), (152, 2048, 6144, 0), (1, 256, 512, 0), (700, 1024, 512, 0),
     (8015, 256, 256, 0), (37, 384, 1408, 3), (152, 128, 64, 1), (300, 768, 192, 2),
+    # split-K: 5 splits of uneven length, two prompt-row tiles (the second ragged) with 8 splits,
+    # 12 splits of the down projection's K
+    (152, 4096, 2048, 5), (400, 384, 1024, 0), (152, 2048, 6144, 12),
     # long prompts: the persistent kernel (tiles of 256 weight rows x 128 prompt rows, several per CTA;
     # ragged last prompt-row tile; K = 6144 as in the down projection)
     (8015, 12288, 2048, 0), (2048, 4096, 2048, 0), (1500, 2048, 6144, 0),
