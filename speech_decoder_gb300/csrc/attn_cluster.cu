@@ -40,8 +40,12 @@ struct ClSmem {
     float qs[NREP][kCD];               // normed, rotated queries
     float p[NREP][kCT];                // scores, then exp(score - m)
     float accp[2][NREP][kCD];          // P V of the two key halves
-    float acc[NREP][kCD];              // this CTA's sum_k exp(s_k - m) v_k (read by the cluster)
-    float m[NREP], l[NREP];            // this CTA's max score and sum of exp (read by the cluster)
+    // the cluster's partial results for this CTA's output slice, pushed by
+    // every CTA t of the cluster: in_acc[t][j] (sum_k exp(s_k - m_t) v_k for
+    // element e0 + j of the slice), in_m[t][r] / in_l[t][r] (CTA t's max score
+    // and sum of exp of head r)
+    float in_acc[NREP * kCD];
+    float in_m[kCMaxSplits][NREP], in_l[kCMaxSplits][NREP];
     uint64_t bar;
 };
 
@@ -73,9 +77,22 @@ __global__ void __launch_bounds__(kCThreads, 1)
     ptx::pdl_launch();
     ptx::pdl_wait();
 
+    // the row's raw projections, in flight with the state: warp r < NREP the
+    // query of head g n_rep + r, warps NREP and NREP + 1 the key and value
+    // (used by the split that owns slot n_past)
+    const size_t ldq = (size_t)(a.nq + 2 * a.nkv) * kCD;
+    const float *row = a.qkv + (size_t)b * ldq;
+    float raw[PL];
+    if (warp < NREP + 2) {
+        const int hrow = warp < NREP ? g * NREP + warp : a.nq + (warp == NREP ? 0 : a.nkv) + g;
+        load_vec_cg<PL>(row + (size_t)hrow * kCD + lane * PL, raw);
+    }
     const int pos = a.st->n_past[b], off = a.st->kv_off[b];
     // a finished row: every CTA of the cluster sees the same state and leaves
     if (!row_live(a.st, b)) return;
+    // distributed shared memory may be written only once every CTA of the
+    // cluster runs: arrive now, wait just before the first push
+    ptx::cluster_arrive_relaxed();
     const int len = pos + 1;
     int chunk = (len + S - 1) / S;
     if (chunk > kCT) {                                      // the launch sized S for the capacity: never
@@ -101,8 +118,6 @@ __global__ void __launch_bounds__(kCThreads, 1)
 
     // queries (warp r: head g n_rep + r) and, in the split that owns slot pos,
     // the new key (warp NREP) and value (warp NREP + 1)
-    const size_t ldq = (size_t)(a.nq + 2 * a.nkv) * kCD;
-    const float *row = a.qkv + (size_t)b * ldq;
     float2 cs[PL];
     {
         const float2 *rope_row = a.rope + (size_t)pos * (kCD / 2) + (lane & 15) * PL;
@@ -115,15 +130,12 @@ __global__ void __launch_bounds__(kCThreads, 1)
     }
     __half nh[PL];
     if (warp < NREP) {
-        float v[PL];
-        load_vec_cg<PL>(row + (size_t)(g * NREP + warp) * kCD + lane * PL, v);
-        norm_rope_regs<PL>(v, qw, cs, a.eps, kCD, lane);
+        norm_rope_regs<PL>(raw, qw, cs, a.eps, kCD, lane);
 #pragma unroll
-        for (int e = 0; e < PL; ++e) sm.qs[warp][lane * PL + e] = v[e];
+        for (int e = 0; e < PL; ++e) sm.qs[warp][lane * PL + e] = raw[e];
     } else if (mine && warp < NREP + 2) {
         const bool is_k = warp == NREP;
-        float v[PL];
-        load_vec_cg<PL>(row + (size_t)(a.nq + (is_k ? 0 : a.nkv) + g) * kCD + lane * PL, v);
+        float (&v)[PL] = raw;
         if (is_k) norm_rope_regs<PL>(v, kw, cs, a.eps, kCD, lane);
         __half *pool = reinterpret_cast<__half *>(is_k ? a.Kc : a.Vc) + ((size_t)g * a.slots + off + pos) * kCD;
 #pragma unroll
@@ -172,6 +184,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
         }
     }
     __syncthreads();
+    ptx::cluster_wait();
     // softmax statistics of this CTA's keys: warp r owns head r
     if (warp < NREP) {
         float mx = -INFINITY;
@@ -186,9 +199,10 @@ __global__ void __launch_bounds__(kCThreads, 1)
             sum += e;
         }
         sum = warp_sum(sum);
-        if (lane == 0) {
-            sm.m[warp] = mx;
-            sm.l[warp] = sum;
+        // this head's statistics to every CTA of the cluster
+        if (lane < S) {
+            ptx::st_cluster(&sm.in_m[s][warp], (uint32_t)lane, mx);
+            ptx::st_cluster(&sm.in_l[s][warp], (uint32_t)lane, sum);
         }
     }
     __syncthreads();
@@ -212,34 +226,32 @@ __global__ void __launch_bounds__(kCThreads, 1)
         }
     }
     __syncthreads();
-    for (int idx = tid; idx < NREP * kCD; idx += kCThreads) {
-        const int r = idx / kCD, i = idx % kCD;
-        sm.acc[r][i] = sm.accp[0][r][i] + sm.accp[1][r][i];
+    // CTA t normalises output elements [t E / S, (t + 1) E / S): push this
+    // CTA's partial sums of each element to its owner
+    constexpr int E = NREP * kCD;
+    const int ES = E / S;                          // S divides E (S a power of two up to 8)
+    for (int idx = tid; idx < E; idx += kCThreads) {
+        const int r = idx / kCD, i = idx % kCD, t = idx / ES;
+        ptx::st_cluster(&sm.in_acc[s * ES + (idx - t * ES)], (uint32_t)t, sm.accp[0][r][i] + sm.accp[1][r][i]);
     }
-    // every CTA's (m, l, acc) complete and visible to the cluster
+    // every push complete and visible; afterwards no CTA touches another's
+    // shared memory, so none has to wait for its peers before leaving
     ptx::cluster_sync();
-    // combine: CTA s normalises output elements [s E / S, (s + 1) E / S)
-    {
-        constexpr int E = NREP * kCD;
-        const int e0 = E * s / S, e1 = E * (s + 1) / S;
-        for (int idx = e0 + tid; idx < e1; idx += kCThreads) {
-            const int r = idx / kCD, i = idx % kCD;
-            float M = -INFINITY;
-            for (int t = 0; t < S; ++t) M = fmaxf(M, ptx::ld_cluster(&sm.m[r], t));
-            float L = 0.f, O = 0.f;
-            for (int t = 0; t < S; ++t) {
-                const float mt = ptx::ld_cluster(&sm.m[r], t);
-                const float w = mt == -INFINITY ? 0.f : expf(mt - M);
-                L = fmaf(w, ptx::ld_cluster(&sm.l[r], t), L);
-                O = fmaf(w, ptx::ld_cluster(&sm.acc[r][i], t), O);
-            }
-            const size_t oi = (size_t)b * a.nq * kCD + (size_t)(g * NREP + r) * kCD + i;
-            a.o[oi] = O / L;
-            if (a.o_bf16) store_planes(a.o_bf16, a.o_bf16_lo, oi, O / L);
+    for (int j = tid; j < ES; j += kCThreads) {
+        const int idx = s * ES + j, r = idx / kCD, i = idx % kCD;
+        float M = -INFINITY;
+        for (int t = 0; t < S; ++t) M = fmaxf(M, sm.in_m[t][r]);
+        float L = 0.f, O = 0.f;
+        for (int t = 0; t < S; ++t) {
+            const float mt = sm.in_m[t][r];
+            const float w = mt == -INFINITY ? 0.f : expf(mt - M);
+            L = fmaf(w, sm.in_l[t][r], L);
+            O = fmaf(w, sm.in_acc[t * ES + j], O);
         }
+        const size_t oi = (size_t)b * a.nq * kCD + (size_t)(g * NREP + r) * kCD + i;
+        a.o[oi] = O / L;
+        if (a.o_bf16) store_planes(a.o_bf16, a.o_bf16_lo, oi, O / L);
     }
-    // no CTA leaves while another may still read its shared memory
-    ptx::cluster_sync();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_cl_encode = nullptr;

@@ -113,6 +113,7 @@ struct dec_handle {
     int gemv_ctas = 1;              // GEMV CTAs per SM
     float *tc_scratch = nullptr;    // split-K partial tiles of the tensor-core GEMM
     int pf_bytes = 0;               // L2 look-ahead of the decode GEMVs, bytes per CTA
+    int self_pf = 0;                // rows of its own past the ring a GEMV CTA pulls into L2 at entry
     // persistent step kernel
     StepLayer *step_layers = nullptr;
     CUtensorMap *kv_maps = nullptr;  // [L][2] K and V pool maps of the step kernel's attention tiles
@@ -204,6 +205,8 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     {
         const char *c = std::getenv("SPEECH_DECODER_GEMV_PF_KB");
         h->pf_bytes = (c ? std::max(0, std::min(4096, std::atoi(c))) : 64) * 1024;
+        const char *sp = std::getenv("SPEECH_DECODER_GEMV_SELF_PF_KB");
+        h->self_pf = (sp ? std::max(0, std::min(4096, std::atoi(sp))) : 64) * 1024;
     }
     const size_t ws = wsize(hp), kvs = kvsize(hp), as = ws;   // activations use the weight format
     const size_t H = hp.hidden, d = hp.head_dim, nq = hp.n_heads, nkv = hp.n_kv_heads, F = hp.ffn;
@@ -407,6 +410,7 @@ static void set_prefetch(const dec_handle *h, GemvArgs &g, WSrc W, int N, int K)
     g.pf_K = K;
     g.pf_bytes = h->pf_bytes;
     g.pf_wb = W.scale ? 1 : 2;
+    g.self_pf = h->self_pf;
 }
 
 // Step attention of layer l over the q|k|v rows in qkvd (K/V appended at n_past).

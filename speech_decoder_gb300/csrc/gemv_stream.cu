@@ -187,8 +187,14 @@ template <int NB, int IN, int EPC>
 __device__ void prologue(const GemvArgs &a, float *xs, const float (&nwr)[kNwRegs], int b0, int *live, int CPR,
                          float *sred) {
     const int K = a.K, tid = threadIdx.x;
-    if (tid < kGroupB) live[tid] = tid < NB && b0 + tid < a.B && row_live(a.st, b0 + tid);
-    if (IN == IN_EMBED_NORM) cons_sync();                 // the token ids come from the state
+    // the rows' liveness flags: loaded here, stored to shared memory only after
+    // the activation loads are issued (a store through the generic pointer
+    // first would hold those loads back by a whole memory round trip)
+    const bool lv = tid < kGroupB && tid < NB && b0 + tid < a.B && row_live(a.st, b0 + tid);
+    if (IN == IN_EMBED_NORM) {                            // the token ids come from the state
+        if (tid < kGroupB) live[tid] = lv;
+        cons_sync();
+    }
     // loads in flight per thread and row: one pass over K = 2048, and over
     // K = 6144 (down projection inputs) for a single row
     constexpr int P = (IN == IN_SWIGLU || IN == IN_PLAIN) && NB == 1 ? 24 : 8;
@@ -230,6 +236,7 @@ __device__ void prologue(const GemvArgs &a, float *xs, const float (&nwr)[kNwReg
                 }
             }
         }
+        if (IN != IN_EMBED_NORM && k0 == tid && tid < kGroupB) live[tid] = lv;
         constexpr bool kNorm = IN == IN_NORM || IN == IN_EMBED_NORM;
         static_assert(!kNorm || P <= kNwRegs, "the first pass's norm weights are the registers");
 #pragma unroll
@@ -495,6 +502,22 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
     const int pre = min(NS, n_chunks);
     if (warp == kCW && lane == 0) {
         for (int g = 0; g < pre; ++g) issue(g);          // weights: no dependency on earlier kernels
+        // the rows the ring cannot hold yet, into L2, so HBM keeps streaming
+        // while the consumers wait for their inputs
+        int left = a.self_pf;
+        for (int g = pre; g < n_chunks && left > 0; ++g) {
+            const int u = r0 + g * R, n = min(R, r1 - u);
+            if (kPair) {
+                const size_t grow = (size_t)(u >> 7) * 256 + (u & 127);
+                const uint32_t half = (uint32_t)(n * rb);
+                ptx::bulk_prefetch_l2(W + grow * rb, half);
+                ptx::bulk_prefetch_l2(W + (grow + 128) * rb, half);
+                left -= 2 * (int)half;
+            } else {
+                ptx::bulk_prefetch_l2(W + (size_t)u * rb, (uint32_t)(n * rb));
+                left -= n * (int)rb;
+            }
+        }
         // this layer's cached keys and values, for the attention that follows:
         // one (sequence, kv head, K or V) range per CTA, pulled into L2.  The
         // state may still be changing (a hint only); ranges are clamped to the pool.

@@ -103,6 +103,12 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// the two halves of a cluster barrier, with work between them
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ float ld_cluster(const float *local, uint32_t rank) {
     uint32_t a = smem_u32(local), r;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
@@ -111,6 +117,13 @@ __device__ __forceinline__ float ld_cluster(const float *local, uint32_t rank) {
     // clobber, so independent loads issue back to back
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(r));
     return v;
+}
+
+// a float into CTA `rank`'s shared memory at the address of `local` in this CTA
+__device__ __forceinline__ void st_cluster(float *local, uint32_t rank, float v) {
+    uint32_t a = smem_u32(local), r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(r), "f"(v) : "memory");
 }
 
 // Programmatic dependent launch: wait for the preceding grid's results /
