@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kCThreads, 1)
     {
         const int kk = tid & (kCT - 1);
         for (int r = tid / kCT; r < NREP; r += kCThreads / kCT) {
-            float d = 0.f;
+            float d = 0.f, e = 0.f;                 // two FMA chains
             if (kk < nk) {
 #pragma unroll
                 for (int c = 0; c < kCD / 8; ++c) {
@@ -174,12 +174,13 @@ __global__ void __launch_bounds__(kCThreads, 1)
                     d = fmaf(f[1], q0.y, d);
                     d = fmaf(f[2], q0.z, d);
                     d = fmaf(f[3], q0.w, d);
-                    d = fmaf(f[4], q1.x, d);
-                    d = fmaf(f[5], q1.y, d);
-                    d = fmaf(f[6], q1.z, d);
-                    d = fmaf(f[7], q1.w, d);
+                    e = fmaf(f[4], q1.x, e);
+                    e = fmaf(f[5], q1.y, e);
+                    e = fmaf(f[6], q1.z, e);
+                    e = fmaf(f[7], q1.w, e);
                 }
             }
+            d += e;
             sm.p[r][kk] = kk < nk ? d * scale : -INFINITY;
         }
     }
@@ -213,16 +214,28 @@ __global__ void __launch_bounds__(kCThreads, 1)
             const int h = idx / PER, rem = idx % PER, r = rem >> 6, dp = rem & 63;
             const int d0 = 2 * dp, part = d0 >> 6, col = d0 & 63;
             const unsigned char *vb = reinterpret_cast<const unsigned char *>(&sm.V[part][0][0]);
-            float a0 = 0.f, a1 = 0.f;
-            for (int kk = h; kk < nk; kk += 2) {
-                const __half2 v = *reinterpret_cast<const __half2 *>(vb + sw_off(kk, col >> 3) + (col & 7) * 2);
-                const float2 vf = __half22float2(v);
-                const float pk = sm.p[r][kk];
-                a0 = fmaf(pk, vf.x, a0);
-                a1 = fmaf(pk, vf.y, a1);
+            // keys h, h + 2, ...: two pairs of accumulators, four loads in flight
+            float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+            const unsigned char *vc = vb + (col & 7) * 2;
+            int kk = h;
+#pragma unroll 2
+            for (; kk + 2 < nk; kk += 4) {
+                const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(vc + sw_off(kk, col >> 3)));
+                const float2 w = __half22float2(*reinterpret_cast<const __half2 *>(vc + sw_off(kk + 2, col >> 3)));
+                const float pk = sm.p[r][kk], pw = sm.p[r][kk + 2];
+                a0 = fmaf(pk, v.x, a0);
+                a1 = fmaf(pk, v.y, a1);
+                b0 = fmaf(pw, w.x, b0);
+                b1 = fmaf(pw, w.y, b1);
             }
-            sm.accp[h][r][d0] = a0;
-            sm.accp[h][r][d0 + 1] = a1;
+            if (kk < nk) {
+                const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(vc + sw_off(kk, col >> 3)));
+                const float pk = sm.p[r][kk];
+                a0 = fmaf(pk, v.x, a0);
+                a1 = fmaf(pk, v.y, a1);
+            }
+            sm.accp[h][r][d0] = a0 + b0;
+            sm.accp[h][r][d0 + 1] = a1 + b1;
         }
     }
     __syncthreads();
@@ -320,7 +333,11 @@ int attn_cluster_splits(int capacity, int nq, int nkv, int d, bool kv_f16, int B
     if (!g_cl_ready || !kv_f16 || d != kCD || B < 1 || B > kGroupB || nkv < 1 || nq % nkv ||
         (n_rep != 1 && n_rep != 2 && n_rep != 4) || capacity < 1)
         return 0;
+    // the smallest cluster with at most kCT / 2 keys per CTA (scores and P V
+    // are latency-bound loops over the CTA's keys), at most 8 CTAs, at least
+    // enough for the whole context at kCT keys per CTA
     int S = 1;
+    while (S * (kCT / 2) < capacity && S < kCMaxSplits) S *= 2;
     while (S * kCT < capacity) S *= 2;
     return S <= kCMaxSplits ? S : 0;
 }

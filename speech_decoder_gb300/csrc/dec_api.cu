@@ -113,7 +113,7 @@ struct dec_handle {
     int gemv_ctas = 1;              // GEMV CTAs per SM
     float *tc_scratch = nullptr;    // split-K partial tiles of the tensor-core GEMM
     int pf_bytes = 0;               // L2 look-ahead of the decode GEMVs, bytes per CTA
-    int self_pf = 0;                // rows of its own past the ring a GEMV CTA pulls into L2 at entry
+    int pre_bulk = 0;               // ring chunks a GEMV copies before its dependency wait (0: all)
     // persistent step kernel
     StepLayer *step_layers = nullptr;
     CUtensorMap *kv_maps = nullptr;  // [L][2] K and V pool maps of the step kernel's attention tiles
@@ -205,8 +205,8 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     {
         const char *c = std::getenv("SPEECH_DECODER_GEMV_PF_KB");
         h->pf_bytes = (c ? std::max(0, std::min(4096, std::atoi(c))) : 64) * 1024;
-        const char *sp = std::getenv("SPEECH_DECODER_GEMV_SELF_PF_KB");
-        h->self_pf = (sp ? std::max(0, std::min(4096, std::atoi(sp))) : 64) * 1024;
+        const char *pb = std::getenv("SPEECH_DECODER_GEMV_PRE");
+        h->pre_bulk = pb ? std::max(0, std::min(64, std::atoi(pb))) : 8;
     }
     const size_t ws = wsize(hp), kvs = kvsize(hp), as = ws;   // activations use the weight format
     const size_t H = hp.hidden, d = hp.head_dim, nq = hp.n_heads, nkv = hp.n_kv_heads, F = hp.ffn;
@@ -404,13 +404,13 @@ static double wbytes(const dec_handle *h, int B) { return e4m3_step(h, B) ? 1.0 
 
 // The GEMV that runs next streams W [N, K]: let this one pull its first rows into L2.
 static void set_prefetch(const dec_handle *h, GemvArgs &g, WSrc W, int N, int K) {
+    g.pre_bulk = h->pre_bulk;
     if (!h->w_bf16 || h->pf_bytes <= 0) return;
     g.pf = W.W;
     g.pf_N = N;
     g.pf_K = K;
     g.pf_bytes = h->pf_bytes;
     g.pf_wb = W.scale ? 1 : 2;
-    g.self_pf = h->self_pf;
 }
 
 // Step attention of layer l over the q|k|v rows in qkvd (K/V appended at n_past).

@@ -61,7 +61,7 @@ struct GemvArgs {
     const void *pf;
     int pf_N, pf_K, pf_bytes;
     int pf_wb;              // bytes per weight of the next kernel's rows (0: 2, bf16)
-    int self_pf;            // bytes per CTA of its own rows past the ring's first fill pulled into L2 at entry
+    int pre_bulk;           // ring chunks copied before the dependency wait (0: the whole first fill)
     // KV of this layer pulled into L2 for the attention that follows (may be null)
     const void *kvp_K, *kvp_V;
     int kvp_slots, kvp_nkv, kvp_row_bytes;

@@ -44,6 +44,7 @@ constexpr int kMaxStages = 12;
 constexpr int kAutoStages = 12;               // 192 KB in flight per SM covers the loaded HBM latency
 constexpr uint64_t kWaitNs = 200000000ull;    // every wait gives up after 0.2 s
 constexpr int kBarCons = 1;                   // named barrier of the consumer warps
+constexpr int kBarProd = 2;                   // consumers arrive, the producer warp waits: prologue published
 
 __device__ __forceinline__ void cons_sync() { ptx::named_bar_sync(kBarCons, kCT); }
 
@@ -499,25 +500,27 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
         __threadfence_block();
         issued_s = g + 1;
     };
-    const int pre = min(NS, n_chunks);
+    // chunk g's rows into L2 only (no copy to shared memory)
+    auto pf_chunk = [&](int g) {
+        const int u = r0 + g * R, n = min(R, r1 - u);
+        if (kPair) {
+            const size_t grow = (size_t)(u >> 7) * 256 + (u & 127);
+            const uint32_t half = (uint32_t)(n * rb);
+            ptx::bulk_prefetch_l2(W + grow * rb, half);
+            ptx::bulk_prefetch_l2(W + (grow + 128) * rb, half);
+        } else {
+            ptx::bulk_prefetch_l2(W + (size_t)u * rb, (uint32_t)(n * rb));
+        }
+    };
+    // Before the dependency wait only the first a.pre_bulk chunks are copied
+    // into the ring; the rest of the ring's first fill goes to L2 and is
+    // copied after the consumers' activation loads: bulk copies in flight to
+    // this SM would queue those loads behind up to 192 KB of weights.
+    const int fill = min(NS, n_chunks);
+    const int pre = a.pre_bulk > 0 ? min(a.pre_bulk, fill) : fill;
     if (warp == kCW && lane == 0) {
         for (int g = 0; g < pre; ++g) issue(g);          // weights: no dependency on earlier kernels
-        // the rows the ring cannot hold yet, into L2, so HBM keeps streaming
-        // while the consumers wait for their inputs
-        int left = a.self_pf;
-        for (int g = pre; g < n_chunks && left > 0; ++g) {
-            const int u = r0 + g * R, n = min(R, r1 - u);
-            if (kPair) {
-                const size_t grow = (size_t)(u >> 7) * 256 + (u & 127);
-                const uint32_t half = (uint32_t)(n * rb);
-                ptx::bulk_prefetch_l2(W + grow * rb, half);
-                ptx::bulk_prefetch_l2(W + (grow + 128) * rb, half);
-                left -= 2 * (int)half;
-            } else {
-                ptx::bulk_prefetch_l2(W + (size_t)u * rb, (uint32_t)(n * rb));
-                left -= n * (int)rb;
-            }
-        }
+        for (int g = pre; g < fill; ++g) pf_chunk(g);
         // this layer's cached keys and values, for the attention that follows:
         // one (sequence, kv head, K or V) range per CTA, pulled into L2.  The
         // state may still be changing (a hint only); ranges are clamped to the pool.
@@ -559,8 +562,13 @@ __global__ void __launch_bounds__(kTT, OUT == OUT_QKV_ATTN ? 1 : 2) k_gemv_strea
         if (rpre && b0 + tid / nres < a.B) rv0 = a.out[(size_t)(b0 + tid / nres) * a.N + r0 + tid % nres];
         prologue<NB, IN, 16 / WB>(a, xs, nwr, b0, live_s, CPR, sred);
         if (rpre) resid_s[tid] = rv0;
+        // rows, partial sums, live_s, resid_s: published to the consumers
+        // without waiting for the producer, which may still be issuing copies
+        ptx::named_bar_arrive(kBarProd, kTT);
+        cons_sync();
+    } else {
+        ptx::named_bar_sync(kBarProd, kTT);               // the producer needs live_s
     }
-    __syncthreads();                                      // rows, partial sums, live_s, resid_s
     bool any = false;
 #pragma unroll
     for (int b = 0; b < NB; ++b) any |= live_s[b] != 0;

@@ -2,7 +2,8 @@
 head, the keys split over the cluster's CTAs and combined through
 distributed shared memory) against the oracle and against the split-KV
 attention kernel, for every cluster size the context capacity selects
-(1, 2, 4, 8 CTAs) and 1, 2 and 4 query heads per KV head."""
+(1, 2, 4, 8 CTAs, and 8 CTAs holding up to 128 keys each) and 1, 2 and 4
+query heads per KV head."""
 import os
 
 import numpy as np
@@ -38,13 +39,14 @@ def make(spec, w, attn=None, **kw):
 
 
 HEADS = [(2, 2), (4, 2), (8, 2)]            # (query heads, KV heads): n_rep 1, 2, 4
-# (prompt, context capacity): one, two, four and eight CTAs per cluster (128 keys each)
-SIZES = [(synth.Prompt(3, 60, 2), 100), (synth.Prompt(5, 170, 4), 250), (synth.Prompt(9, 400, 6), 500),
-         (synth.Prompt(9, 850, 6), 1000)]
+# (prompt, context capacity): one, two, four and eight CTAs per cluster (up to 64 keys each while
+# the cluster can grow), and eight CTAs of up to 128 keys each
+SIZES = [(synth.Prompt(3, 40, 2), 60), (synth.Prompt(3, 60, 2), 100), (synth.Prompt(5, 170, 4), 250),
+         (synth.Prompt(9, 400, 6), 500), (synth.Prompt(9, 850, 6), 1000)]
 
 
 @pytest.mark.parametrize("heads", HEADS, ids=[f"q{a}kv{b}" for a, b in HEADS])
-@pytest.mark.parametrize("size", SIZES, ids=["S1", "S2", "S4", "S8"])
+@pytest.mark.parametrize("size", SIZES, ids=["S1", "S2", "S4", "S8", "S8full"])
 def test_cluster_attention_teacher_forced(heads, size):
     nq, nkv = heads
     prompt, cap = size
