@@ -261,7 +261,31 @@ __global__ void __launch_bounds__(512) k_argmax_rows(const float *logits, int V,
     const float *row = logits + (size_t)b * V;
     float bv = -INFINITY;
     int bix = 0x7fffffff;
-    for (int i = tid; i < V; i += blockDim.x) {
+    int i0 = 0;
+    if ((V & 3) == 0) {
+        // float4 loads, eight in flight per thread; each thread still visits
+        // its indices in ascending order
+        const float4 *r4 = reinterpret_cast<const float4 *>(row);
+        const int V4 = V >> 2, nt = (int)blockDim.x;
+        for (int base = tid; base < V4; base += 8 * nt) {
+            float4 v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = base + u * nt;
+                v[u] = i < V4 ? __ldcg(r4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = 4 * (base + u * nt);
+                if (v[u].x > bv) { bv = v[u].x; bix = i; }
+                if (v[u].y > bv) { bv = v[u].y; bix = i + 1; }
+                if (v[u].z > bv) { bv = v[u].z; bix = i + 2; }
+                if (v[u].w > bv) { bv = v[u].w; bix = i + 3; }
+            }
+        }
+        i0 = V;
+    }
+    for (int i = i0 + tid; i < V; i += blockDim.x) {
         const float v = __ldcg(row + i);
         if (v > bv) { bv = v; bix = i; }
     }
