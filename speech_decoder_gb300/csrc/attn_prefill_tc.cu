@@ -181,13 +181,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             float sv[kBK];
             tmem_ld128(tS(j) + lane_off, sv);
+            // raw scores; the positive scale is applied to the maximum and
+            // folded into the exponent's FMA.  A tile wholly inside every
+            // row's causal range (warp-uniform test) needs no mask.
             float mx = -INFINITY;
+            if ((j + 1) * kBK - 1 <= pos0 + 32 * quarter && 32 * quarter + 31 < n_rows) {
 #pragma unroll
-            for (int c = 0; c < kBK; ++c) {
-                const bool vis = row_ok && j * kBK + c <= qpos;
-                sv[c] = vis ? sv[c] * c2 : -INFINITY;
-                mx = fmaxf(mx, sv[c]);
+                for (int c = 0; c < kBK; ++c) mx = fmaxf(mx, sv[c]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < kBK; ++c) {
+                    const bool vis = row_ok && j * kBK + c <= qpos;
+                    sv[c] = vis ? sv[c] : -INFINITY;
+                    mx = fmaxf(mx, sv[c]);
+                }
             }
+            mx *= c2;
             const bool resc = __any_sync(0xffffffffu, mx > m + kLazy);
             float corr = 1.f;
             if (resc) {
@@ -195,13 +204,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 corr = m == -INFINITY ? 0.f : ex2(m - m_new);
                 m = m_new;
             }
-            float ls = 0.f;
+            const bool none = m == -INFINITY;
+            const float nm = -m;
+            float ls4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < kBK; ++c) {
-                sv[c] = m == -INFINITY ? 0.f : ex2(sv[c] - m);
-                ls += sv[c];
+                sv[c] = none ? 0.f : ex2(fmaf(sv[c], c2, nm));
+                ls4[c & 3] += sv[c];
             }
-            l = l * corr + ls;
+            l = l * corr + ((ls4[0] + ls4[1]) + (ls4[2] + ls4[3]));
             // P buffer j & 1 was last read by P . V of tile j - 2
             if (j >= 2) {
                 ok = __all_sync(0xffffffffu,
