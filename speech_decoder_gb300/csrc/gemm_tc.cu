@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(256) k_splitk_reduce(TcArgs a, int mt) {
 // pass).  The accumulator is double-buffered in TMEM (columns 0-255 and
 // 256-511): the epilogue warps drain tile i while the MMA warp runs tile i + 1,
 // and the TMA producer runs ahead through a ring that spans tile boundaries.
-constexpr int kPtBN = 128;
+constexpr int kPtBN = 128;              // prompt rows per tile (fewer for a short batch of rows: a.BN)
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_gemm_tc_pt(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -298,7 +298,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = a.n_stages;
-    const uint32_t a_bytes = 2u * 16384u, b_bytes = (uint32_t)kPtBN * 128u;
+    const int BN = a.BN;                          // a multiple of 16, at most kPtBN
+    const uint32_t a_bytes = 2u * 16384u, b_bytes = (uint32_t)BN * 128u;
     const uint32_t stage_bytes = a_bytes + (uint32_t)a.planes * b_bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * stage_bytes);
     uint64_t *empty = full + S;
@@ -308,8 +309,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ int abort_s;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int MT = a.n_feat * (a.epi == EPI_SWIGLU_BF16 ? 2 : 1) / 256;   // 256-row weight tiles
-    const int NT = (a.T + kPtBN - 1) / kPtBN;
+    // 256-row weight tiles; the last may be half outside the matrix (its
+    // rows read as zeros, its outputs skipped)
+    const int MT = (a.n_feat * (a.epi == EPI_SWIGLU_BF16 ? 2 : 1) + 255) / 256;
+    const int NT = (a.T + BN - 1) / BN;
     const int tiles = MT * NT;
     const int KT = a.k_tiles;
 
@@ -343,7 +346,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int it = 0;
         bool waited = false;
         for (int t = blockIdx.x; t < tiles && !*(volatile int *)&abort_s; t += gridDim.x) {
-            const int m0 = (t % MT) * 256, n0 = (t / MT) * kPtBN;
+            const int m0 = (t % MT) * 256, n0 = (t / MT) * BN;
             for (int kt = 0; kt < KT; ++kt, ++it) {
                 const int s = it % S;
                 if (it >= S && !ptx::mbar_wait_bounded(&empty[s], ((it / S) - 1) & 1, kTcPolls)) {
@@ -376,7 +379,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (*(volatile int *)&abort_s) break;
             tc_fence_after();
-            const uint32_t acc = tmem + (uint32_t)(buf * 2 * kPtBN);
+            const uint32_t acc = tmem + (uint32_t)(buf * 2 * BN);
             for (int kt = 0; kt < KT; ++kt, ++it) {
                 const int s = it % S;
                 if (!ptx::mbar_wait_bounded(&full[s], (it / S) & 1, kTcPolls)) {
@@ -392,7 +395,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const uint64_t bdesc = sw128_desc(bbase + pl * b_bytes + kk * 32);
 #pragma unroll
                         for (int g = 0; g < 2; ++g)
-                            mma_f16(acc + (uint32_t)(g * kPtBN), sw128_desc(abase + g * 16384 + kk * 32), bdesc,
+                            mma_f16(acc + (uint32_t)(g * BN), sw128_desc(abase + g * 16384 + kk * 32), bdesc,
                                     a.idesc, (kt | kk | pl) != 0);
                     }
                 }
@@ -417,16 +420,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             // warp-uniform: the TMEM loads below are warp-collective
             if (__any_sync(0xffffffffu, !ok || *(volatile int *)&abort_s)) break;
             tc_fence_after();
-            const int mt = t % MT, n0 = (t / MT) * kPtBN;
-            const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 2 * kPtBN);
+            const int mt = t % MT, n0 = (t / MT) * BN;
+            const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 2 * BN);
             const bool swiglu = a.epi == EPI_SWIGLU_BF16;
             const int f = swiglu ? mt * 128 + r : mt * 256 + r;
-            for (int c = 0; c < kPtBN; c += 32) {
+            int c = 0;
+            for (; c + 32 <= BN; c += 32) {
                 float v[32], u[32];
                 tmem_ld32(tq + c, v);
-                tmem_ld32(tq + kPtBN + c, u);
+                tmem_ld32(tq + BN + c, u);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
+                    epi_store(a, f, n0 + c + j, v[j], u[j]);
+                    if (!swiglu) epi_store(a, f + 128, n0 + c + j, u[j], 0.f);
+                }
+            }
+            if (c < BN) {                                // a 16-column remainder
+                float v[16], u[16];
+                tmem_ld16(tq + c, v);
+                tmem_ld16(tq + BN + c, u);
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
                     epi_store(a, f, n0 + c + j, v[j], u[j]);
                     if (!swiglu) epi_store(a, f + 128, n0 + c + j, u[j], 0.f);
                 }
@@ -481,9 +495,10 @@ void init_gemm_tc() {
 
 bool gemm_tc_ready() { return g_tc_ready; }
 
-// persistent form: stages of 256 weight rows + planes x 128 prompt rows of 64 K each
-static int pt_stages(int planes) {
-    const int stage = 2 * 16384 + planes * kPtBN * 128;
+// persistent form: stages of 256 weight rows + planes x BN prompt rows of 64 K each
+static int pt_bn(int T) { return T >= kPtBN ? kPtBN : (T + 15) / 16 * 16; }
+static int pt_stages(int planes, int BN) {
+    const int stage = 2 * 16384 + planes * BN * 128;
     const int n = (g_pt_max_smem - 1024 - 256) / stage;
     return n > 6 ? 6 : n;
 }
@@ -538,11 +553,17 @@ TcPlan gemm_tc_plan(int T, int n_feat, int K, int groups, int num_sms, size_t sc
 
 // Long prompts with 256-row weight tiles: the persistent kernel (at least one
 // tile per SM, no split-K).
-static bool use_persistent(int T, int n_feat, int K, int groups, int planes, int num_sms, int force_splits) {
-    if (!g_tc_ready || g_pt_max_smem <= 0 || groups != 2 || force_splits > 0 || K % kBK || n_feat % 256) return false;
-    if (pt_stages(planes) < 3) return false;
-    const long long tiles = (long long)(n_feat / 256) * ((T + kPtBN - 1) / kPtBN);
-    return T >= 1024 && tiles >= num_sms;
+// Persistent kernel: at least one 256-row weight tile per SM, no split-K
+// (long prompts; the vocabulary projection of a batch of rows).  SwiGLU
+// needs whole 256-row gate|up blocks; otherwise the last tile may be partial.
+static bool use_persistent(int T, int n_feat, int K, int groups, int epi, int planes, int num_sms,
+                           int force_splits) {
+    if (!g_tc_ready || g_pt_max_smem <= 0 || force_splits > 0 || K % kBK || n_feat % 128) return false;
+    if (epi == EPI_SWIGLU_BF16 && (groups != 2 || n_feat % 256)) return false;
+    const int BN = pt_bn(T);
+    if (pt_stages(planes, BN) < 3) return false;
+    const long long tiles = (long long)((n_feat + 255) / 256) * ((T + BN - 1) / BN);
+    return (T >= 1024 || BN < kPtBN) && tiles >= num_sms;
 }
 
 static bool pt_disabled() {
@@ -560,11 +581,12 @@ cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W
                            const float *bias) {
     if (epi == EPI_BIAS_F32 && !bias) return cudaErrorInvalidValue;
     const int planes = X_lo ? 2 : 1;
-    if (!pt_disabled() && use_persistent(T, n_feat, K, groups, planes, num_sms, force_splits)) {
+    if (!pt_disabled() && use_persistent(T, n_feat, K, groups, epi, planes, num_sms, force_splits)) {
+        const int BN = pt_bn(T);
         CUtensorMap mA, mB, mB2;
         if (!make_map(&mA, W, (uint64_t)n_feat, (uint64_t)K, 256u) ||
-            !make_map(&mB, X, (uint64_t)T, (uint64_t)K, (uint32_t)kPtBN) ||
-            !make_map(&mB2, X_lo ? X_lo : X, (uint64_t)T, (uint64_t)K, (uint32_t)kPtBN))
+            !make_map(&mB, X, (uint64_t)T, (uint64_t)K, (uint32_t)BN) ||
+            !make_map(&mB2, X_lo ? X_lo : X, (uint64_t)T, (uint64_t)K, (uint32_t)BN))
             return cudaErrorInvalidValue;
         TcArgs a{};
         a.n_feat = epi == EPI_SWIGLU_BF16 ? n_feat / 2 : n_feat;
@@ -572,8 +594,8 @@ cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W
         a.K = K;
         a.groups = 2;
         a.planes = planes;
-        a.BN = kPtBN;
-        a.n_stages = pt_stages(planes);
+        a.BN = BN;
+        a.n_stages = pt_stages(planes, BN);
         a.k_tiles = K / kBK;
         a.splits = 1;
         a.kt_per_split = a.k_tiles;
@@ -585,13 +607,13 @@ cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W
         a.ldh = ldh;
         a.bias = bias;
         a.err = err;
-        a.idesc = mma_idesc_f16(true, 128, kPtBN);
+        a.idesc = mma_idesc_f16(true, 128, BN);
         a.tmem_cols = 512;
-        const int tiles = (n_feat / 256) * ((T + kPtBN - 1) / kPtBN);
+        const int tiles = ((n_feat + 255) / 256) * ((T + BN - 1) / BN);
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3(std::min(num_sms, tiles));
         cfg.blockDim = dim3(kTcThreads);
-        cfg.dynamicSmemBytes = (size_t)a.n_stages * (2 * 16384 + planes * kPtBN * 128) + 1024 + 256;
+        cfg.dynamicSmemBytes = (size_t)a.n_stages * (2 * 16384 + planes * BN * 128) + 1024 + 256;
         cfg.stream = s;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

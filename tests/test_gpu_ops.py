@@ -130,6 +130,9 @@ GEMMS = [  # T, N, K, splits (0 = automatic)
     # long prompts: the persistent kernel (tiles of 256 weight rows x 128 prompt rows, several per CTA;
     # ragged last prompt-row tile; K = 6144 as in the down projection)
     (8015, 12288, 2048, 0), (2048, 4096, 2048, 0), (1500, 2048, 6144, 0),
+    # a short batch of rows against many weight rows (the vocabulary projection of a batch): the
+    # persistent kernel with 32- and 48-row tiles, the last 256-row weight tile half outside the matrix
+    (32, 39040, 256, 0), (17, 39040, 256, 0), (48, 39040, 512, 0),
 ]
 
 
