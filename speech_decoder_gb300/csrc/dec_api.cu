@@ -81,6 +81,7 @@ struct dec_handle {
     float *am_val = nullptr;
     int *am_idx = nullptr;
     unsigned *am_counter = nullptr;
+    bool no_fold_rope = false;      // SPEECH_DECODER_FOLD_ROPE=0: the prompt's rope kernel runs separately
     int lm_grid = 0;
     int32_t *out_ids = nullptr;
     SeqState *st = nullptr;
@@ -205,6 +206,8 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     {
         const char *c = std::getenv("SPEECH_DECODER_GEMV_PF_KB");
         h->pf_bytes = (c ? std::max(0, std::min(4096, std::atoi(c))) : 64) * 1024;
+        const char *fr = std::getenv("SPEECH_DECODER_FOLD_ROPE");
+        h->no_fold_rope = fr && fr[0] == '0';
         const char *pb = std::getenv("SPEECH_DECODER_GEMV_PRE");
         h->pre_bulk = pb ? std::max(0, std::min(64, std::atoi(pb))) : 8;
     }
@@ -783,7 +786,6 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
     for (int l = 0; l < hp.n_layers; ++l) {
         const DevLayer &L = h->L[l];
         launch_rmsnorm_rows(h->x, L.attn_norm, hp.rms_eps, h->xn, h->xn_lo, h->w_bf16, total, H, s);
-        gemm(h, h->xn, lo_plane(h, 1, h->xn_lo), L.wqkv, h->qkv, qkv_rows(hp), total, qkv_rows(hp), H, EPI_STORE_F32);
         RopeKvArgs r{};
         r.qkv = h->qkv;
         r.qn_w = L.qn;
@@ -811,8 +813,19 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
                 h->enq++;
             }
         }
-        launch_qk_rope_kv(h->kv_f16, r, s);
-        h->enq += 2;
+        // q|k|v projection; where it runs split-K, the per-head Q/K norm, RoPE
+        // and KV write happen in its reduction (no q|k|v round trip)
+        if (!(h->use_tc && h->w_bf16 && h->kv_f16 && hp.head_dim == 128 && !h->no_fold_rope &&
+              launch_gemm_tc_qkv_rope(h->xn, lo_plane(h, 1, h->xn_lo), total, L.wqkv, qkv_rows(hp), H, r,
+                                      h->tc_scratch, kTcScratchFloats, dev_error(h), h->num_sms, s) == cudaSuccess)) {
+            gemm(h, h->xn, lo_plane(h, 1, h->xn_lo), L.wqkv, h->qkv, qkv_rows(hp), total, qkv_rows(hp), H,
+                 EPI_STORE_F32);
+            launch_qk_rope_kv(h->kv_f16, r, s);
+            h->enq++;
+        } else {
+            h->enq++;                                   // the GEMM and its reduction (gemm() counts one)
+        }
+        h->enq++;
         if (l + 1 == hp.n_layers && ck.on && !ck.final) break;   // KV of every block written; no head
         if (l + 1 < hp.n_layers) {
             AttnPrefillArgs a{};

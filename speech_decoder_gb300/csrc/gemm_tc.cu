@@ -33,6 +33,7 @@
 #include <cstdlib>
 
 #include "gemm_tc.cuh"
+#include "prefill.cuh"
 #include "ptx.cuh"
 #include "tc.cuh"
 
@@ -245,10 +246,44 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(a.tmem_cols) : "memory");
 }
 
+// Per-head Q/K RMSNorm + RoPE + KV write of one prompt row's head (the warp
+// holds its 128 values, lane L features 4L .. 4L + 3 of q|k|v head hh):
+// queries to r.q_out, keys to the pool, values to the pool and V^T.
+__device__ __forceinline__ void rope_kv_head(const RopeKvArgs &r, int t, int hh, float (&v)[4], int lane) {
+    constexpr int D = 128, PL = 4;
+    const int pos = r.row_pos[t];
+    const float2 *rope_row = r.rope + (size_t)pos * (D / 2);
+    if (hh < r.nq) {
+        norm_rope_lane<PL>(v, r.qn_w, r.eps, D, rope_row, lane);
+        __half *q = reinterpret_cast<__half *>(r.q_out) + ((size_t)t * r.nq + hh) * D + lane * PL;
+#pragma unroll
+        for (int e = 0; e < PL; ++e) q[e] = __float2half_rn(v[e]);
+    } else if (hh < r.nq + r.nkv) {
+        const int g = hh - r.nq;
+        norm_rope_lane<PL>(v, r.kn_w, r.eps, D, rope_row, lane);
+        __half *K = reinterpret_cast<__half *>(r.Kc) + ((size_t)g * r.slots + r.row_slot[t]) * D + lane * PL;
+#pragma unroll
+        for (int e = 0; e < PL; ++e) K[e] = __float2half_rn(v[e]);
+    } else {
+        const int g = hh - r.nq - r.nkv;
+        __half *V = reinterpret_cast<__half *>(r.Vc) + ((size_t)g * r.slots + r.row_slot[t]) * D + lane * PL;
+        __half *vt = r.vt ? reinterpret_cast<__half *>(r.vt) + (size_t)(g * D + lane * PL) * r.vt_ld + r.row_vtcol[t]
+                          : nullptr;
+#pragma unroll
+        for (int e = 0; e < PL; ++e) {
+            const __half x = __float2half_rn(v[e]);
+            V[e] = x;
+            if (vt) vt[(size_t)e * r.vt_ld] = x;
+        }
+    }
+}
+
 // Sum the split-K partial tiles in split order and apply the epilogue.  One
 // thread per (tile, token column, 4 consecutive features): reads are
 // 512-byte coalesced per column and every load of a thread is independent.
-__global__ void __launch_bounds__(256) k_splitk_reduce(TcArgs a, int mt) {
+// With rope set (128-row tiles = heads), a warp is one (head, row) and applies
+// the Q/K norm, RoPE and KV write instead of storing q|k|v.
+__global__ void __launch_bounds__(256) k_splitk_reduce(TcArgs a, int mt, RopeKvArgs rk, int rope) {
     ptx::pdl_launch();
     ptx::pdl_wait();
     const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -268,6 +303,11 @@ __global__ void __launch_bounds__(256) k_splitk_reduce(TcArgs a, int mt) {
             const float4 w = __ldcg(reinterpret_cast<const float4 *>(base + ((size_t)s * ncols + a.BN + c) * 128 + r));
             u.x += w.x; u.y += w.y; u.z += w.z; u.w += w.w;
         }
+    }
+    if (rope) {
+        float v[4] = {g.x, g.y, g.z, g.w};
+        rope_kv_head(rk, t, tx, v, threadIdx.x & 31);
+        return;
     }
     const int f = (a.epi == EPI_SWIGLU_BF16 ? tx * 128 : tx * 128 * a.groups) + r;
     epi_store(a, f, t, g.x, u.x);
@@ -575,13 +615,14 @@ static bool pt_disabled() {
     return v == 1;
 }
 
-cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K, int groups,
-                           int epi, float *C, int ldc, void *Hout, void *Hout_lo, int ldh, float *scratch,
-                           size_t scratch_floats, int *err, int num_sms, cudaStream_t s, int force_splits,
-                           const float *bias) {
+static cudaError_t launch_tc(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K, int groups,
+                             int epi, float *C, int ldc, void *Hout, void *Hout_lo, int ldh, float *scratch,
+                             size_t scratch_floats, int *err, int num_sms, cudaStream_t s, int force_splits,
+                             const float *bias, const RopeKvArgs *rope) {
     if (epi == EPI_BIAS_F32 && !bias) return cudaErrorInvalidValue;
     const int planes = X_lo ? 2 : 1;
     if (!pt_disabled() && use_persistent(T, n_feat, K, groups, epi, planes, num_sms, force_splits)) {
+        if (rope) return cudaErrorNotSupported;
         const int BN = pt_bn(T);
         CUtensorMap mA, mB, mB2;
         if (!make_map(&mA, W, (uint64_t)n_feat, (uint64_t)K, 256u) ||
@@ -625,6 +666,8 @@ cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W
     }
     const TcPlan p = gemm_tc_plan(T, n_feat, K, groups, num_sms, scratch_floats, force_splits, planes);
     if (!p.ok) return cudaErrorInvalidValue;
+    // the folded rope needs the reduction kernel with one 128-row tile per head
+    if (rope && (p.splits < 2 || groups != 1 || p.nt != 1 || rope->d != 128 || n_feat % 128)) return cudaErrorNotSupported;
     CUtensorMap mA, mB, mB2;
     if (!make_map(&mA, W, (uint64_t)n_feat, (uint64_t)K, 128u * groups) ||
         !make_map(&mB, X, (uint64_t)T, (uint64_t)K, (uint32_t)p.BN) ||
@@ -669,9 +712,24 @@ cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W
         cfg.gridDim = dim3((unsigned)((threads + 255) / 256));
         cfg.blockDim = dim3(256);
         cfg.dynamicSmemBytes = 0;
-        e = cudaLaunchKernelEx(&cfg, k_splitk_reduce, a, p.mt);
+        e = cudaLaunchKernelEx(&cfg, k_splitk_reduce, a, p.mt, rope ? *rope : RopeKvArgs{}, rope ? 1 : 0);
     }
     return e != cudaSuccess ? e : cudaPeekAtLastError();
+}
+
+cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K, int groups,
+                           int epi, float *C, int ldc, void *Hout, void *Hout_lo, int ldh, float *scratch,
+                           size_t scratch_floats, int *err, int num_sms, cudaStream_t s, int force_splits,
+                           const float *bias) {
+    return launch_tc(X, X_lo, T, W, n_feat, K, groups, epi, C, ldc, Hout, Hout_lo, ldh, scratch, scratch_floats, err,
+                     num_sms, s, force_splits, bias, nullptr);
+}
+
+cudaError_t launch_gemm_tc_qkv_rope(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K,
+                                    const RopeKvArgs &r, float *scratch, size_t scratch_floats, int *err, int num_sms,
+                                    cudaStream_t s) {
+    return launch_tc(X, X_lo, T, W, n_feat, K, 1, EPI_STORE_F32, nullptr, 0, nullptr, nullptr, 0, scratch,
+                     scratch_floats, err, num_sms, s, 0, nullptr, &r);
 }
 
 }  // namespace dec

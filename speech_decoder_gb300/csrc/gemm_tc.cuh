@@ -9,6 +9,8 @@ namespace dec {
 // Epilogues of the prefill projections (shared with the CUDA-core GEMM).
 enum GemmEpi { EPI_STORE_F32 = 0, EPI_RESID_F32 = 1, EPI_SWIGLU_BF16 = 2, EPI_BIAS_F32 = 3 };
 
+struct RopeKvArgs;
+
 struct TcPlan {
     bool ok;
     int BN, n_stages, mt, nt, k_tiles, splits, kt_per_split, tmem_cols;
@@ -34,6 +36,14 @@ cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W
                            int epi, float *C, int ldc, void *Hout, void *Hout_lo, int ldh, float *scratch,
                            size_t scratch_floats, int *err, int num_sms, cudaStream_t s, int force_splits = 0,
                            const float *bias = nullptr);
+// The q|k|v projection of the prompt with the per-head Q/K RMSNorm, RoPE and
+// KV write of the rope kernel folded into the split-K reduction (one warp per
+// row and head: head_dim 128, fp16 KV).  Returns cudaErrorNotSupported (and
+// launches nothing) where the projection would not run split-K in one
+// 128-row tile per head; the caller then runs the GEMM and the rope kernel.
+cudaError_t launch_gemm_tc_qkv_rope(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K,
+                                    const RopeKvArgs &r, float *scratch, size_t scratch_floats, int *err, int num_sms,
+                                    cudaStream_t s);
 void init_gemm_tc();
 bool gemm_tc_ready();
 
