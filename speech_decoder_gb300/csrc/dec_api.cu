@@ -82,6 +82,8 @@ struct dec_handle {
     int *am_idx = nullptr;
     unsigned *am_counter = nullptr;
     bool no_fold_rope = false;      // SPEECH_DECODER_FOLD_ROPE=0: the prompt's rope kernel runs separately
+    bool no_fold_norm = false;      // SPEECH_DECODER_FOLD_NORM=0: RMSNorms of prompt / batch rows run separately
+    bool norm_ready = false;        // batched step: xn already holds the next RMSNorm (written by the down GEMM)
     int lm_grid = 0;
     int32_t *out_ids = nullptr;
     SeqState *st = nullptr;
@@ -206,6 +208,8 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     {
         const char *c = std::getenv("SPEECH_DECODER_GEMV_PF_KB");
         h->pf_bytes = (c ? std::max(0, std::min(4096, std::atoi(c))) : 64) * 1024;
+        const char *fn = std::getenv("SPEECH_DECODER_FOLD_NORM");
+        h->no_fold_norm = fn && fn[0] == '0';
         const char *fr = std::getenv("SPEECH_DECODER_FOLD_ROPE");
         h->no_fold_rope = fr && fr[0] == '0';
         const char *pb = std::getenv("SPEECH_DECODER_GEMV_PRE");
@@ -312,6 +316,21 @@ static void gemm(dec_handle *h, const void *A, const void *A_lo, const void *W, 
     h->enq++;
 }
 
+// A residual projection (o, down) of M rows whose split-K reduction also
+// writes RMSNorm(C) * norm_w into the xn planes for the next projection.
+// False (nothing launched) where that does not apply: then the caller runs
+// gemm() and the RMSNorm kernel.
+static bool gemm_resid_norm(dec_handle *h, const void *A, const void *A_lo, const void *W, float *C, int M, int N,
+                            int K, const float *norm_w) {
+    if (!h->use_tc || !h->w_bf16 || h->no_fold_norm || !norm_w) return false;
+    const cudaError_t e = launch_gemm_tc_resid_norm(A, A_lo, M, W, N, K, C, N, norm_w, h->hp.rms_eps, h->xn, h->xn_lo,
+                                                    h->tc_scratch, kTcScratchFloats, dev_error(h), h->num_sms,
+                                                    h->stream);
+    if (e == cudaErrorNotSupported) return false;
+    h->enq += 2;                                       // any launch error surfaces at the end of the pass
+    return true;
+}
+
 // The second activation plane of a prompt projection, or null where the
 // projection takes one bf16 plane (bit of h->lo_planes: 1 q|k|v, 2 o,
 // 4 gate|up, 8 down).
@@ -358,8 +377,11 @@ static void enqueue_decode_layer_tc(dec_handle *h, int l, int B, bool from_embed
         launch_embed_rows(h->embed, h->w_bf16, h->st, h->xd, B, H, s);
         h->enq++;
     }
-    launch_rmsnorm_rows(h->xd, L.attn_norm, hp.rms_eps, h->xn, h->xn_lo, true, B, H, s);
-    h->enq++;
+    if (!(h->norm_ready && !(from_embed && l == 0))) {
+        launch_rmsnorm_rows(h->xd, L.attn_norm, hp.rms_eps, h->xn, h->xn_lo, true, B, H, s);
+        h->enq++;
+    }
+    h->norm_ready = false;
     gemm(h, h->xn, h->xn_lo, L.wqkv, h->qkvd, qkv_rows(hp), B, qkv_rows(hp), H, EPI_STORE_F32);
 
     AttnDecArgs a{};
@@ -385,11 +407,16 @@ static void enqueue_decode_layer_tc(dec_handle *h, int l, int B, bool from_embed
     a.min_chunk = attn_min_chunk(h, B);
     launch_attn_decode(h->kv_f16, a, splits_for(h, B), s);
     h->enq++;
-    gemm(h, h->attn_o, h->attn_o_lo, L.wo, h->xd, H, B, H, nqd, EPI_RESID_F32);
-    launch_rmsnorm_rows(h->xd, L.ffn_norm, hp.rms_eps, h->xn, h->xn_lo, true, B, H, s);
-    h->enq++;
+    if (!gemm_resid_norm(h, h->attn_o, h->attn_o_lo, L.wo, h->xd, B, H, nqd, L.ffn_norm)) {
+        gemm(h, h->attn_o, h->attn_o_lo, L.wo, h->xd, H, B, H, nqd, EPI_RESID_F32);
+        launch_rmsnorm_rows(h->xd, L.ffn_norm, hp.rms_eps, h->xn, h->xn_lo, true, B, H, s);
+        h->enq++;
+    }
     gemm_swiglu(h, h->xn, h->xn_lo, L.wgu, B, F, H);
-    gemm(h, h->hbuf, h->hbuf_lo, L.wd, h->xd, H, B, H, F, EPI_RESID_F32);
+    // the next layer's (or the head's) RMSNorm in the down projection's reduction
+    const float *next_norm = l + 1 < hp.n_layers ? h->L[l + 1].attn_norm : h->final_norm;
+    if (gemm_resid_norm(h, h->hbuf, h->hbuf_lo, L.wd, h->xd, B, H, F, next_norm)) h->norm_ready = true;
+    else gemm(h, h->hbuf, h->hbuf_lo, L.wd, h->xd, H, B, H, F, EPI_RESID_F32);
 }
 
 // The matrix one step GEMV streams: e4m3 codes and row scales when the handle
@@ -609,10 +636,14 @@ static void enqueue_decode_layer(dec_handle *h, int l, int B, bool from_embed) {
 static void enqueue_head(dec_handle *h, int B) {
     if (batched_path(h, B)) {
         const dec_hparams &hp = h->hp;
-        launch_rmsnorm_rows(h->xd, h->final_norm, hp.rms_eps, h->xn, h->xn_lo, true, B, hp.hidden, h->stream);
+        if (!h->norm_ready) {
+            launch_rmsnorm_rows(h->xd, h->final_norm, hp.rms_eps, h->xn, h->xn_lo, true, B, hp.hidden, h->stream);
+            h->enq++;
+        }
+        h->norm_ready = false;
         gemm(h, h->xn, h->xn_lo, h->embed, h->logits, hp.vocab, B, hp.vocab, hp.hidden, EPI_STORE_F32);
         launch_argmax_rows(h->logits, B, hp.vocab, h->st, h->out_ids, hp.max_new, h->stream);
-        h->enq += 2;
+        h->enq++;
         return;
     }
     GemvArgs g{};
@@ -674,6 +705,7 @@ static StepArgs step_args(dec_handle *h) {
 static bool step_path(const dec_handle *h, int B) { return h->use_step && B == 1; }
 
 static void enqueue_step(dec_handle *h, int B) {
+    h->norm_ready = false;
     if (step_path(h, B)) {
         launch_step(step_args(h), h->num_sms, h->stream);
         h->enq++;
@@ -783,9 +815,11 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
         h->dump_b0_valid = false;
     }
     h->lo_planes_now = prompt_planes(h, total);
+    bool norm_ready = false;                       // xn holds this block's input norm (the down GEMM wrote it)
     for (int l = 0; l < hp.n_layers; ++l) {
         const DevLayer &L = h->L[l];
-        launch_rmsnorm_rows(h->x, L.attn_norm, hp.rms_eps, h->xn, h->xn_lo, h->w_bf16, total, H, s);
+        if (!norm_ready) launch_rmsnorm_rows(h->x, L.attn_norm, hp.rms_eps, h->xn, h->xn_lo, h->w_bf16, total, H, s);
+        norm_ready = false;
         RopeKvArgs r{};
         r.qkv = h->qkv;
         r.qn_w = L.qn;
@@ -862,11 +896,18 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
             } else {
                 launch_attn_prefill_simt(h->kv_f16, h->w_bf16, a, s);
             }
-            gemm(h, h->attn_o, lo_plane(h, 2, h->attn_o_lo), L.wo, h->x, H, total, H, nqd, EPI_RESID_F32);
-            launch_rmsnorm_rows(h->x, L.ffn_norm, hp.rms_eps, h->xn, h->xn_lo, h->w_bf16, total, H, s);
+            // residual projections whose split-K reduction also writes the next RMSNorm
+            if (!gemm_resid_norm(h, h->attn_o, lo_plane(h, 2, h->attn_o_lo), L.wo, h->x, total, H, nqd, L.ffn_norm)) {
+                gemm(h, h->attn_o, lo_plane(h, 2, h->attn_o_lo), L.wo, h->x, H, total, H, nqd, EPI_RESID_F32);
+                launch_rmsnorm_rows(h->x, L.ffn_norm, hp.rms_eps, h->xn, h->xn_lo, h->w_bf16, total, H, s);
+                h->enq++;
+            }
             gemm_swiglu(h, h->xn, lo_plane(h, 4, h->xn_lo), L.wgu, total, F, H);
-            gemm(h, h->hbuf, lo_plane(h, 8, h->hbuf_lo), L.wd, h->x, H, total, H, F, EPI_RESID_F32);
-            h->enq += 2;
+            if (gemm_resid_norm(h, h->hbuf, lo_plane(h, 8, h->hbuf_lo), L.wd, h->x, total, H, F, h->L[l + 1].attn_norm))
+                norm_ready = true;
+            else
+                gemm(h, h->hbuf, lo_plane(h, 8, h->hbuf_lo), L.wd, h->x, H, total, H, F, EPI_RESID_F32);
+            h->enq++;
             if (h->dumps && l == 0) {
                 CK(cudaMemcpyAsync(h->dump_b0, h->x, (size_t)total * H * 4, cudaMemcpyDeviceToDevice, s));
                 h->dump_b0_valid = true;

@@ -322,6 +322,43 @@ __global__ void __launch_bounds__(256) k_splitk_reduce(TcArgs a, int mt, RopeKvA
     }
 }
 
+// Split-K sum of a residual projection (o, down) and the RMSNorm of the
+// finished rows: one CTA per prompt row, warp w = 128-row weight tile w (lane
+// L its features 4L .. 4L + 3).  The residual row is stored, its sum of
+// squares reduced over the CTA, and the normalised row written as two bf16
+// planes for the next projection.
+struct NormArgs {
+    const float *w;
+    float eps;
+    __nv_bfloat16 *hi, *lo;
+};
+
+__global__ void __launch_bounds__(1024) k_splitk_resid_norm(TcArgs a, NormArgs n) {
+    __shared__ float red[32];
+    ptx::pdl_launch();
+    ptx::pdl_wait();
+    const int t = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = a.n_feat, f = w * 128 + 4 * lane;
+    const float *base = a.part + (size_t)w * a.splits * a.BN * 128 + (size_t)t * 128 + 4 * lane;
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp = 0; sp < a.splits; ++sp) {               // in split order
+        const float4 v = __ldcg(reinterpret_cast<const float4 *>(base + (size_t)sp * a.BN * 128));
+        g.x += v.x; g.y += v.y; g.z += v.z; g.w += v.w;
+    }
+    float4 *c = reinterpret_cast<float4 *>(a.C + (size_t)t * a.ldc + f);
+    float4 x = *c;
+    x.x += g.x; x.y += g.y; x.z += g.z; x.w += g.w;
+    *c = x;
+    const float ss = block_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w, red);
+    const float r = rsqrtf(ss / (float)H + n.eps);
+    const float4 wv = *reinterpret_cast<const float4 *>(n.w + f);
+    const size_t o = (size_t)t * H + f;
+    store_planes(n.hi, n.lo, o, x.x * r * wv.x);
+    store_planes(n.hi, n.lo, o + 1, x.y * r * wv.y);
+    store_planes(n.hi, n.lo, o + 2, x.z * r * wv.z);
+    store_planes(n.hi, n.lo, o + 3, x.w * r * wv.w);
+}
+
 // ------------------------------------------------------------------ persistent form (long prompts)
 // One CTA per SM walks output tiles of 256 weight rows (two 128-row MMA groups:
 // gate and up rows for SwiGLU) x 128 prompt rows, the tiles of one prompt-row
@@ -618,11 +655,11 @@ static bool pt_disabled() {
 static cudaError_t launch_tc(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K, int groups,
                              int epi, float *C, int ldc, void *Hout, void *Hout_lo, int ldh, float *scratch,
                              size_t scratch_floats, int *err, int num_sms, cudaStream_t s, int force_splits,
-                             const float *bias, const RopeKvArgs *rope) {
+                             const float *bias, const RopeKvArgs *rope, const NormArgs *norm = nullptr) {
     if (epi == EPI_BIAS_F32 && !bias) return cudaErrorInvalidValue;
     const int planes = X_lo ? 2 : 1;
     if (!pt_disabled() && use_persistent(T, n_feat, K, groups, epi, planes, num_sms, force_splits)) {
-        if (rope) return cudaErrorNotSupported;
+        if (rope || norm) return cudaErrorNotSupported;
         const int BN = pt_bn(T);
         CUtensorMap mA, mB, mB2;
         if (!make_map(&mA, W, (uint64_t)n_feat, (uint64_t)K, 256u) ||
@@ -668,6 +705,9 @@ static cudaError_t launch_tc(const void *X, const void *X_lo, int T, const void 
     if (!p.ok) return cudaErrorInvalidValue;
     // the folded rope needs the reduction kernel with one 128-row tile per head
     if (rope && (p.splits < 2 || groups != 1 || p.nt != 1 || rope->d != 128 || n_feat % 128)) return cudaErrorNotSupported;
+    if (norm && (p.splits < 2 || groups != 1 || p.nt != 1 || epi != EPI_RESID_F32 || n_feat % 128 ||
+                 n_feat > 32 * 128 || ldc % 4 || p.BN < T))
+        return cudaErrorNotSupported;
     CUtensorMap mA, mB, mB2;
     if (!make_map(&mA, W, (uint64_t)n_feat, (uint64_t)K, 128u * groups) ||
         !make_map(&mB, X, (uint64_t)T, (uint64_t)K, (uint32_t)p.BN) ||
@@ -707,7 +747,12 @@ static cudaError_t launch_tc(const void *X, const void *X_lo, int T, const void 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc, mA, mB, mB2, a);
-    if (e == cudaSuccess && p.splits > 1) {
+    if (e == cudaSuccess && norm) {
+        cfg.gridDim = dim3((unsigned)T);
+        cfg.blockDim = dim3((unsigned)(32 * p.mt));
+        cfg.dynamicSmemBytes = 0;
+        e = cudaLaunchKernelEx(&cfg, k_splitk_resid_norm, a, *norm);
+    } else if (e == cudaSuccess && p.splits > 1) {
         const long long threads = (long long)p.mt * p.nt * p.BN * 32;
         cfg.gridDim = dim3((unsigned)((threads + 255) / 256));
         cfg.blockDim = dim3(256);
@@ -723,6 +768,14 @@ cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W
                            const float *bias) {
     return launch_tc(X, X_lo, T, W, n_feat, K, groups, epi, C, ldc, Hout, Hout_lo, ldh, scratch, scratch_floats, err,
                      num_sms, s, force_splits, bias, nullptr);
+}
+
+cudaError_t launch_gemm_tc_resid_norm(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K,
+                                      float *C, int ldc, const float *norm_w, float eps, void *hi, void *lo,
+                                      float *scratch, size_t scratch_floats, int *err, int num_sms, cudaStream_t s) {
+    const NormArgs n{norm_w, eps, static_cast<__nv_bfloat16 *>(hi), static_cast<__nv_bfloat16 *>(lo)};
+    return launch_tc(X, X_lo, T, W, n_feat, K, 1, EPI_RESID_F32, C, ldc, nullptr, nullptr, 0, scratch, scratch_floats,
+                     err, num_sms, s, 0, nullptr, nullptr, &n);
 }
 
 cudaError_t launch_gemm_tc_qkv_rope(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K,

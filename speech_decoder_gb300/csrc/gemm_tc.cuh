@@ -41,6 +41,14 @@ cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W
 // row and head: head_dim 128, fp16 KV).  Returns cudaErrorNotSupported (and
 // launches nothing) where the projection would not run split-K in one
 // 128-row tile per head; the caller then runs the GEMM and the rope kernel.
+// A residual projection of the prompt (o, down: C += X W^T) whose split-K
+// reduction also writes the RMSNorm of the finished rows for the next
+// projection: hi/lo = two bf16 planes of C[t] * rsqrt(mean(C[t]^2) + eps) * w.
+// cudaErrorNotSupported (nothing launched) unless it runs split-K in one
+// prompt-row tile with 128-row weight tiles and n_feat <= 4096.
+cudaError_t launch_gemm_tc_resid_norm(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K,
+                                      float *C, int ldc, const float *norm_w, float eps, void *hi, void *lo,
+                                      float *scratch, size_t scratch_floats, int *err, int num_sms, cudaStream_t s);
 cudaError_t launch_gemm_tc_qkv_rope(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K,
                                     const RopeKvArgs &r, float *scratch, size_t scratch_floats, int *err, int num_sms,
                                     cudaStream_t s);
