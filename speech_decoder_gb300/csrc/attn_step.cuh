@@ -300,6 +300,43 @@ __device__ __forceinline__ void load_seg(const float *p, float (&f)[N]) {
     }
 }
 
+// The lane with index g in its key group holds, of each D-element row, the
+// 16-byte chunks c * kLG + g (c < DL / EPC, EPC elements per chunk): the kLG
+// lanes of a group read 128 contiguous bytes per load, free of bank
+// conflicts.  ildim gives the row element behind local element i.
+template <typename TKV>
+__host__ __device__ constexpr int il_epc() { return 16 / (int)sizeof(TKV); }
+template <typename TKV>
+__device__ __forceinline__ int ildim(int i, int g) {
+    constexpr int EPC = il_epc<TKV>();
+    return ((i / EPC) * kLG + g) * EPC + i % EPC;
+}
+template <int N>
+__device__ __forceinline__ void load_seg_il(const __half *row, int g, float (&f)[N]) {
+#pragma unroll
+    for (int c = 0; c < N / 8; ++c) {
+        const uint4 u = reinterpret_cast<const uint4 *>(row)[c * kLG + g];
+        const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 t = __half22float2(h[i]);
+            f[c * 8 + 2 * i] = t.x;
+            f[c * 8 + 2 * i + 1] = t.y;
+        }
+    }
+}
+template <int N>
+__device__ __forceinline__ void load_seg_il(const float *row, int g, float (&f)[N]) {
+#pragma unroll
+    for (int c = 0; c < N / 4; ++c) {
+        const float4 u = reinterpret_cast<const float4 *>(row)[c * kLG + g];
+        f[4 * c] = u.x;
+        f[4 * c + 1] = u.y;
+        f[4 * c + 2] = u.z;
+        f[4 * c + 3] = u.w;
+    }
+}
+
 template <typename TKV, int D>
 constexpr int attn_tile_keys() {
     return 65536 / (D * (int)sizeof(TKV)) < 256 ? 65536 / (D * (int)sizeof(TKV)) : 256;
@@ -380,7 +417,7 @@ __device__ void attn_step_core(const AttnDecArgs &a, float scale, int g, int s, 
 #pragma unroll
         for (int e = 0; e < AL; ++e) acc[r][e] = 0.f;
     }
-    const int dq = (lane % kLG) * DL, kslot = lane / kLG;   // grouped scoring: dims and key of this lane
+    const int lg = lane % kLG, kslot = lane / kLG;  // grouped scoring: dims (ildim) and key of this lane
     float qr[NREP ? NREP : 1][NREP ? DL : 1];
     bool failed = false;
     for (int t0 = j0; t0 < j1; t0 += T) {
@@ -436,14 +473,14 @@ __device__ void attn_step_core(const AttnDecArgs &a, float scale, int g, int s, 
 #pragma unroll
                 for (int r = 0; r < NREP; ++r)
 #pragma unroll
-                    for (int i = 0; i < DL; ++i) qr[r][i] = sm.qs[r][dq + i];
+                    for (int i = 0; i < DL; ++i) qr[r][i] = sm.qs[r][ildim<TKV>(i, lg)];
             }
             for (int jb = t0 + warp * (32 / kLG); jb < t1; jb += W * (32 / kLG)) {
                 const int j = jb + kslot;
                 const bool valid = j < t1;
                 float kk[DL];
                 if (valid) {
-                    load_seg<DL>(Ks + (size_t)(j - t0) * D + dq, kk);
+                    load_seg_il<DL>(Ks + (size_t)(j - t0) * D, lg, kk);
                 } else {
 #pragma unroll
                     for (int i = 0; i < DL; ++i) kk[i] = 0.f;
@@ -460,7 +497,7 @@ __device__ void attn_step_core(const AttnDecArgs &a, float scale, int g, int s, 
                 }
                 if (valid) {
                     float vv[DL];
-                    load_seg<DL>(Vs + (size_t)(j - t0) * D + dq, vv);
+                    load_seg_il<DL>(Vs + (size_t)(j - t0) * D, lg, vv);
 #pragma unroll
                     for (int r = 0; r < NREP; ++r) {
                         const float mb = fmaxf(m[r], sc[r]);
@@ -509,7 +546,7 @@ __device__ void attn_step_core(const AttnDecArgs &a, float scale, int g, int s, 
                 float v = acc[r][i] * f;
 #pragma unroll
                 for (int o = kLG; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (kslot == 0) sm.wacc[warp][r][dq + i] = v;
+                if (kslot == 0) sm.wacc[warp][r][ildim<TKV>(i, lg)] = v;
             }
             if (lane == 0) {
                 sm.wm[warp][r] = M;
