@@ -261,6 +261,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 0; c < kD; c += 16) {
                 const float *t = o + c;
                 uint32_t wh[8], wl[8];
+                if (a.o_f16) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const __half2 hh = __floats2half2_rn(t[2 * i] * inv, t[2 * i + 1] * inv);
+                        wh[i] = *reinterpret_cast<const uint32_t *>(&hh);
+                    }
+                    if (!row_ok) continue;
+                    uint4 *dh = reinterpret_cast<uint4 *>(hi + c);
+                    dh[0] = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+                    dh[1] = make_uint4(wh[4], wh[5], wh[6], wh[7]);
+                    continue;
+                }
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const float v0 = t[2 * i] * inv, v1 = t[2 * i + 1] * inv;

@@ -27,6 +27,8 @@ struct DevLayer {
     // DEC_E4M3: the same matrices as e4m3 codes with per-row scales
     uint8_t *wqkv8 = nullptr, *wo8 = nullptr, *wgu8 = nullptr, *wd8 = nullptr;
     float *wqkv_s = nullptr, *wo_s = nullptr, *wgu_s = nullptr, *wd_s = nullptr;
+    // fp16 copies of the (bf16) projection matrices for the prompt GEMMs' fp16 mode
+    void *wqkv16 = nullptr, *wo16 = nullptr, *wgu16 = nullptr, *wd16 = nullptr;
     float *attn_norm = nullptr, *ffn_norm = nullptr, *qn = nullptr, *kn = nullptr;
     void *K = nullptr, *V = nullptr;
 };
@@ -74,6 +76,8 @@ struct dec_handle {
     int32_t *row_vtcol = nullptr, *item_kv_off = nullptr, *item_vt_col = nullptr;
     int4 *attn_tiles = nullptr;
     bool tc_attn = false;
+    bool f16_copies = false;        // the workspace holds fp16 copies of the projection matrices
+    bool pf16 = false;              // prompt GEMMs in fp16 (one activation plane), else bf16 (two planes)
     // decode activations and scratch
     float *xd = nullptr, *qkvd = nullptr, *od = nullptr, *gud = nullptr, *logits = nullptr;
     float *attn_part = nullptr;
@@ -208,6 +212,9 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
     {
         const char *c = std::getenv("SPEECH_DECODER_GEMV_PF_KB");
         h->pf_bytes = (c ? std::max(0, std::min(4096, std::atoi(c))) : 64) * 1024;
+        const char *pf = std::getenv("SPEECH_DECODER_PROMPT_F16");
+        h->f16_copies = !(pf && pf[0] == '0') && hp.weight_dtype != DEC_F32 && hp.hidden % 128 == 0 &&
+                        hp.ffn % 128 == 0 && (hp.n_heads * hp.head_dim) % 128 == 0;
         const char *fn = std::getenv("SPEECH_DECODER_FOLD_NORM");
         h->no_fold_norm = fn && fn[0] == '0';
         const char *fr = std::getenv("SPEECH_DECODER_FOLD_ROPE");
@@ -233,6 +240,12 @@ static size_t plan(dec_handle *h, const dec_hparams &hp, char *base, int num_sms
         l.wo = b.take<char>(H * nq * d * ws);
         l.wgu = b.take<char>(2 * F * H * ws);
         l.wd = b.take<char>(H * F * ws);
+        if (h->f16_copies) {
+            l.wqkv16 = b.take<char>((size_t)qkv_rows(hp) * H * 2);
+            l.wo16 = b.take<char>(H * nq * d * 2);
+            l.wgu16 = b.take<char>(2 * F * H * 2);
+            l.wd16 = b.take<char>(H * F * 2);
+        }
         if (e4m3) {
             l.wqkv8 = b.take<uint8_t>((size_t)qkv_rows(hp) * H);
             l.wo8 = b.take<uint8_t>(H * nq * d);
@@ -304,13 +317,16 @@ static int *dev_error(dec_handle *h) { return &h->st->error; }
 // Prompt-row projection C[M, N] (=|+=) A[M, K] W[N, K]^T: tcgen05 for bf16
 // weights, CUDA cores for the fp32 debug build.
 // A_lo: the second bf16 plane of A (bf16 builds), read by the tensor-core path.
+// f16: W and A are fp16 (the prompt GEMMs' fp16 mode: A_lo unused; the
+// shapes it is enabled for always plan on the tensor cores)
 static void gemm(dec_handle *h, const void *A, const void *A_lo, const void *W, float *C, int ldc, int M, int N, int K,
-                 int epi) {
+                 int epi, bool f16 = false) {
     // long prompts: 256 weight rows per CTA share each activation tile
     const int groups = M > 256 && N % 256 == 0 ? 2 : 1;
-    if (h->use_tc && h->w_bf16 && gemm_tc_plan(M, N, K, groups, h->num_sms, kTcScratchFloats, 0, A_lo ? 2 : 1).ok)
+    if (f16 || (h->use_tc && h->w_bf16 &&
+                gemm_tc_plan(M, N, K, groups, h->num_sms, kTcScratchFloats, 0, A_lo ? 2 : 1).ok))
         launch_gemm_tc(A, A_lo, M, W, N, K, groups, epi, C, ldc, nullptr, nullptr, 0, h->tc_scratch, kTcScratchFloats,
-                       dev_error(h), h->num_sms, h->stream);   // a launch error surfaces at the end of the pass
+                       dev_error(h), h->num_sms, h->stream, 0, nullptr, f16);   // a launch error surfaces at the end
     else
         launch_gemm_simt(A, h->w_bf16, W, h->w_bf16, C, ldc, M, N, K, epi, h->stream);
     h->enq++;
@@ -321,11 +337,11 @@ static void gemm(dec_handle *h, const void *A, const void *A_lo, const void *W, 
 // False (nothing launched) where that does not apply: then the caller runs
 // gemm() and the RMSNorm kernel.
 static bool gemm_resid_norm(dec_handle *h, const void *A, const void *A_lo, const void *W, float *C, int M, int N,
-                            int K, const float *norm_w) {
+                            int K, const float *norm_w, bool f16 = false) {
     if (!h->use_tc || !h->w_bf16 || h->no_fold_norm || !norm_w) return false;
     const cudaError_t e = launch_gemm_tc_resid_norm(A, A_lo, M, W, N, K, C, N, norm_w, h->hp.rms_eps, h->xn, h->xn_lo,
                                                     h->tc_scratch, kTcScratchFloats, dev_error(h), h->num_sms,
-                                                    h->stream);
+                                                    h->stream, f16);
     if (e == cudaErrorNotSupported) return false;
     h->enq += 2;                                       // any launch error surfaces at the end of the pass
     return true;
@@ -335,7 +351,7 @@ static bool gemm_resid_norm(dec_handle *h, const void *A, const void *A_lo, cons
 // projection takes one bf16 plane (bit of h->lo_planes: 1 q|k|v, 2 o,
 // 4 gate|up, 8 down).
 static const void *lo_plane(const dec_handle *h, int bit, const void *lo) {
-    return (h->lo_planes_now & bit) ? lo : nullptr;
+    return !h->pf16 && (h->lo_planes_now & bit) ? lo : nullptr;
 }
 
 // Projections that take the second plane in a prompt of `rows` rows: all of
@@ -350,10 +366,12 @@ static int prompt_planes(const dec_handle *h, int rows) {
 }
 
 // Gate|up projection and SwiGLU into h->hbuf (and its second plane).
-static void gemm_swiglu(dec_handle *h, const void *A, const void *A_lo, const void *Wgu, int M, int F, int K) {
-    if (h->use_tc && h->w_bf16 && gemm_tc_plan(M, 2 * F, K, 2, h->num_sms, kTcScratchFloats, 0, A_lo ? 2 : 1).ok) {
+static void gemm_swiglu(dec_handle *h, const void *A, const void *A_lo, const void *Wgu, int M, int F, int K,
+                        bool f16 = false) {
+    if (f16 || (h->use_tc && h->w_bf16 &&
+                gemm_tc_plan(M, 2 * F, K, 2, h->num_sms, kTcScratchFloats, 0, A_lo ? 2 : 1).ok)) {
         launch_gemm_tc(A, A_lo, M, Wgu, 2 * F, K, 2, EPI_SWIGLU_BF16, nullptr, 0, h->hbuf, h->hbuf_lo, F,
-                       h->tc_scratch, kTcScratchFloats, dev_error(h), h->num_sms, h->stream);
+                       h->tc_scratch, kTcScratchFloats, dev_error(h), h->num_sms, h->stream, 0, nullptr, f16);
         h->enq++;
     } else {
         launch_gemm_simt(A, h->w_bf16, Wgu, h->w_bf16, h->gu, 2 * F, M, 2 * F, K, EPI_STORE_F32, h->stream);
@@ -816,9 +834,13 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
     }
     h->lo_planes_now = prompt_planes(h, total);
     bool norm_ready = false;                       // xn holds this block's input norm (the down GEMM wrote it)
+    const bool f16 = h->pf16;                      // prompt GEMMs in fp16 (one plane), else bf16 planes
     for (int l = 0; l < hp.n_layers; ++l) {
         const DevLayer &L = h->L[l];
-        if (!norm_ready) launch_rmsnorm_rows(h->x, L.attn_norm, hp.rms_eps, h->xn, h->xn_lo, h->w_bf16, total, H, s);
+        if (!norm_ready) {
+            if (f16) launch_rmsnorm_rows_f16(h->x, L.attn_norm, hp.rms_eps, h->xn, total, H, s);
+            else launch_rmsnorm_rows(h->x, L.attn_norm, hp.rms_eps, h->xn, h->xn_lo, h->w_bf16, total, H, s);
+        }
         norm_ready = false;
         RopeKvArgs r{};
         r.qkv = h->qkv;
@@ -850,10 +872,11 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
         // q|k|v projection; where it runs split-K, the per-head Q/K norm, RoPE
         // and KV write happen in its reduction (no q|k|v round trip)
         if (!(h->use_tc && h->w_bf16 && h->kv_f16 && hp.head_dim == 128 && !h->no_fold_rope &&
-              launch_gemm_tc_qkv_rope(h->xn, lo_plane(h, 1, h->xn_lo), total, L.wqkv, qkv_rows(hp), H, r,
-                                      h->tc_scratch, kTcScratchFloats, dev_error(h), h->num_sms, s) == cudaSuccess)) {
-            gemm(h, h->xn, lo_plane(h, 1, h->xn_lo), L.wqkv, h->qkv, qkv_rows(hp), total, qkv_rows(hp), H,
-                 EPI_STORE_F32);
+              launch_gemm_tc_qkv_rope(h->xn, lo_plane(h, 1, h->xn_lo), total, f16 ? L.wqkv16 : L.wqkv, qkv_rows(hp),
+                                      H, r, h->tc_scratch, kTcScratchFloats, dev_error(h), h->num_sms, s,
+                                      f16) == cudaSuccess)) {
+            gemm(h, h->xn, lo_plane(h, 1, h->xn_lo), f16 ? L.wqkv16 : L.wqkv, h->qkv, qkv_rows(hp), total,
+                 qkv_rows(hp), H, EPI_STORE_F32, f16);
             launch_qk_rope_kv(h->kv_f16, r, s);
             h->enq++;
         } else {
@@ -885,6 +908,7 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
                 t.vt_col = h->item_vt_col;
                 t.o = static_cast<__nv_bfloat16 *>(h->attn_o);
                 t.o_lo = static_cast<__nv_bfloat16 *>(h->attn_o_lo);
+                t.o_f16 = f16 ? 1 : 0;
                 t.err = dev_error(h);
                 t.q_rows = total;
                 t.nq = hp.n_heads;
@@ -897,16 +921,20 @@ static dec_status prefill_rows(dec_handle *h, const int32_t *cu, int B, int32_t 
                 launch_attn_prefill_simt(h->kv_f16, h->w_bf16, a, s);
             }
             // residual projections whose split-K reduction also writes the next RMSNorm
-            if (!gemm_resid_norm(h, h->attn_o, lo_plane(h, 2, h->attn_o_lo), L.wo, h->x, total, H, nqd, L.ffn_norm)) {
-                gemm(h, h->attn_o, lo_plane(h, 2, h->attn_o_lo), L.wo, h->x, H, total, H, nqd, EPI_RESID_F32);
-                launch_rmsnorm_rows(h->x, L.ffn_norm, hp.rms_eps, h->xn, h->xn_lo, h->w_bf16, total, H, s);
+            const void *wo = f16 ? L.wo16 : L.wo, *wgu = f16 ? L.wgu16 : L.wgu, *wd = f16 ? L.wd16 : L.wd;
+            if (!gemm_resid_norm(h, h->attn_o, lo_plane(h, 2, h->attn_o_lo), wo, h->x, total, H, nqd, L.ffn_norm,
+                                 f16)) {
+                gemm(h, h->attn_o, lo_plane(h, 2, h->attn_o_lo), wo, h->x, H, total, H, nqd, EPI_RESID_F32, f16);
+                if (f16) launch_rmsnorm_rows_f16(h->x, L.ffn_norm, hp.rms_eps, h->xn, total, H, s);
+                else launch_rmsnorm_rows(h->x, L.ffn_norm, hp.rms_eps, h->xn, h->xn_lo, h->w_bf16, total, H, s);
                 h->enq++;
             }
-            gemm_swiglu(h, h->xn, lo_plane(h, 4, h->xn_lo), L.wgu, total, F, H);
-            if (gemm_resid_norm(h, h->hbuf, lo_plane(h, 8, h->hbuf_lo), L.wd, h->x, total, H, F, h->L[l + 1].attn_norm))
+            gemm_swiglu(h, h->xn, lo_plane(h, 4, h->xn_lo), wgu, total, F, H, f16);
+            if (gemm_resid_norm(h, h->hbuf, lo_plane(h, 8, h->hbuf_lo), wd, h->x, total, H, F, h->L[l + 1].attn_norm,
+                                f16))
                 norm_ready = true;
             else
-                gemm(h, h->hbuf, lo_plane(h, 8, h->hbuf_lo), L.wd, h->x, H, total, H, F, EPI_RESID_F32);
+                gemm(h, h->hbuf, lo_plane(h, 8, h->hbuf_lo), wd, h->x, H, total, H, F, EPI_RESID_F32, f16);
             h->enq++;
             if (h->dumps && l == 0) {
                 CK(cudaMemcpyAsync(h->dump_b0, h->x, (size_t)total * H * 4, cudaMemcpyDeviceToDevice, s));
@@ -1158,6 +1186,14 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
             launch_quantize_e4m3_rows(D.wd, H, (int)F, D.wd8, D.wd_s, D.wd, s);
             CKC(cudaGetLastError());
         }
+        if (h->f16_copies) {
+            // the same (rounded) values in fp16: exact for bf16 values in fp16's normal range
+            launch_bf16_to_f16(D.wqkv, D.wqkv16, (size_t)qkv_rows(*hp) * H, s);
+            launch_bf16_to_f16(D.wo, D.wo16, H * nq * d, s);
+            launch_bf16_to_f16(D.wgu, D.wgu16, 2 * F * H, s);
+            launch_bf16_to_f16(D.wd, D.wd16, H * F, s);
+            CKC(cudaGetLastError());
+        }
         CKC(cudaStreamSynchronize(s));
         CKC(put_norm(D.attn_norm, W.attn_norm, H));
         CKC(put_norm(D.ffn_norm, W.ffn_norm, H));
@@ -1226,6 +1262,9 @@ dec_status dec_create(const dec_hparams *hp, const dec_weights *w, void *workspa
         // zero probabilities and must hold finite values, so the scratch starts at 0
         const char *pa = std::getenv("SPEECH_DECODER_PREFILL_ATTN");
         h->tc_attn = h->use_tc && h->vt && attn_prefill_tc_ok((int)d, h->kv_f16) && !(pa && !std::strcmp(pa, "simt"));
+        // prompt GEMMs in fp16: fp16 weights and one fp16 activation plane
+        // (an fp16 rounding, 8 times finer than bf16's, of each projection input)
+        h->pf16 = h->f16_copies && h->w_bf16 && h->tc_attn && h->kv_f16 && d == 128;
         if (h->vt) CKC(cudaMemsetAsync(h->vt, 0, (size_t)nkv * d * h->vt_ld * 2, s));
     }
     CKC(cudaMemsetAsync(h->am_counter, 0, 64 * sizeof(unsigned), s));

@@ -52,6 +52,7 @@ struct TcArgs {
     float *C;
     int ldc;
     __nv_bfloat16 *Hout, *Hout_lo;  // SwiGLU output planes (Hout_lo may be null)
+    int out_f16;                 // SwiGLU output: one fp16 plane in Hout (operands of an fp16 GEMM)
     int ldh;
     float *part;
     const float *bias;           // EPI_BIAS_F32
@@ -69,6 +70,10 @@ __device__ __forceinline__ void epi_store(const TcArgs &a, int f, int t, float v
     if (t >= a.T) return;
     if (a.epi == EPI_SWIGLU_BF16) {
         const float h = v / (1.f + expf(-v)) * up;
+        if (a.out_f16) {
+            reinterpret_cast<__half *>(a.Hout)[(size_t)t * a.ldh + f] = __float2half_rn(h);
+            return;
+        }
         const __nv_bfloat16 hi = __float2bfloat16_rn(h);
         a.Hout[(size_t)t * a.ldh + f] = hi;
         if (a.Hout_lo) a.Hout_lo[(size_t)t * a.ldh + f] = __float2bfloat16_rn(h - __bfloat162float(hi));
@@ -331,6 +336,7 @@ struct NormArgs {
     const float *w;
     float eps;
     __nv_bfloat16 *hi, *lo;
+    int f16;                     // one fp16 plane in hi instead of two bf16 planes
 };
 
 __global__ void __launch_bounds__(1024) k_splitk_resid_norm(TcArgs a, NormArgs n) {
@@ -353,6 +359,12 @@ __global__ void __launch_bounds__(1024) k_splitk_resid_norm(TcArgs a, NormArgs n
     const float r = rsqrtf(ss / (float)H + n.eps);
     const float4 wv = *reinterpret_cast<const float4 *>(n.w + f);
     const size_t o = (size_t)t * H + f;
+    if (n.f16) {
+        __half2 *hp = reinterpret_cast<__half2 *>(reinterpret_cast<__half *>(n.hi) + o);
+        hp[0] = __floats2half2_rn(x.x * r * wv.x, x.y * r * wv.y);
+        hp[1] = __floats2half2_rn(x.z * r * wv.z, x.w * r * wv.w);
+        return;
+    }
     store_planes(n.hi, n.lo, o, x.x * r * wv.x);
     store_planes(n.hi, n.lo, o + 1, x.y * r * wv.y);
     store_planes(n.hi, n.lo, o + 2, x.z * r * wv.z);
@@ -580,12 +592,13 @@ static int pt_stages(int planes, int BN) {
     return n > 6 ? 6 : n;
 }
 
-static bool make_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t K, uint32_t box_rows) {
+static bool make_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t K, uint32_t box_rows, bool f16 = false) {
     const cuuint64_t dims[2] = {K, rows};
     const cuuint64_t strides[1] = {K * 2};
     const cuuint32_t box[2] = {(cuuint32_t)kBK, box_rows};
     const cuuint32_t es[2] = {1, 1};
-    return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, es,
+    return g_encode(m, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void *>(ptr), dims, strides, box, es,
                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -655,16 +668,19 @@ static bool pt_disabled() {
 static cudaError_t launch_tc(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K, int groups,
                              int epi, float *C, int ldc, void *Hout, void *Hout_lo, int ldh, float *scratch,
                              size_t scratch_floats, int *err, int num_sms, cudaStream_t s, int force_splits,
-                             const float *bias, const RopeKvArgs *rope, const NormArgs *norm = nullptr) {
+                             const float *bias, const RopeKvArgs *rope, const NormArgs *norm = nullptr,
+                             bool f16 = false) {
+    // f16: weights and activations both fp16 (one plane; a tcgen05 f16-kind
+    // MMA takes A and B of one type), else bf16
     if (epi == EPI_BIAS_F32 && !bias) return cudaErrorInvalidValue;
     const int planes = X_lo ? 2 : 1;
     if (!pt_disabled() && use_persistent(T, n_feat, K, groups, epi, planes, num_sms, force_splits)) {
         if (rope || norm) return cudaErrorNotSupported;
         const int BN = pt_bn(T);
         CUtensorMap mA, mB, mB2;
-        if (!make_map(&mA, W, (uint64_t)n_feat, (uint64_t)K, 256u) ||
-            !make_map(&mB, X, (uint64_t)T, (uint64_t)K, (uint32_t)BN) ||
-            !make_map(&mB2, X_lo ? X_lo : X, (uint64_t)T, (uint64_t)K, (uint32_t)BN))
+        if (!make_map(&mA, W, (uint64_t)n_feat, (uint64_t)K, 256u, f16) ||
+            !make_map(&mB, X, (uint64_t)T, (uint64_t)K, (uint32_t)BN, f16) ||
+            !make_map(&mB2, X_lo ? X_lo : X, (uint64_t)T, (uint64_t)K, (uint32_t)BN, f16))
             return cudaErrorInvalidValue;
         TcArgs a{};
         a.n_feat = epi == EPI_SWIGLU_BF16 ? n_feat / 2 : n_feat;
@@ -685,7 +701,8 @@ static cudaError_t launch_tc(const void *X, const void *X_lo, int T, const void 
         a.ldh = ldh;
         a.bias = bias;
         a.err = err;
-        a.idesc = mma_idesc_f16(true, 128, BN);
+        a.idesc = mma_idesc_f16(!f16, 128, BN);
+        a.out_f16 = f16;
         a.tmem_cols = 512;
         const int tiles = ((n_feat + 255) / 256) * ((T + BN - 1) / BN);
         cudaLaunchConfig_t cfg{};
@@ -709,9 +726,9 @@ static cudaError_t launch_tc(const void *X, const void *X_lo, int T, const void 
                  n_feat > 32 * 128 || ldc % 4 || p.BN < T))
         return cudaErrorNotSupported;
     CUtensorMap mA, mB, mB2;
-    if (!make_map(&mA, W, (uint64_t)n_feat, (uint64_t)K, 128u * groups) ||
-        !make_map(&mB, X, (uint64_t)T, (uint64_t)K, (uint32_t)p.BN) ||
-        !make_map(&mB2, X_lo ? X_lo : X, (uint64_t)T, (uint64_t)K, (uint32_t)p.BN))
+    if (!make_map(&mA, W, (uint64_t)n_feat, (uint64_t)K, 128u * groups, f16) ||
+        !make_map(&mB, X, (uint64_t)T, (uint64_t)K, (uint32_t)p.BN, f16) ||
+        !make_map(&mB2, X_lo ? X_lo : X, (uint64_t)T, (uint64_t)K, (uint32_t)p.BN, f16))
         return cudaErrorInvalidValue;
     TcArgs a{};
     a.n_feat = epi == EPI_SWIGLU_BF16 ? n_feat / 2 : n_feat;
@@ -733,8 +750,9 @@ static cudaError_t launch_tc(const void *X, const void *X_lo, int T, const void 
     a.part = scratch;
     a.bias = bias;
     a.err = err;
-    // instruction descriptor: f32 accumulate, bf16 A and B, both K-major, N = BN, M = 128
-    a.idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(p.BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    // instruction descriptor: f32 accumulate, A and B bf16 (or fp16), both K-major, N = BN, M = 128
+    a.idesc = mma_idesc_f16(!f16, 128, p.BN);
+    a.out_f16 = f16;
     a.tmem_cols = (uint32_t)p.tmem_cols;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.mt, p.nt, p.splits);
@@ -765,24 +783,26 @@ static cudaError_t launch_tc(const void *X, const void *X_lo, int T, const void 
 cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K, int groups,
                            int epi, float *C, int ldc, void *Hout, void *Hout_lo, int ldh, float *scratch,
                            size_t scratch_floats, int *err, int num_sms, cudaStream_t s, int force_splits,
-                           const float *bias) {
-    return launch_tc(X, X_lo, T, W, n_feat, K, groups, epi, C, ldc, Hout, Hout_lo, ldh, scratch, scratch_floats, err,
-                     num_sms, s, force_splits, bias, nullptr);
+                           const float *bias, bool f16) {
+    return launch_tc(X, f16 ? nullptr : X_lo, T, W, n_feat, K, groups, epi, C, ldc, Hout, f16 ? nullptr : Hout_lo, ldh,
+                     scratch, scratch_floats, err, num_sms, s, force_splits, bias, nullptr, nullptr, f16);
 }
 
 cudaError_t launch_gemm_tc_resid_norm(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K,
                                       float *C, int ldc, const float *norm_w, float eps, void *hi, void *lo,
-                                      float *scratch, size_t scratch_floats, int *err, int num_sms, cudaStream_t s) {
-    const NormArgs n{norm_w, eps, static_cast<__nv_bfloat16 *>(hi), static_cast<__nv_bfloat16 *>(lo)};
-    return launch_tc(X, X_lo, T, W, n_feat, K, 1, EPI_RESID_F32, C, ldc, nullptr, nullptr, 0, scratch, scratch_floats,
-                     err, num_sms, s, 0, nullptr, nullptr, &n);
+                                      float *scratch, size_t scratch_floats, int *err, int num_sms, cudaStream_t s,
+                                      bool f16) {
+    const NormArgs n{norm_w, eps, static_cast<__nv_bfloat16 *>(hi), f16 ? nullptr : static_cast<__nv_bfloat16 *>(lo),
+                     f16 ? 1 : 0};
+    return launch_tc(X, f16 ? nullptr : X_lo, T, W, n_feat, K, 1, EPI_RESID_F32, C, ldc, nullptr, nullptr, 0, scratch,
+                     scratch_floats, err, num_sms, s, 0, nullptr, nullptr, &n, f16);
 }
 
 cudaError_t launch_gemm_tc_qkv_rope(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K,
                                     const RopeKvArgs &r, float *scratch, size_t scratch_floats, int *err, int num_sms,
-                                    cudaStream_t s) {
-    return launch_tc(X, X_lo, T, W, n_feat, K, 1, EPI_STORE_F32, nullptr, 0, nullptr, nullptr, 0, scratch,
-                     scratch_floats, err, num_sms, s, 0, nullptr, &r);
+                                    cudaStream_t s, bool f16) {
+    return launch_tc(X, f16 ? nullptr : X_lo, T, W, n_feat, K, 1, EPI_STORE_F32, nullptr, 0, nullptr, nullptr, 0,
+                     scratch, scratch_floats, err, num_sms, s, 0, nullptr, &r, nullptr, f16);
 }
 
 }  // namespace dec

@@ -18,7 +18,8 @@ struct TcPlan {
 };
 
 // Y = X W^T for X [T, K] (bf16 rows of the prompt) and W [n_feat, K] (bf16
-// weights).  X_lo (may be null) is a second bf16 plane of the same shape with
+// weights); with f16 both are fp16 and X_lo / Hout_lo are unused (SwiGLU
+// writes one fp16 plane).  X_lo (may be null) is a second bf16 plane of the same shape with
 // X + X_lo the activation (the bf16 rounding residual): both planes enter the
 // product.  epi: EPI_STORE_F32 writes C[t][f]; EPI_RESID_F32 adds into C;
 // EPI_SWIGLU_BF16 (groups = 2, W packed in blocks of 128 gate rows + 128 up
@@ -35,7 +36,7 @@ TcPlan gemm_tc_plan(int T, int n_feat, int K, int groups, int num_sms, size_t sc
 cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K, int groups,
                            int epi, float *C, int ldc, void *Hout, void *Hout_lo, int ldh, float *scratch,
                            size_t scratch_floats, int *err, int num_sms, cudaStream_t s, int force_splits = 0,
-                           const float *bias = nullptr);
+                           const float *bias = nullptr, bool f16 = false);
 // The q|k|v projection of the prompt with the per-head Q/K RMSNorm, RoPE and
 // KV write of the rope kernel folded into the split-K reduction (one warp per
 // row and head: head_dim 128, fp16 KV).  Returns cudaErrorNotSupported (and
@@ -48,10 +49,11 @@ cudaError_t launch_gemm_tc(const void *X, const void *X_lo, int T, const void *W
 // prompt-row tile with 128-row weight tiles and n_feat <= 4096.
 cudaError_t launch_gemm_tc_resid_norm(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K,
                                       float *C, int ldc, const float *norm_w, float eps, void *hi, void *lo,
-                                      float *scratch, size_t scratch_floats, int *err, int num_sms, cudaStream_t s);
+                                      float *scratch, size_t scratch_floats, int *err, int num_sms, cudaStream_t s,
+                                      bool f16 = false);
 cudaError_t launch_gemm_tc_qkv_rope(const void *X, const void *X_lo, int T, const void *W, int n_feat, int K,
                                     const RopeKvArgs &r, float *scratch, size_t scratch_floats, int *err, int num_sms,
-                                    cudaStream_t s);
+                                    cudaStream_t s, bool f16 = false);
 void init_gemm_tc();
 bool gemm_tc_ready();
 

@@ -6,6 +6,7 @@
 // and encoder rows are concatenated (prefix | enc_out | suffix), every block
 // runs on all rows with the causal mask of qwen3_asr/model.cpp, run (key c
 // visible to query r iff c <= r), the KV of every position is written.
+#include <type_traits>
 #include "prefill.cuh"
 
 namespace dec {
@@ -25,9 +26,15 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float *x, const floa
     const float r = rsqrtf(ss / (float)H + eps);
     for (int k = threadIdx.x; k < H; k += blockDim.x) {
         const float v = xr[k] * r * w[k];
-        if constexpr (sizeof(TO) == 2) store_planes(out, out_lo, t * H + k, v);
+        if constexpr (std::is_same<TO, __half>::value) out[t * H + k] = __float2half_rn(v);
+        else if constexpr (sizeof(TO) == 2) store_planes(out, out_lo, t * H + k, v);
         else out[t * H + k] = v;
     }
+}
+
+void launch_rmsnorm_rows_f16(const float *x, const float *w, float eps, void *out, int T, int H, cudaStream_t s) {
+    if (T <= 0) return;
+    launch_pdl(k_rmsnorm_rows<__half>, dim3(T), dim3(256), 0, s, x, w, eps, (__half *)out, (__half *)nullptr, H);
 }
 
 void launch_rmsnorm_rows(const float *x, const float *w, float eps, void *out, void *out_lo, bool act_bf16, int T,
@@ -37,6 +44,19 @@ void launch_rmsnorm_rows(const float *x, const float *w, float eps, void *out, v
         launch_pdl(k_rmsnorm_rows<__nv_bfloat16>, dim3(T), dim3(256), 0, s, x, w, eps, (__nv_bfloat16 *)out,
                    (__nv_bfloat16 *)out_lo, H);
     else launch_pdl(k_rmsnorm_rows<float>, dim3(T), dim3(256), 0, s, x, w, eps, (float *)out, (float *)nullptr, H);
+}
+
+// ------------------------------------------------------------------ bf16 -> fp16 (weights, once)
+__global__ void k_bf16_to_f16(const __nv_bfloat16 *src, __half *dst, size_t n) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = __float2half_rn(__bfloat162float(src[i]));
+}
+
+void launch_bf16_to_f16(const void *src, void *dst, size_t n, cudaStream_t s) {
+    if (n == 0) return;
+    const size_t blocks = (n + 255) / 256;
+    k_bf16_to_f16<<<(unsigned)(blocks < 65535 * 8 ? blocks : 65535 * 8), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16 *>(src), static_cast<__half *>(dst), n);
 }
 
 // ------------------------------------------------------------------ two bf16 planes

@@ -6,6 +6,10 @@ namespace dec {
 
 // rows of x (float32 [T, H]) -> RMSNorm(x) * w in bf16 (act_bf16; out_lo, if not
 // null, receives the bf16 rounding residual) or float32
+// fp16 copy of bf16 values (the prompt GEMMs' fp16 weights)
+void launch_bf16_to_f16(const void *src, void *dst, size_t n, cudaStream_t s);
+// RMSNorm of rows into one fp16 plane (operands of the fp16 prompt GEMMs)
+void launch_rmsnorm_rows_f16(const float *x, const float *w, float eps, void *out, int T, int H, cudaStream_t s);
 void launch_rmsnorm_rows(const float *x, const float *w, float eps, void *out, void *out_lo, bool act_bf16, int T,
                          int H, cudaStream_t s);
 
@@ -49,6 +53,7 @@ struct AttnPrefillTcArgs {
     const int4 *tiles;
     const int32_t *kv_off, *vt_col;
     __nv_bfloat16 *o, *o_lo;   // [rows][nq d] two bf16 planes (o_lo may be null)
+    int o_f16;                 // 1: o holds one fp16 plane instead (o_lo unused)
     int *err;                  // device error code if a bounded wait expires
     int q_rows, nq, nkv, slots, vt_ld;
     float scale;
