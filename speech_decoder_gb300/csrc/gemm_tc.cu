@@ -85,6 +85,37 @@ __device__ __forceinline__ void epi_store(const TcArgs &a, int f, int t, float v
     }
 }
 
+// Residual epilogue of one chunk of N tokens [t0, t0 + N): feature row f and,
+// with two_rows, row f + 128.  Every residual load is issued before the
+// first store.  Written as `*c += v` per element, each load would wait for
+// the previous element's store (the compiler cannot rule out that the two
+// addresses alias), one memory round trip per element in turn.
+template <int N>
+__device__ __forceinline__ void resid_load(const TcArgs &a, int f, int t0, bool two_rows, float (&x0)[N],
+                                           float (&x1)[N]) {
+    const bool in0 = f < a.n_feat, in1 = two_rows && f + 128 < a.n_feat;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        const int t = t0 + j;
+        const float *c = a.C + (size_t)t * a.ldc + f;
+        x0[j] = t < a.T && in0 ? __ldcg(c) : 0.f;
+        x1[j] = t < a.T && in1 ? __ldcg(c + 128) : 0.f;
+    }
+}
+template <int N>
+__device__ __forceinline__ void resid_store(const TcArgs &a, int f, int t0, bool two_rows, const float (&x0)[N],
+                                            const float (&x1)[N], const float (&v)[N], const float (&u)[N]) {
+    const bool in0 = f < a.n_feat, in1 = two_rows && f + 128 < a.n_feat;
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+        const int t = t0 + j;
+        if (t >= a.T) break;
+        float *c = a.C + (size_t)t * a.ldc + f;
+        if (in0) c[0] = x0[j] + v[j];
+        if (in1) c[128] = x1[j] + u[j];
+    }
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmB2, TcArgs a) {
@@ -201,10 +232,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int c = 0;
             // two groups outside SwiGLU: rows m0 + 128 + r in the second TMEM range
             const bool pair = a.groups == 2 && a.epi != EPI_SWIGLU_BF16;
+            const bool resid = a.epi == EPI_RESID_F32;
             for (; c + 32 <= a.BN; c += 32) {
-                float v[32], u[32];
+                float v[32], u[32], x0[32], x1[32];
+                if (resid) resid_load<32>(a, f, n0 + c, pair, x0, x1);
                 tmem_ld32(tq + c, v);
                 if (a.groups == 2) tmem_ld32(tq + a.BN + c, u);
+                if (resid) {
+                    resid_store<32>(a, f, n0 + c, pair, x0, x1, v, u);
+                    continue;
+                }
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     epi_store(a, f, n0 + c + j, v[j], a.groups == 2 ? u[j] : 0.f);
@@ -212,9 +249,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             for (; c < a.BN; c += 16) {
-                float v[16], u[16];
+                float v[16], u[16], x0[16], x1[16];
+                if (resid) resid_load<16>(a, f, n0 + c, pair, x0, x1);
                 tmem_ld16(tq + c, v);
                 if (a.groups == 2) tmem_ld16(tq + a.BN + c, u);
+                if (resid) {
+                    resid_store<16>(a, f, n0 + c, pair, x0, x1, v, u);
+                    continue;
+                }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     epi_store(a, f, n0 + c + j, v[j], a.groups == 2 ? u[j] : 0.f);
@@ -373,12 +415,14 @@ __global__ void __launch_bounds__(1024) k_splitk_resid_norm(TcArgs a, NormArgs n
 
 // ------------------------------------------------------------------ persistent form (long prompts)
 // One CTA per SM walks output tiles of 256 weight rows (two 128-row MMA groups:
-// gate and up rows for SwiGLU) x 128 prompt rows, the tiles of one prompt-row
+// gate and up rows for SwiGLU) x BN prompt rows, the tiles of one prompt-row
 // block consecutively (its activation panel stays in L2 while the weights
-// pass).  The accumulator is double-buffered in TMEM (columns 0-255 and
-// 256-511): the epilogue warps drain tile i while the MMA warp runs tile i + 1,
-// and the TMA producer runs ahead through a ring that spans tile boundaries.
-constexpr int kPtBN = 128;              // prompt rows per tile (fewer for a short batch of rows: a.BN)
+// pass); the TMA producer runs ahead through a ring that spans tile
+// boundaries.  Up to BN = 128 the accumulator is double-buffered in TMEM
+// (columns 0-255 and 256-511): the epilogue warps drain tile i while the MMA
+// warp runs tile i + 1.  With BN = 256 one accumulator fills the 512 columns
+// and the MMAs of tile i + 1 start once the epilogue has drained tile i.
+constexpr int kPtBN = 128;              // a batch of fewer rows is short: one prompt-row tile of its own size
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_gemm_tc_pt(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -387,8 +431,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = a.n_stages;
-    const int BN = a.BN;                          // a multiple of 16, at most kPtBN
-    const uint32_t a_bytes = 2u * 16384u, b_bytes = (uint32_t)BN * 128u;
+    const int BN = a.BN;                          // a multiple of 16, at most 256
+    constexpr int G = 2;                          // 128-row weight groups per tile (SwiGLU: gate, up)
+    const uint32_t a_bytes = (uint32_t)G * 16384u, b_bytes = (uint32_t)BN * 128u;
     const uint32_t stage_bytes = a_bytes + (uint32_t)a.planes * b_bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)S * stage_bytes);
     uint64_t *empty = full + S;
@@ -400,10 +445,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // 256-row weight tiles; the last may be half outside the matrix (its
     // rows read as zeros, its outputs skipped)
-    const int MT = (a.n_feat * (a.epi == EPI_SWIGLU_BF16 ? 2 : 1) + 255) / 256;
+    const int MT = (a.n_feat * (a.epi == EPI_SWIGLU_BF16 ? 2 : 1) + 128 * G - 1) / (128 * G);
     const int NT = (a.T + BN - 1) / BN;
     const int tiles = MT * NT;
     const int KT = a.k_tiles;
+    // accumulators that fit TMEM's 512 columns (2 BN columns each): two up to
+    // BN = 128 (tile i's epilogue overlaps tile i + 1's MMAs), else one
+    const int nbuf = 2 * G * BN <= 512 ? 2 : 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -435,7 +483,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int it = 0;
         bool waited = false;
         for (int t = blockIdx.x; t < tiles && !*(volatile int *)&abort_s; t += gridDim.x) {
-            const int m0 = (t % MT) * 256, n0 = (t / MT) * BN;
+            const int m0 = (t % MT) * 128 * G, n0 = (t / MT) * BN;
             for (int kt = 0; kt < KT; ++kt, ++it) {
                 const int s = it % S;
                 if (it >= S && !ptx::mbar_wait_bounded(&empty[s], ((it / S) - 1) & 1, kTcPolls)) {
@@ -461,14 +509,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ---------------------------------------------------------- MMA issuer
         int it = 0, tl = 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++tl) {
-            const int buf = tl & 1;
-            if (tl >= 2 && !ptx::mbar_wait_bounded(&tempty[buf], ((tl >> 1) - 1) & 1, kTcPolls)) {
+            const int buf = tl % nbuf, use = tl / nbuf;
+            if (tl >= nbuf && !ptx::mbar_wait_bounded(&tempty[buf], (use - 1) & 1, kTcPolls)) {
                 tc_report(a.err, 15);
                 abort_s = 1;
             }
             if (*(volatile int *)&abort_s) break;
             tc_fence_after();
-            const uint32_t acc = tmem + (uint32_t)(buf * 2 * BN);
+            const uint32_t acc = tmem + (uint32_t)(buf * G * BN);
             for (int kt = 0; kt < KT; ++kt, ++it) {
                 const int s = it % S;
                 if (!ptx::mbar_wait_bounded(&full[s], (it / S) & 1, kTcPolls)) {
@@ -483,7 +531,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int pl = 0; pl < a.planes; ++pl) {
                         const uint64_t bdesc = sw128_desc(bbase + pl * b_bytes + kk * 32);
 #pragma unroll
-                        for (int g = 0; g < 2; ++g)
+                        for (int g = 0; g < G; ++g)
                             mma_f16(acc + (uint32_t)(g * BN), sw128_desc(abase + g * 16384 + kk * 32), bdesc,
                                     a.idesc, (kt | kk | pl) != 0);
                     }
@@ -500,8 +548,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int r = 32 * q + lane;                    // row within a 128-row group
         int tl = 0;
         for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++tl) {
-            const int buf = tl & 1;
-            const bool ok = ptx::mbar_wait_bounded(&tfull[buf], (tl >> 1) & 1, kTcPolls);
+            const int buf = tl % nbuf, use = tl / nbuf;
+            const bool ok = ptx::mbar_wait_bounded(&tfull[buf], use & 1, kTcPolls);
             if (!ok && lane == 0) {
                 tc_report(a.err, 17);
                 abort_s = 1;
@@ -510,28 +558,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (__any_sync(0xffffffffu, !ok || *(volatile int *)&abort_s)) break;
             tc_fence_after();
             const int mt = t % MT, n0 = (t / MT) * BN;
-            const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * 2 * BN);
+            const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * G * BN);
             const bool swiglu = a.epi == EPI_SWIGLU_BF16;
-            const int f = swiglu ? mt * 128 + r : mt * 256 + r;
+            const int f = swiglu ? mt * 128 + r : mt * 128 * G + r;
+            const bool resid = a.epi == EPI_RESID_F32;
+            const bool two = G == 2;                     // the tile's second 128 rows in columns BN ..
+            const bool pair = two && !swiglu;            // ... are rows f + 128 (SwiGLU: the up rows)
             int c = 0;
             for (; c + 32 <= BN; c += 32) {
-                float v[32], u[32];
+                float v[32], u[32], x0[32], x1[32];
+                if (resid) resid_load<32>(a, f, n0 + c, pair, x0, x1);
                 tmem_ld32(tq + c, v);
-                tmem_ld32(tq + BN + c, u);
+                if (two) tmem_ld32(tq + BN + c, u);
+                if (resid) {
+                    resid_store<32>(a, f, n0 + c, pair, x0, x1, v, u);
+                    continue;
+                }
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    epi_store(a, f, n0 + c + j, v[j], u[j]);
-                    if (!swiglu) epi_store(a, f + 128, n0 + c + j, u[j], 0.f);
+                    epi_store(a, f, n0 + c + j, v[j], two ? u[j] : 0.f);
+                    if (pair) epi_store(a, f + 128, n0 + c + j, u[j], 0.f);
                 }
             }
             if (c < BN) {                                // a 16-column remainder
-                float v[16], u[16];
+                float v[16], u[16], x0[16], x1[16];
+                if (resid) resid_load<16>(a, f, n0 + c, pair, x0, x1);
                 tmem_ld16(tq + c, v);
-                tmem_ld16(tq + BN + c, u);
+                if (two) tmem_ld16(tq + BN + c, u);
+                if (resid) {
+                    resid_store<16>(a, f, n0 + c, pair, x0, x1, v, u);
+                } else {
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    epi_store(a, f, n0 + c + j, v[j], u[j]);
-                    if (!swiglu) epi_store(a, f + 128, n0 + c + j, u[j], 0.f);
+                    for (int j = 0; j < 16; ++j) {
+                        epi_store(a, f, n0 + c + j, v[j], two ? u[j] : 0.f);
+                        if (pair) epi_store(a, f + 128, n0 + c + j, u[j], 0.f);
+                    }
                 }
             }
             tc_fence_before();
@@ -584,12 +645,36 @@ void init_gemm_tc() {
 
 bool gemm_tc_ready() { return g_tc_ready; }
 
-// persistent form: stages of 256 weight rows + planes x BN prompt rows of 64 K each
-static int pt_bn(int T) { return T >= kPtBN ? kPtBN : (T + 15) / 16 * 16; }
-static int pt_stages(int planes, int BN) {
-    const int stage = 2 * 16384 + planes * BN * 128;
-    const int n = (g_pt_max_smem - 1024 - 256) / stage;
-    return n > 6 ? 6 : n;
+// Persistent form: tiles of 256 weight rows x BN prompt rows, ring stages of
+// 64 K.  Long prompts take BN = 256 (128 x 256 MMAs: fewer shared-memory
+// operand bytes per FLOP than 128 x 128, one accumulator in TMEM) except in
+// the gate|up projection, whose SwiGLU epilogue gains more from overlapping
+// the next tile's MMAs (BN = 128, two accumulators).  Run-time options, BN a
+// multiple of 16 up to 256: SPEECH_DECODER_PT_BN (default 256),
+// SPEECH_DECODER_PT_BN_GU (gate|up, default 128) and SPEECH_DECODER_PT_STAGES
+// (ring stages at most, 3 to 6; default 6).
+static int env_int(const char *name, int dflt, int lo, int hi) {
+    const char *e = std::getenv(name);
+    const int v = e ? std::atoi(e) : dflt;
+    return v < lo ? lo : (v > hi ? hi : v);
+}
+struct PtShape {
+    int BN, stages;
+    long long tiles;
+    size_t smem;
+};
+static PtShape pt_shape(int T, int n_feat, int epi, int planes) {
+    static const int bn_pr = env_int("SPEECH_DECODER_PT_BN", 256, 16, 256) / 16 * 16;
+    static const int bn_gu = env_int("SPEECH_DECODER_PT_BN_GU", 128, 16, 256) / 16 * 16;
+    static const int cap = env_int("SPEECH_DECODER_PT_STAGES", 6, 3, 6);
+    PtShape p{};
+    const int bn = epi == EPI_SWIGLU_BF16 ? bn_gu : bn_pr;
+    p.BN = T >= bn ? bn : (T + 15) / 16 * 16;
+    const int stage = 2 * 16384 + planes * p.BN * 128;
+    p.stages = std::min(cap, (g_pt_max_smem - 1024 - 256) / stage);
+    p.tiles = (long long)((n_feat + 255) / 256) * ((T + p.BN - 1) / p.BN);
+    p.smem = (size_t)p.stages * stage + 1024 + 256;
+    return p;
 }
 
 static bool make_map(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t K, uint32_t box_rows, bool f16 = false) {
@@ -650,10 +735,9 @@ static bool use_persistent(int T, int n_feat, int K, int groups, int epi, int pl
                            int force_splits) {
     if (!g_tc_ready || g_pt_max_smem <= 0 || force_splits > 0 || K % kBK || n_feat % 128) return false;
     if (epi == EPI_SWIGLU_BF16 && (groups != 2 || n_feat % 256)) return false;
-    const int BN = pt_bn(T);
-    if (pt_stages(planes, BN) < 3) return false;
-    const long long tiles = (long long)((n_feat + 255) / 256) * ((T + BN - 1) / BN);
-    return (T >= 1024 || BN < kPtBN) && tiles >= num_sms;
+    const PtShape p = pt_shape(T, n_feat, epi, planes);
+    if (p.stages < 3) return false;
+    return (T >= 1024 || p.BN < kPtBN) && p.tiles >= num_sms;
 }
 
 static bool pt_disabled() {
@@ -676,7 +760,8 @@ static cudaError_t launch_tc(const void *X, const void *X_lo, int T, const void 
     const int planes = X_lo ? 2 : 1;
     if (!pt_disabled() && use_persistent(T, n_feat, K, groups, epi, planes, num_sms, force_splits)) {
         if (rope || norm) return cudaErrorNotSupported;
-        const int BN = pt_bn(T);
+        const PtShape ps = pt_shape(T, n_feat, epi, planes);
+        const int BN = ps.BN;
         CUtensorMap mA, mB, mB2;
         if (!make_map(&mA, W, (uint64_t)n_feat, (uint64_t)K, 256u, f16) ||
             !make_map(&mB, X, (uint64_t)T, (uint64_t)K, (uint32_t)BN, f16) ||
@@ -689,7 +774,7 @@ static cudaError_t launch_tc(const void *X, const void *X_lo, int T, const void 
         a.groups = 2;
         a.planes = planes;
         a.BN = BN;
-        a.n_stages = pt_stages(planes, BN);
+        a.n_stages = ps.stages;
         a.k_tiles = K / kBK;
         a.splits = 1;
         a.kt_per_split = a.k_tiles;
@@ -704,11 +789,10 @@ static cudaError_t launch_tc(const void *X, const void *X_lo, int T, const void 
         a.idesc = mma_idesc_f16(!f16, 128, BN);
         a.out_f16 = f16;
         a.tmem_cols = 512;
-        const int tiles = ((n_feat + 255) / 256) * ((T + BN - 1) / BN);
         cudaLaunchConfig_t cfg{};
-        cfg.gridDim = dim3(std::min(num_sms, tiles));
+        cfg.gridDim = dim3((unsigned)std::min<long long>(num_sms, ps.tiles));
         cfg.blockDim = dim3(kTcThreads);
-        cfg.dynamicSmemBytes = (size_t)a.n_stages * (2 * 16384 + planes * BN * 128) + 1024 + 256;
+        cfg.dynamicSmemBytes = ps.smem;
         cfg.stream = s;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -32,14 +32,76 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows(const float *x, const floa
     }
 }
 
+// One warp per row for H = 128 NJ: lane L holds float4 groups L + 32 j of
+// the row in registers, so all of a row's loads are in flight together, the
+// sum of squares is a shuffle reduction and no block barrier is needed.
+template <typename TO, int NJ>
+__global__ void __launch_bounds__(256) k_rmsnorm_rows_w(const float *x, const float *w, float eps, TO *out,
+                                                        TO *out_lo, int T) {
+    constexpr int H = NJ * 128;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int lane = threadIdx.x & 31;
+    const size_t t = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= (size_t)T) return;
+    const float4 *xr = reinterpret_cast<const float4 *>(x + t * H);
+    float4 v[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) v[j] = xr[lane + 32 * j];
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+    ss = warp_sum(ss);
+    const float r = rsqrtf(ss / (float)H + eps);
+    const float4 *w4 = reinterpret_cast<const float4 *>(w);
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        const float4 g = w4[lane + 32 * j];
+        const float y0 = v[j].x * r * g.x, y1 = v[j].y * r * g.y, y2 = v[j].z * r * g.z, y3 = v[j].w * r * g.w;
+        const size_t o = t * H + 4 * (size_t)(lane + 32 * j);
+        if constexpr (std::is_same<TO, __half>::value) {
+            __half2 *hp = reinterpret_cast<__half2 *>(out + o);
+            hp[0] = __floats2half2_rn(y0, y1);
+            hp[1] = __floats2half2_rn(y2, y3);
+        } else if constexpr (sizeof(TO) == 2) {
+            store_planes(out, out_lo, o, y0);
+            store_planes(out, out_lo, o + 1, y1);
+            store_planes(out, out_lo, o + 2, y2);
+            store_planes(out, out_lo, o + 3, y3);
+        } else {
+            *reinterpret_cast<float4 *>(out + o) = make_float4(y0, y1, y2, y3);
+        }
+    }
+}
+
+// the warp-per-row form for H in {512, 1024, 2048, 4096} with 16-byte aligned
+// rows; false: not applicable
+template <typename TO>
+static bool rmsnorm_rows_w(const float *x, const float *w, float eps, TO *out, TO *out_lo, int T, int H,
+                           cudaStream_t s) {
+    if (((uintptr_t)x | (uintptr_t)w | (uintptr_t)out | (uintptr_t)out_lo) % 16) return false;
+    const dim3 grid((T + 7) / 8), block(256);
+    switch (H) {
+    case 512: launch_pdl(k_rmsnorm_rows_w<TO, 4>, grid, block, 0, s, x, w, eps, out, out_lo, T); return true;
+    case 1024: launch_pdl(k_rmsnorm_rows_w<TO, 8>, grid, block, 0, s, x, w, eps, out, out_lo, T); return true;
+    case 2048: launch_pdl(k_rmsnorm_rows_w<TO, 16>, grid, block, 0, s, x, w, eps, out, out_lo, T); return true;
+    case 4096: launch_pdl(k_rmsnorm_rows_w<TO, 32>, grid, block, 0, s, x, w, eps, out, out_lo, T); return true;
+    default: return false;
+    }
+}
+
 void launch_rmsnorm_rows_f16(const float *x, const float *w, float eps, void *out, int T, int H, cudaStream_t s) {
     if (T <= 0) return;
+    if (rmsnorm_rows_w(x, w, eps, (__half *)out, (__half *)nullptr, T, H, s)) return;
     launch_pdl(k_rmsnorm_rows<__half>, dim3(T), dim3(256), 0, s, x, w, eps, (__half *)out, (__half *)nullptr, H);
 }
 
 void launch_rmsnorm_rows(const float *x, const float *w, float eps, void *out, void *out_lo, bool act_bf16, int T,
                          int H, cudaStream_t s) {
     if (T <= 0) return;
+    if (act_bf16 ? rmsnorm_rows_w(x, w, eps, (__nv_bfloat16 *)out, (__nv_bfloat16 *)out_lo, T, H, s)
+                 : rmsnorm_rows_w(x, w, eps, (float *)out, (float *)nullptr, T, H, s))
+        return;
     if (act_bf16)
         launch_pdl(k_rmsnorm_rows<__nv_bfloat16>, dim3(T), dim3(256), 0, s, x, w, eps, (__nv_bfloat16 *)out,
                    (__nv_bfloat16 *)out_lo, H);
@@ -166,51 +228,99 @@ void launch_swiglu(const float *gu, void *h, void *h_lo, bool act_bf16, int T, i
 }
 
 // ------------------------------------------------------------------ Q/K norm + RoPE + KV write
-// One warp per (row, head): heads [0, nq) are queries, [nq, nq + nkv) are KV
-// heads (the warp also copies that head's V).
+// One CTA per (16 prompt rows, head): heads [0, nq) are queries, [nq, nq + nkv)
+// keys, [nq + nkv, nq + 2 nkv) values; warp w takes rows w and w + 8, lane L
+// the features L PL .. L PL + PL - 1 of the row's head.  Value heads also
+// write V^T: the 16 rows are staged in shared memory and each V^T row gets
+// its 16 consecutive columns as 16-byte stores (one element per store would
+// touch a whole 32-byte sector for 2 bytes).
+constexpr int kRopeRows = 16;
+
+// PL consecutive features: one 16- or 8-byte load, one 8- or 4-byte store
+// of fp16 values
+template <int PL>
+__device__ __forceinline__ void load_lane(const float *src, float (&v)[PL]) {
+    if constexpr (PL == 4) {
+        const float4 x = *reinterpret_cast<const float4 *>(src);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    } else if constexpr (PL == 2) {
+        const float2 x = *reinterpret_cast<const float2 *>(src);
+        v[0] = x.x; v[1] = x.y;
+    } else {
+#pragma unroll
+        for (int e = 0; e < PL; ++e) v[e] = src[e];
+    }
+}
+template <typename TKV, int PL>
+__device__ __forceinline__ void store_lane(TKV *dst, const float (&v)[PL]) {
+    if constexpr (std::is_same<TKV, __half>::value && PL == 4) {
+        const __half2 lo = __floats2half2_rn(v[0], v[1]), hi = __floats2half2_rn(v[2], v[3]);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const unsigned *>(&lo);
+        pk.y = *reinterpret_cast<const unsigned *>(&hi);
+        *reinterpret_cast<uint2 *>(dst) = pk;
+    } else if constexpr (std::is_same<TKV, __half>::value && PL == 2) {
+        *reinterpret_cast<__half2 *>(dst) = __floats2half2_rn(v[0], v[1]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < PL; ++e) dst[e] = from_f32<TKV>(v[e]);
+    }
+}
+
 template <typename TKV, int D>
 __global__ void __launch_bounds__(256) k_qk_rope_kv(RopeKvArgs a) {
     constexpr int PL = D / 32;
-    const int lane = threadIdx.x & 31;
-    const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-    const int nh = a.nq + a.nkv;
-    if (gw >= (long long)a.T * nh) return;
-    const int t = (int)(gw / nh), hh = (int)(gw % nh);
-    const int pos = a.row_pos[t];
+    __shared__ TKV tile[kRopeRows][D + 8];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int hh = blockIdx.y, t0 = blockIdx.x * kRopeRows;
     const size_t ldq = (size_t)(a.nq + 2 * a.nkv) * D;
-    const float *row = a.qkv + (size_t)t * ldq;
-    const float2 *rope_row = a.rope + (size_t)pos * (D / 2);
-    float v[PL];
-    if (hh < a.nq) {
+    const bool is_v = hh >= a.nq + a.nkv;
 #pragma unroll
-        for (int e = 0; e < PL; ++e) v[e] = row[(size_t)hh * D + lane * PL + e];
-        norm_rope_lane<PL>(v, a.qn_w, a.eps, D, rope_row, lane);
-        TKV *q = reinterpret_cast<TKV *>(a.q_out) + ((size_t)t * a.nq + hh) * D + lane * PL;
+    for (int i = 0; i < kRopeRows / 8; ++i) {
+        const int tr = warp + 8 * i, t = t0 + tr;
+        if (t >= a.T) break;                                   // warp-uniform
+        float v[PL];
+        load_lane<PL>(a.qkv + (size_t)t * ldq + (size_t)hh * D + lane * PL, v);
+        if (!is_v) {
+            const bool is_q = hh < a.nq;
+            const float2 *rope_row = a.rope + (size_t)a.row_pos[t] * (D / 2);
+            norm_rope_lane<PL>(v, is_q ? a.qn_w : a.kn_w, a.eps, D, rope_row, lane);
+            TKV *dst = is_q ? reinterpret_cast<TKV *>(a.q_out) + ((size_t)t * a.nq + hh) * D
+                            : reinterpret_cast<TKV *>(a.Kc) + ((size_t)(hh - a.nq) * a.slots + a.row_slot[t]) * D;
+            store_lane<TKV, PL>(dst + lane * PL, v);
+        } else {
+            const int g = hh - a.nq - a.nkv;
+            store_lane<TKV, PL>(reinterpret_cast<TKV *>(a.Vc) + ((size_t)g * a.slots + a.row_slot[t]) * D + lane * PL, v);
+            store_lane<TKV, PL>(&tile[tr][lane * PL], v);
+        }
+    }
+    if (!is_v || !a.vt) return;                                // CTA-uniform
+    __syncthreads();
+    if (threadIdx.x >= D) return;
+    const int e = threadIdx.x, g = hh - a.nq - a.nkv;
+    TKV *dst = reinterpret_cast<TKV *>(a.vt) + (size_t)(g * D + e) * a.vt_ld;
 #pragma unroll
-        for (int e = 0; e < PL; ++e) q[e] = from_f32<TKV>(v[e]);
-    } else {
-        const int g = hh - a.nq;
-        const size_t slot = ((size_t)g * a.slots + a.row_slot[t]) * D + lane * PL;
+    for (int h8 = 0; h8 < kRopeRows; h8 += 8) {
+        const int tb = t0 + h8;
+        if (tb >= a.T) break;
+        const int c0 = a.row_vtcol[tb];
+        bool vec = sizeof(TKV) == 2 && tb + 7 < a.T && c0 % 8 == 0;
+        for (int k = 1; vec && k < 8; ++k) vec = a.row_vtcol[tb + k] == c0 + k;
+        if (vec) {
+            uint4 pk;
+            uint16_t *h = reinterpret_cast<uint16_t *>(&pk);
 #pragma unroll
-        for (int e = 0; e < PL; ++e) v[e] = row[(size_t)(a.nq + g) * D + lane * PL + e];
-        norm_rope_lane<PL>(v, a.kn_w, a.eps, D, rope_row, lane);
-        TKV *K = reinterpret_cast<TKV *>(a.Kc) + slot;
-        TKV *V = reinterpret_cast<TKV *>(a.Vc) + slot;
-        TKV *vt = a.vt ? reinterpret_cast<TKV *>(a.vt) + (size_t)(g * D + lane * PL) * a.vt_ld + a.row_vtcol[t] : nullptr;
-#pragma unroll
-        for (int e = 0; e < PL; ++e) {
-            K[e] = from_f32<TKV>(v[e]);
-            const TKV x = from_f32<TKV>(row[(size_t)(a.nq + a.nkv + g) * D + lane * PL + e]);
-            V[e] = x;
-            if (vt) vt[(size_t)e * a.vt_ld] = x;
+            for (int k = 0; k < 8; ++k) h[k] = *reinterpret_cast<const uint16_t *>(&tile[h8 + k][e]);
+            *reinterpret_cast<uint4 *>(dst + c0) = pk;
+        } else {
+            for (int k = 0; k < 8 && tb + k < a.T; ++k) dst[a.row_vtcol[tb + k]] = tile[h8 + k][e];
         }
     }
 }
 
 void launch_qk_rope_kv(bool kv_f16, const RopeKvArgs &a, cudaStream_t s) {
     if (a.T <= 0) return;
-    const long long warps = (long long)a.T * (a.nq + a.nkv);
-    const int grid = (int)((warps + 7) / 8);
+    const dim3 grid((a.T + kRopeRows - 1) / kRopeRows, a.nq + 2 * a.nkv);
     if (kv_f16) {
         if (a.d == 128) k_qk_rope_kv<__half, 128><<<grid, 256, 0, s>>>(a);
         else k_qk_rope_kv<__half, 64><<<grid, 256, 0, s>>>(a);
