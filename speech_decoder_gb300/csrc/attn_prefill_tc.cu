@@ -78,8 +78,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ Sync sy;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int4 tile = a.tiles[blockIdx.x];      // (first global row, first position, rows, item)
-    const int h = blockIdx.y, g = h / (a.nq / a.nkv);
+    const int4 tile = a.tiles[blockIdx.y];      // (first global row, first position, rows, item)
+    const int h = blockIdx.x, g = h / (a.nq / a.nkv);
     const int row0 = tile.x, pos0 = tile.y, n_rows = tile.z, item = tile.w;
     const int kv_off = a.kv_off[item], vt_col = a.vt_col[item];
     const int n_kt = (pos0 + n_rows + kBK - 1) / kBK;   // key tiles up to the causal limit
@@ -362,7 +362,11 @@ cudaError_t launch_attn_prefill_tc(const AttnPrefillTcArgs &a, int n_tiles, cuda
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
-    dim3 grid(n_tiles, a.nq);
+    // heads vary fastest: blocks are dispatched in index order, so every
+    // head's longest query tiles (the tile list is sorted by causal length)
+    // start before any head's short ones and the grid ends on short tiles
+    if (n_tiles > 65535) return cudaErrorInvalidValue;
+    dim3 grid(a.nq, n_tiles);
     k_attn_prefill_tc<<<grid, kThreads, Smem::bytes + 1024, s>>>(mQ, mK, mVt, a);
     return cudaPeekAtLastError();
 }

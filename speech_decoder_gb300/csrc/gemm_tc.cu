@@ -116,6 +116,11 @@ __device__ __forceinline__ void resid_store(const TcArgs &a, int f, int t0, bool
     }
 }
 
+// kResid: the residual epilogue of one split (its own instance, so that the
+// residual values' registers do not raise the other instances' count: a
+// CTA with fewer registers shares its SM with more of the preceding
+// kernel's CTAs under programmatic launch)
+template <bool kResid>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
               const __grid_constant__ CUtensorMap tmB2, TcArgs a) {
@@ -232,16 +237,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int c = 0;
             // two groups outside SwiGLU: rows m0 + 128 + r in the second TMEM range
             const bool pair = a.groups == 2 && a.epi != EPI_SWIGLU_BF16;
-            const bool resid = a.epi == EPI_RESID_F32;
+            if (kResid) {
+                // 16 columns at a time: the residual values live next to the
+                // accumulator values
+                for (; c < a.BN; c += 16) {
+                    float v[16], u[16], x0[16], x1[16];
+                    resid_load<16>(a, f, n0 + c, pair, x0, x1);
+                    tmem_ld16(tq + c, v);
+                    if (a.groups == 2) tmem_ld16(tq + a.BN + c, u);
+                    resid_store<16>(a, f, n0 + c, pair, x0, x1, v, u);
+                }
+            }
             for (; c + 32 <= a.BN; c += 32) {
-                float v[32], u[32], x0[32], x1[32];
-                if (resid) resid_load<32>(a, f, n0 + c, pair, x0, x1);
+                float v[32], u[32];
                 tmem_ld32(tq + c, v);
                 if (a.groups == 2) tmem_ld32(tq + a.BN + c, u);
-                if (resid) {
-                    resid_store<32>(a, f, n0 + c, pair, x0, x1, v, u);
-                    continue;
-                }
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     epi_store(a, f, n0 + c + j, v[j], a.groups == 2 ? u[j] : 0.f);
@@ -249,14 +259,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             for (; c < a.BN; c += 16) {
-                float v[16], u[16], x0[16], x1[16];
-                if (resid) resid_load<16>(a, f, n0 + c, pair, x0, x1);
+                float v[16], u[16];
                 tmem_ld16(tq + c, v);
                 if (a.groups == 2) tmem_ld16(tq + a.BN + c, u);
-                if (resid) {
-                    resid_store<16>(a, f, n0 + c, pair, x0, x1, v, u);
-                    continue;
-                }
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     epi_store(a, f, n0 + c + j, v[j], a.groups == 2 ? u[j] : 0.f);
@@ -424,6 +429,7 @@ __global__ void __launch_bounds__(1024) k_splitk_resid_norm(TcArgs a, NormArgs n
 // and the MMAs of tile i + 1 start once the epilogue has drained tile i.
 constexpr int kPtBN = 128;              // a batch of fewer rows is short: one prompt-row tile of its own size
 
+template <bool kResid>   // the residual epilogue (o, down) as its own instance, as in k_gemm_tc
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_gemm_tc_pt(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                  const __grid_constant__ CUtensorMap tmB2, TcArgs a) {
@@ -561,19 +567,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(buf * G * BN);
             const bool swiglu = a.epi == EPI_SWIGLU_BF16;
             const int f = swiglu ? mt * 128 + r : mt * 128 * G + r;
-            const bool resid = a.epi == EPI_RESID_F32;
             const bool two = G == 2;                     // the tile's second 128 rows in columns BN ..
             const bool pair = two && !swiglu;            // ... are rows f + 128 (SwiGLU: the up rows)
             int c = 0;
+            if (kResid) {
+                // 16 columns at a time (BN is a multiple of 16): the residual
+                // values live next to the accumulator values
+                for (; c < BN; c += 16) {
+                    float v[16], u[16], x0[16], x1[16];
+                    resid_load<16>(a, f, n0 + c, pair, x0, x1);
+                    tmem_ld16(tq + c, v);
+                    if (two) tmem_ld16(tq + BN + c, u);
+                    resid_store<16>(a, f, n0 + c, pair, x0, x1, v, u);
+                }
+            }
             for (; c + 32 <= BN; c += 32) {
-                float v[32], u[32], x0[32], x1[32];
-                if (resid) resid_load<32>(a, f, n0 + c, pair, x0, x1);
+                float v[32], u[32];
                 tmem_ld32(tq + c, v);
                 if (two) tmem_ld32(tq + BN + c, u);
-                if (resid) {
-                    resid_store<32>(a, f, n0 + c, pair, x0, x1, v, u);
-                    continue;
-                }
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     epi_store(a, f, n0 + c + j, v[j], two ? u[j] : 0.f);
@@ -581,18 +592,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 }
             }
             if (c < BN) {                                // a 16-column remainder
-                float v[16], u[16], x0[16], x1[16];
-                if (resid) resid_load<16>(a, f, n0 + c, pair, x0, x1);
+                float v[16], u[16];
                 tmem_ld16(tq + c, v);
                 if (two) tmem_ld16(tq + BN + c, u);
-                if (resid) {
-                    resid_store<16>(a, f, n0 + c, pair, x0, x1, v, u);
-                } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        epi_store(a, f, n0 + c + j, v[j], two ? u[j] : 0.f);
-                        if (pair) epi_store(a, f + 128, n0 + c + j, u[j], 0.f);
-                    }
+                for (int j = 0; j < 16; ++j) {
+                    epi_store(a, f, n0 + c + j, v[j], two ? u[j] : 0.f);
+                    if (pair) epi_store(a, f + 128, n0 + c + j, u[j], 0.f);
                 }
             }
             tc_fence_before();
@@ -626,15 +632,19 @@ void init_gemm_tc() {
         cudaFuncAttributes fa{};
         if (cudaGetDevice(&dev) == cudaSuccess &&
             cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) == cudaSuccess &&
-            cudaFuncGetAttributes(&fa, k_gemm_tc) == cudaSuccess) {
+            cudaFuncGetAttributes(&fa, k_gemm_tc<true>) == cudaSuccess) {
             g_max_dyn_smem = optin - (int)fa.sharedSizeBytes;
-            if (cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, g_max_dyn_smem) ==
-                cudaSuccess)
+            if (cudaFuncSetAttribute(k_gemm_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_max_dyn_smem) ==
+                    cudaSuccess &&
+                cudaFuncSetAttribute(k_gemm_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_max_dyn_smem) ==
+                    cudaSuccess)
                 g_tc_ready = true;
             cudaFuncAttributes fp{};
-            if (cudaFuncGetAttributes(&fp, k_gemm_tc_pt) == cudaSuccess) {
+            if (cudaFuncGetAttributes(&fp, k_gemm_tc_pt<true>) == cudaSuccess) {
                 g_pt_max_smem = optin - (int)fp.sharedSizeBytes;
-                if (cudaFuncSetAttribute(k_gemm_tc_pt, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                if (cudaFuncSetAttribute(k_gemm_tc_pt<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         g_pt_max_smem) != cudaSuccess ||
+                    cudaFuncSetAttribute(k_gemm_tc_pt<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          g_pt_max_smem) != cudaSuccess)
                     g_pt_max_smem = 0;
             }
@@ -799,7 +809,8 @@ static cudaError_t launch_tc(const void *X, const void *X_lo, int T, const void 
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc_pt, mA, mB, mB2, a);
+        const cudaError_t e = epi == EPI_RESID_F32 ? cudaLaunchKernelEx(&cfg, k_gemm_tc_pt<true>, mA, mB, mB2, a)
+                                                   : cudaLaunchKernelEx(&cfg, k_gemm_tc_pt<false>, mA, mB, mB2, a);
         return e != cudaSuccess ? e : cudaPeekAtLastError();
     }
     const TcPlan p = gemm_tc_plan(T, n_feat, K, groups, num_sms, scratch_floats, force_splits, planes);
@@ -848,7 +859,8 @@ static cudaError_t launch_tc(const void *X, const void *X_lo, int T, const void 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc, mA, mB, mB2, a);
+    cudaError_t e = epi == EPI_RESID_F32 && p.splits == 1 ? cudaLaunchKernelEx(&cfg, k_gemm_tc<true>, mA, mB, mB2, a)
+                                                           : cudaLaunchKernelEx(&cfg, k_gemm_tc<false>, mA, mB, mB2, a);
     if (e == cudaSuccess && norm) {
         cfg.gridDim = dim3((unsigned)T);
         cfg.blockDim = dim3((unsigned)(32 * p.mt));
