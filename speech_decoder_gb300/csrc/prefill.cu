@@ -75,11 +75,12 @@ __global__ void __launch_bounds__(256) k_rmsnorm_rows_w(const float *x, const fl
 }
 
 // the warp-per-row form for H in {512, 1024, 2048, 4096} with 16-byte aligned
-// rows; false: not applicable
+// rows, from 512 rows (fewer rows, as in a batched step's 32, would occupy a
+// handful of SMs: one CTA per row spreads them wider); false: not applicable
 template <typename TO>
 static bool rmsnorm_rows_w(const float *x, const float *w, float eps, TO *out, TO *out_lo, int T, int H,
                            cudaStream_t s) {
-    if (((uintptr_t)x | (uintptr_t)w | (uintptr_t)out | (uintptr_t)out_lo) % 16) return false;
+    if (T < 512 || ((uintptr_t)x | (uintptr_t)w | (uintptr_t)out | (uintptr_t)out_lo) % 16) return false;
     const dim3 grid((T + 7) / 8), block(256);
     switch (H) {
     case 512: launch_pdl(k_rmsnorm_rows_w<TO, 4>, grid, block, 0, s, x, w, eps, out, out_lo, T); return true;
