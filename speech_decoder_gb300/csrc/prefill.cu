@@ -233,8 +233,10 @@ void launch_swiglu(const float *gu, void *h, void *h_lo, bool act_bf16, int T, i
 // keys, [nq + nkv, nq + 2 nkv) values; warp w takes rows w and w + 8, lane L
 // the features L PL .. L PL + PL - 1 of the row's head.  Value heads also
 // write V^T: the 16 rows are staged in shared memory and each V^T row gets
-// its 16 consecutive columns as 16-byte stores (one element per store would
-// touch a whole 32-byte sector for 2 bytes).
+// its 16 columns as two 16-byte stores of 8 consecutive columns (one element
+// per store would touch a whole 32-byte sector for 2 bytes); 8 rows whose
+// columns are not consecutive from a multiple of 8 (a sequence boundary, a
+// chunk at an odd position) are written element by element.
 constexpr int kRopeRows = 16;
 
 // PL consecutive features: one 16- or 8-byte load, one 8- or 4-byte store
